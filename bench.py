@@ -1,0 +1,437 @@
+"""Benchmark of the KDA hot path on GB300.
+
+Headline (one JSON line on rank 0): packed-decode state-bytes GB/s on the serving
+decode workload (128 sequences x 32 heads, K = V = 128, fp32 state pool of 512 slots,
+state indices = column 0 of an int32 [128, 8] block table), lower_bound = -5.0.
+A step is one kda_packed_decode call over that batch. Each step addresses one of four
+disjoint sets of 128 slots in turn, so the 256 MiB a step reads were last touched
+four steps (1 GiB of state traffic) earlier: L2 (129 MB) cannot serve them.
+
+The same line carries the other rows of the path measured on their own workloads
+(chunked prefill tokens/s, spec-verify, mixed batch), the decode kernel's roofline
+against the measured HBM copy bandwidth, the fp64 oracle's throughput on the host
+cores (cpu_baseline), an end-to-end number through the public binding with host
+buffers, and the SM clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this path has) on the
+same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PREFILL_ALG_FLOPS_PER_CHUNK = None  # computed from the lengths below
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK, source="fallback")
+
+
+def prefill_alg_flops(lengths, H, K, V, C=64):
+    """Algorithmic flops of the chunked form: per (chunk of c rows, head)
+    6cKV + c^2 (3K + 2V) + c^3 / 3 (triangular products counted at half)."""
+    tot = 0
+    for L in lengths:
+        full, rem = divmod(int(L), C)
+        for c in [C] * full + ([rem] if rem else []):
+            tot += 6 * c * K * V + c * c * (3 * K + 2 * V) + c ** 3 / 3
+    return tot * H
+
+
+def prefill_min_bytes(w):
+    """q, k, v, raw_g in bf16, o out bf16, beta bf16, and each sequence's state R+W."""
+    N, H, K, V = w.N, w.H, w.K, w.V
+    per_tok = 2 * (2 * H * K + H * V) + 2 * H * K + 2 * H + 2 * H * V
+    return N * per_tok + w.num_entries * 2 * 4 * H * K * V
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_attention_state_recurrent_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, sha):
+    """dram bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel_key)
+        if ent and ent.get("source_sha") == sha:
+            return float(ent["dram_bytes_per_launch"])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from linear_attention_state_recurrent_gb300 import workloads as wl
+    from oracle import kda_oracle as ko
+    w = wl.serving_decode(-5.0)
+    sets = wl.serving_decode_index_sets(w)
+    cores = ko.max_threads()
+    for i in range(args.warmup):
+        ko.run(w, slots=sets[i % 4])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ko.run(w, slots=sets[i % 4])
+    dt = time.perf_counter() - t0
+    gbs = w.state_bytes_per_call() * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": "KDA decode state-bytes GB/s", "value": gbs,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "serving_decode 128 seqs x H=32, K=V=128, lower_bound=-5.0"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} full serving-decode calls (4096 state tiles each)"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_decode(w, sets, budget_s=10.0):
+    from oracle import kda_oracle as ko
+    cores = ko.max_threads()
+    ko.run(w, slots=sets[0])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        ko.run(w, slots=sets[n % 4])
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    return {"value": w.state_bytes_per_call() * n / dt / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} full serving-decode calls (128 seqs x 32 heads) in {dt:.1f} s, fp64, OpenMP over (seq, head)"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from linear_attention_state_recurrent_gb300 import kda
+    from linear_attention_state_recurrent_gb300 import workloads as wl
+
+    dev = f"cuda:{local}"
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    # ---- headline: serving decode ----
+    w = wl.serving_decode(-5.0)
+    dw = wl.DeviceWorkload(w, dev)
+    sets = wl.serving_decode_index_sets(w)
+    idx_dev = [torch.from_numpy(s).to(dev) for s in sets]
+    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+    hd = kda.make_heads(dw.A_log, dw.dt_bias, w.lower_bound, w.K, w.V, w.scale, w.eps)
+    states = [kda.make_state(dw.pool_view(), ix) for ix in idx_dev]
+    lib = kda.lib
+    s_ptr = ctypes.c_void_p(stream.cuda_stream)
+    call_args = [(ctypes.c_void_p(dw.mixed_qkv.data_ptr()), dw.mixed_qkv.stride(0),
+                  ctypes.c_void_p(dw.raw_g.data_ptr()), dw.raw_g.stride(0),
+                  ctypes.c_void_p(dw.raw_beta.data_ptr()), dw.raw_beta.stride(0), w.N,
+                  ctypes.byref(hd), ctypes.byref(st), ctypes.c_void_p(out.data_ptr()),
+                  out.stride(0), None, s_ptr) for st in states]
+
+    def step(i):
+        s = lib.kda_packed_decode(*call_args[i & 3])
+        if s:
+            raise RuntimeError(kda.last_error())
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_total / args.steps
+    state_bytes = w.state_bytes_per_call()
+    value = state_bytes * world * args.steps / (ms_total * 1e-3) / 1e9
+    achieved = state_bytes / (ms_step * 1e-3) / 1e9
+    sha = source_sha("kda_recurrent.cu", "kda_common.cuh")
+    traffic = ncu_traffic("recurrent_kernel<128,128> serving_decode", sha)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{pk['source']} HBM copy bandwidth (of {pk['source']})",
+                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "algorithmic_bytes_per_launch": state_bytes,
+                "kernel": "kda::recurrent_kernel<128,128>"}
+
+    # ---- end to end through the public binding with host buffers ----
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        h_qkv, h_g, h_b = pin(dw.mixed_qkv), pin(dw.raw_g), pin(dw.raw_beta)
+        h_idx = [pin(torch.from_numpy(s)) for s in sets]
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d_idx = torch.empty_like(idx_dev[0])
+        e2e_steps = min(args.steps, 2000)
+
+        def e2e_step(i):
+            dw.mixed_qkv.copy_(h_qkv, non_blocking=True)
+            dw.raw_g.copy_(h_g, non_blocking=True)
+            dw.raw_beta.copy_(h_b, non_blocking=True)
+            d_idx.copy_(h_idx[i & 3], non_blocking=True)
+            o, _ = kda.kda_packed_decode(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias,
+                                         w.lower_bound, dw.pool_view(), d_idx, scale=w.scale,
+                                         l2_eps=w.eps, out=out)
+            h_out.copy_(o, non_blocking=True)
+            stream.synchronize()
+
+        for i in range(5):
+            e2e_step(i)
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        dt = time.perf_counter() - t0
+        h2d = sum(t.numel() * t.element_size() for t in (h_qkv, h_g, h_b, h_idx[0]))
+        d2h = h_out.numel() * h_out.element_size()
+        e2e = {"value": state_bytes * e2e_steps / dt / 1e9 * world, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
+               "api": "kda.kda_packed_decode (pinned host -> device copies, call, device -> host copy, stream sync each step)"}
+
+    # ---- other rows (rank 0 only) ----
+    secondary = {}
+    if rank == 0 and not args.no_secondary:
+        secondary = measure_secondary(torch, kda, wl, dev, stream, pk)
+
+    del dw, states, call_args
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_decode(w, sets)
+
+    if rank == 0:
+        line = {"metric": "KDA decode state-bytes GB/s", "value": value, "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": "serving decode: 128 seqs x H=32 heads, K=V=128, fp32 pool "
+                                       "512 slots (1 GiB), state_indices = column 0 of an int32 "
+                                       "[128,8] block table (stride 8), lower_bound=-5.0",
+                           "l2": "inputs larger than L2: steps rotate over 4 disjoint 128-slot "
+                                 "sets (256 MiB read per step, 1 GiB between reuses)",
+                           "parallelism": f"replicas x{world} (no collective)"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": clk.summary()}
+        line.update(secondary)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def time_calls(torch, fn, stream, n, warmup=2):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n):
+        fn()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / n
+
+
+def measure_secondary(torch, kda, wl, dev, stream, pk):
+    res = {}
+    # spec verify: 16 requests x 8 tokens
+    w = wl.spec_verify()
+    dw = wl.DeviceWorkload(w, dev)
+    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+    ms = time_calls(torch, lambda: wl.run_gpu(dw, kda, out=out), stream, 200, 5)
+    tiles = w.num_entries * w.H
+    null_tiles = sum(1 for s in w.indices() if s == w.null_slot) * w.H
+    sbytes = (tiles - null_tiles) * 2 * 4 * w.K * w.V + null_tiles * 4 * w.K * w.V
+    res["spec_verify"] = {"workload": "16 requests x 8 tokens, H=32, K=V=128, 2 padding requests on the null slot",
+                          "us_per_call": ms * 1e3, "state_gbs": sbytes / (ms * 1e-3) / 1e9,
+                          "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    del dw
+    # chunked prefill: seed-1 lengths, 33,494 tokens
+    w = wl.chunked_prefill(None)
+    dw = wl.DeviceWorkload(w, dev)
+    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+    cu_h = torch.from_numpy(w.cu_seqlens)
+    nb = kda.kda_chunk_prefill_workspace_bytes(cu_h, w.H, w.K, w.V)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+
+    def pf():
+        kda.kda_chunk_prefill(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, None,
+                              dw.pool_view(), dw.indices_view(), dw.cu, cu_seqlens_host=cu_h,
+                              scale=w.scale, out=out, workspace=ws)
+    ms = time_calls(torch, pf, stream, 5, 2)
+    flops = prefill_alg_flops(wl.PREFILL_LENGTHS_SEED1, w.H, w.K, w.V)
+    mb = prefill_min_bytes(w)
+    res["chunk_prefill"] = {"metric": "chunk-prefill tokens/s", "value": w.N / (ms * 1e-3),
+                            "unit": "tokens/s", "ms_per_call": ms,
+                            "workload": "8 seqs (seed-1 lengths, 33,494 tokens), H=32, K=V=128, chunk 64, lower_bound=None",
+                            "tflops_algorithmic": flops / (ms * 1e-3) / 1e12,
+                            "frac_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                            "hbm_gbs_min_bytes": mb / (ms * 1e-3) / 1e9,
+                            "frac_hbm": mb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                            "flop_count": "6cKV + c^2(3K+2V) + c^3/3 per (chunk of c rows, head)"}
+    del dw, ws
+    # mixed batch
+    w = wl.mixed_batch()
+    dw = wl.DeviceWorkload(w, dev)
+    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+    cu_h = torch.from_numpy(w.cu_seqlens)
+
+    def mb_call():
+        kda.kda_mixed_batch(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, None,
+                            dw.pool_view(), dw.indices_view(), dw.cu, w.num_decodes,
+                            cu_seqlens_host=cu_h, scale=w.scale, out=out)
+    ms = time_calls(torch, mb_call, stream, 5, 2)
+    res["mixed_batch"] = {"workload": "96 decodes + 4 x 4096 prefill tokens, H=32, K=V=128, index stride 4",
+                          "tokens_per_s": w.N / (ms * 1e-3), "ms_per_call": ms}
+    del dw
+    return res
+
+
+if __name__ == "__main__":
+    main()

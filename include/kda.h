@@ -1,0 +1,188 @@
+/*
+ * kda.h — C ABI of libkda: the Kimi Delta Attention (KDA) gated delta-rule
+ * recurrence on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (the "KDA recurrence" of the Kimi-K3 pages; vLLM PR #60683
+ * "specialized decode for Kimi-K3 on MI355X", section Purpose, and the packed
+ * decode call of vLLM PR #51682, section "key source excerpts"), per token t of a
+ * sequence and per head h, with channels c < K and value columns j < V:
+ *
+ *   x_c   = raw_g[t, h*K + c] + dt_bias[h*K + c]
+ *   g_c   = -exp(A_log[h]) * softplus(x_c)                  if !has_lower_bound
+ *         =  lower_bound * sigmoid(exp(A_log[h]) * x_c)      if  has_lower_bound
+ *   alpha = exp(g)                          (per-channel decay, in (0, 1])
+ *   beta  = sigmoid(raw_beta[t, h])
+ *   q^    = scale * q / sqrt(|q|^2 + l2_eps),   k^ = k / sqrt(|k|^2 + l2_eps)
+ *   S_t   = (I - beta k^ k^T) Diag(alpha) S_{t-1} + beta k^ v^T      (K x V, fp32)
+ *   o_t   = S_t^T q^                                                  (V, bf16 out)
+ *
+ * The pages name the gate's inputs (raw_g, A_log, dt_bias, lower_bound) but print
+ * no gate formula; the one above is this library's documented reading.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller. The library
+ *    allocates nothing, keeps no state between calls, never synchronises the
+ *    stream, and enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream). kda_packed_decode and kda_spec_verify can be captured in a
+ *    CUDA graph.
+ *  - bf16 values are passed as uint16_t bit patterns.
+ *  - mixed_qkv: bf16 [N, ld_qkv]; row t = [ q (H*K) | k (H*K) | v (H*V) ], each
+ *    part head-major ([H][K] or [H][V]). raw_g: bf16 [N, ld_g], H*K used.
+ *    raw_beta: bf16 [N, ld_beta], H used. out: bf16 [N, ld_out], H*V written.
+ *  - State pool: fp32, slot s and head h at pool + s*slot_stride + h*K*V, row-major
+ *    [K][V] (V contiguous). slot_stride >= H*K*V may exceed it (a slot can carry
+ *    more than the KDA state; the vLLM kernel takes it as stride_state_token =
+ *    initial_state.stride(0), PR #51682). Updated in place.
+ *  - State indices: the slot of entry i is indices[i * index_stride] (int32). The
+ *    view may be strided — e.g. column 0 of a [rows, 1 + num_speculative_blocks]
+ *    block table — exactly as the vLLM kernel loads
+ *    state_indices + i_n * stride_state_indices (PR #51682, implementation
+ *    breakdown item 1). index_stride must be >= 1 (a non-positive stride is
+ *    rejected: PR #51682's risk section notes that relaxing the check let such
+ *    views through unchecked).
+ *  - Slot semantics: 0 <= slot < num_slots is read and written back in place;
+ *    slot == null_slot (if null_slot >= 0) is read but never written, so padded
+ *    requests of a graph replay can share it (PR #60683, "Refusal and steps",
+ *    CUDA graphs); slot < 0 starts from a zero state and writes nothing;
+ *    slot >= num_slots is skipped: its output rows are written as zeros, nothing
+ *    is read or written in the pool, and bit 0 (KDA_ERRFLAG_SLOT_RANGE) of
+ *    *err_flags is set with an atomic OR (err_flags may be NULL). The device never
+ *    traps. Two entries naming the same writable slot in one call is a caller
+ *    error with an unspecified result.
+ *  - Sizes: H >= 1, K and V in {32, 64, 128}. The pool must be 16-byte aligned and
+ *    slot_stride a multiple of 4.
+ *  - Return value: KDA_OK, or an error code with a message in kda_last_error().
+ *    All argument checks happen on the host before any launch; on error nothing
+ *    is enqueued. A zero-sized call (N == 0 / no entries) returns KDA_OK and
+ *    enqueues nothing.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_OK 0
+#define KDA_ERR_INVALID_ARGUMENT 1 /* a pointer, size, stride or layout is not accepted */
+#define KDA_ERR_UNSUPPORTED 2      /* valid request this build does not serve (e.g. K=96) */
+#define KDA_ERR_WORKSPACE 3        /* workspace missing, too small or misaligned */
+#define KDA_ERR_CUDA 4             /* a CUDA runtime call or launch failed */
+
+#define KDA_ERRFLAG_SLOT_RANGE 1u /* bit 0 of *err_flags: a state index was >= num_slots */
+
+/* Per-layer head parameters shared by every call. */
+typedef struct kda_heads {
+    int32_t H, K, V;        /* heads, key dim, value dim */
+    const float *A_log;     /* device fp32 [H]: log of the per-head decay rate */
+    const float *dt_bias;   /* device fp32 [H*K], per channel; NULL = zeros */
+    int32_t has_lower_bound;/* nonzero: bounded gate lower_bound * sigmoid(...) */
+    float lower_bound;      /* used when has_lower_bound; must be finite and <= 0 */
+    float scale;            /* multiplies q^ (commonly K^-1/2); finite */
+    float l2_eps;           /* epsilon inside the q/k L2 norms; >= 0 (1e-6 typical) */
+} kda_heads;
+
+/* The state pool and the entry -> slot map of one call. */
+typedef struct kda_state {
+    float *pool;            /* device fp32 [num_slots, slot_stride], updated in place */
+    int64_t num_slots;      /* >= 1 */
+    int64_t slot_stride;    /* elements between slots, >= H*K*V, multiple of 4 */
+    const int32_t *indices; /* device int32, entry i at indices[i*index_stride] */
+    int64_t index_stride;   /* >= 1 */
+    int32_t null_slot;      /* slot that is read but never written; -1 = none */
+} kda_state;
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char *kda_last_error(void);
+
+/* Name of a status code. */
+const char *kda_status_string(int status);
+
+/*
+ * kda_gate — the fused decay gate and beta on their own: per token t < N, head h,
+ * channel c, g_out[t*H*K + h*K + c] = g_c (fp32 log-decay, <= 0) and
+ * beta_out[t*H + h] = sigmoid(raw_beta[t, h]). The gate inputs are the ones the
+ * vLLM call passes (raw_g, raw_beta, A_log, dt_bias, lower_bound; PR #51682 test
+ * call); "chunk_kda_with_fused_gate" (PR #50649, Purpose) fuses this step into the
+ * chunk kernel, as every other call here does. K may be any value in 1..1024 here.
+ */
+int kda_gate(const uint16_t *raw_g, int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+             int64_t N, const kda_heads *heads, float *g_out, float *beta_out, void *stream);
+
+/*
+ * kda_packed_decode — one decode token per sequence (fused_recurrent_kda_packed_decode,
+ * PR #51682, key source excerpts). Sequence n < num_seqs is row n of mixed_qkv /
+ * raw_g / raw_beta / out; its state slot is indices[n*index_stride]. The slot's
+ * state is updated in place and o is written to out row n.
+ */
+int kda_packed_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                      int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                      int64_t num_seqs, const kda_heads *heads, const kda_state *state,
+                      uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream);
+
+/*
+ * kda_spec_verify — a pure spec-verify step (PR #60683, "Refusal and steps": whole
+ * uniform requests, width a multiple of k+1, at most 8 rows each in the pages'
+ * deployment). Request r < num_reqs owns rows [r*T, (r+1)*T), T = tokens_per_req
+ * in 1..64, and slot indices[r*index_stride]; its state advances token by token
+ * and is written back once after the last token. Outputs for every row.
+ */
+int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                    int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                    int64_t num_reqs, int32_t tokens_per_req, const kda_heads *heads,
+                    const kda_state *state, uint16_t *out, int64_t ld_out,
+                    uint32_t *err_flags, void *stream);
+
+/*
+ * kda_chunk_prefill_workspace_bytes — device workspace kda_chunk_prefill needs for
+ * these sequence lengths (cu_seqlens_host: host int32 [num_seqs+1]). Returns 0 on
+ * invalid arguments (and sets kda_last_error) or when no workspace is needed.
+ */
+size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t num_seqs,
+                                         const kda_heads *heads, int32_t chunk_size);
+
+/*
+ * kda_chunk_prefill — chunked varlen prefill (chunk_kda_with_fused_gate with its
+ * WY-form recompute_w_u and intra-/inter-chunk products, PR #50649 Purpose).
+ * Sequence s < num_seqs owns rows [cu_seqlens[s], cu_seqlens[s+1]) and slot
+ * indices[s*index_stride]; its state is read from the slot, advanced over every
+ * row, and written back once. cu_seqlens (device) and cu_seqlens_host (host) must
+ * hold the same non-decreasing, non-negative int32 values; the host copy sizes the
+ * launch; mixed_qkv, raw_g, raw_beta and out must hold cu_seqlens[num_seqs] rows.
+ * chunk_size must be 64. `workspace` (device, 256-byte aligned) must
+ * hold kda_chunk_prefill_workspace_bytes(...) bytes; it may be NULL when that is 0.
+ * Zero-length sequences are allowed: their slot is left untouched.
+ */
+int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                      int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                      int64_t num_seqs, int32_t chunk_size, const kda_heads *heads,
+                      const kda_state *state, void *workspace, size_t workspace_bytes,
+                      uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream);
+
+/*
+ * kda_mixed_batch — a mixed decode + prefill batch (PR #50649, Purpose: the decodes
+ * of a mixed batch must not go through the chunk kernel, which returned NaN for
+ * length-1 sequences). Sequences 0..num_decodes-1 must have length 1 and take the
+ * recurrent decode path; sequences num_decodes..num_decodes+num_prefills-1 take
+ * the chunked prefill path. One cu_seqlens (device + host copies) and one strided
+ * index view cover all of them, decodes first. Workspace as for
+ * kda_chunk_prefill over the prefill sequences:
+ * kda_chunk_prefill_workspace_bytes(cu_seqlens_host + num_decodes, num_prefills, ...).
+ */
+int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                    int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                    const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                    int64_t num_decodes, int64_t num_prefills, const kda_heads *heads,
+                    const kda_state *state, void *workspace, size_t workspace_bytes,
+                    uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,307 @@
+// extern "C" entry points of libkda (declared in include/kda.h): host-side
+// argument checks, then kernel launches on the caller's stream. Nothing here
+// allocates, synchronises or keeps state between calls.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/kda.h"
+#include "kda_launch.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int ok()
+{
+    g_last_error[0] = '\0';
+    return KDA_OK;
+}
+
+int cuda_status(cudaError_t e, const char *what)
+{
+    if (e != cudaSuccess)
+        return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+int check_heads(const kda_heads *hd, bool gate_only)
+{
+    if (!hd) return fail(KDA_ERR_INVALID_ARGUMENT, "heads is NULL");
+    if (hd->H < 1) return fail(KDA_ERR_INVALID_ARGUMENT, "H must be >= 1 (got %d)", hd->H);
+    if (gate_only) {
+        if (hd->K < 1 || hd->K > 1024)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "K must be in 1..1024 (got %d)", hd->K);
+    } else {
+        if (hd->K < 1 || hd->V < 1)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "K and V must be >= 1 (got %d, %d)", hd->K, hd->V);
+        if (!supported_dim(hd->K) || !supported_dim(hd->V))
+            return fail(KDA_ERR_UNSUPPORTED, "K and V must each be 32, 64 or 128 (got K=%d, V=%d)",
+                        hd->K, hd->V);
+    }
+    if (!hd->A_log) return fail(KDA_ERR_INVALID_ARGUMENT, "A_log is NULL");
+    if (hd->has_lower_bound && !(std::isfinite(hd->lower_bound) && hd->lower_bound <= 0.f))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "lower_bound must be finite and <= 0 (got %g)",
+                    static_cast<double>(hd->lower_bound));
+    if (!gate_only) {
+        if (!std::isfinite(hd->scale))
+            return fail(KDA_ERR_INVALID_ARGUMENT, "scale must be finite");
+        if (!(hd->l2_eps >= 0.f) || !std::isfinite(hd->l2_eps))
+            return fail(KDA_ERR_INVALID_ARGUMENT, "l2_eps must be finite and >= 0");
+    }
+    return KDA_OK;
+}
+
+// Row-tensor checks shared by every compute call.
+int check_rows(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g, int64_t ld_g,
+               const uint16_t *raw_beta, int64_t ld_beta, const uint16_t *out, int64_t ld_out,
+               const kda_heads *hd)
+{
+    const int64_t H = hd->H, K = hd->K, V = hd->V;
+    if (!mixed_qkv || !raw_g || !raw_beta || !out)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "mixed_qkv, raw_g, raw_beta and out must be non-NULL");
+    if (ld_qkv < 2 * H * K + H * V)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "ld_qkv (%lld) < 2*H*K + H*V (%lld)",
+                    (long long)ld_qkv, (long long)(2 * H * K + H * V));
+    if (ld_g < H * K)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "ld_g (%lld) < H*K (%lld)", (long long)ld_g, (long long)(H * K));
+    if (ld_beta < H)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "ld_beta (%lld) < H (%lld)", (long long)ld_beta, (long long)H);
+    if (ld_out < H * V)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "ld_out (%lld) < H*V (%lld)", (long long)ld_out, (long long)(H * V));
+    if (!aligned(out, 8) || (ld_out % 4) != 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "out must be 8-byte aligned with ld_out a multiple of 4");
+    if (!aligned(mixed_qkv, 2) || !aligned(raw_g, 2) || !aligned(raw_beta, 2))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "bf16 inputs must be 2-byte aligned");
+    return KDA_OK;
+}
+
+int check_state(const kda_state *st, const kda_heads *hd)
+{
+    if (!st) return fail(KDA_ERR_INVALID_ARGUMENT, "state is NULL");
+    if (!st->pool || !st->indices)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "state->pool and state->indices must be non-NULL");
+    if (st->num_slots < 1)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "num_slots must be >= 1 (got %lld)", (long long)st->num_slots);
+    const int64_t hkv = static_cast<int64_t>(hd->H) * hd->K * hd->V;
+    if (st->slot_stride < hkv)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "slot_stride (%lld) < H*K*V (%lld)",
+                    (long long)st->slot_stride, (long long)hkv);
+    if (st->slot_stride % 4 != 0 || !aligned(st->pool, 16))
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "the pool must be 16-byte aligned and slot_stride a multiple of 4");
+    if (st->index_stride < 1)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "index_stride must be >= 1 (got %lld): state_indices is a 1-D view with a positive stride",
+                    (long long)st->index_stride);
+    if (!aligned(st->indices, 4))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "indices must be 4-byte aligned");
+    if (st->null_slot < -1 || st->null_slot >= st->num_slots)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "null_slot must be -1 or in [0, num_slots) (got %d)",
+                    st->null_slot);
+    return KDA_OK;
+}
+
+kda::Params make_params(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                        int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                        const kda_heads *hd, const kda_state *st, uint16_t *out, int64_t ld_out,
+                        uint32_t *err)
+{
+    kda::Params p{};
+    p.qkv = mixed_qkv; p.ld_qkv = ld_qkv;
+    p.rg = raw_g; p.ld_g = ld_g;
+    p.rb = raw_beta; p.ld_beta = ld_beta;
+    p.A_log = hd->A_log; p.dt_bias = hd->dt_bias;
+    p.has_lb = hd->has_lower_bound ? 1 : 0; p.lb = hd->lower_bound;
+    p.scale = hd->scale; p.eps = hd->l2_eps;
+    if (st) {
+        p.pool = st->pool; p.num_slots = st->num_slots; p.slot_stride = st->slot_stride;
+        p.indices = st->indices; p.index_stride = st->index_stride; p.null_slot = st->null_slot;
+    }
+    p.out = out; p.ld_out = ld_out;
+    p.err = err;
+    p.H = hd->H;
+    return p;
+}
+
+int check_cu_host(const int32_t *cu_host, int64_t n)
+{
+    if (!cu_host) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens_host is NULL");
+    if (cu_host[0] < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens[0] must be >= 0");
+    for (int64_t s = 0; s < n; s++)
+        if (cu_host[s + 1] < cu_host[s])
+            return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be non-decreasing (at %lld)", (long long)s);
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_last_error(void) { return g_last_error; }
+
+const char *kda_status_string(int status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_gate(const uint16_t *raw_g, int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+             int64_t N, const kda_heads *heads, float *g_out, float *beta_out, void *stream)
+{
+    int s = check_heads(heads, true);
+    if (s) return s;
+    if (N < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "N must be >= 0");
+    if (!raw_g || !raw_beta || !g_out || !beta_out)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "raw_g, raw_beta, g_out and beta_out must be non-NULL");
+    if (ld_g < static_cast<int64_t>(heads->H) * heads->K || ld_beta < heads->H)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "ld_g must be >= H*K and ld_beta >= H");
+    if (N == 0) return ok();
+    kda::Params p = make_params(nullptr, 0, raw_g, ld_g, raw_beta, ld_beta, heads, nullptr,
+                                nullptr, 0, nullptr);
+    return cuda_status(kda::launch_gate(p, heads->K, N, g_out, beta_out,
+                                        static_cast<cudaStream_t>(stream)), "kda_gate launch");
+}
+
+int kda_packed_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                      int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                      int64_t num_seqs, const kda_heads *heads, const kda_state *state,
+                      uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream)
+{
+    int s;
+    if ((s = check_heads(heads, false))) return s;
+    if ((s = check_rows(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, out, ld_out, heads))) return s;
+    if ((s = check_state(state, heads))) return s;
+    if (num_seqs < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs must be >= 0");
+    if (num_seqs == 0) return ok();
+    kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
+                                out, ld_out, err_flags);
+    return cuda_status(kda::launch_recurrent(p, heads->K, heads->V, 0, 1, nullptr, 0, num_seqs,
+                                             static_cast<cudaStream_t>(stream)),
+                       "kda_packed_decode launch");
+}
+
+int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                    int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                    int64_t num_reqs, int32_t tokens_per_req, const kda_heads *heads,
+                    const kda_state *state, uint16_t *out, int64_t ld_out,
+                    uint32_t *err_flags, void *stream)
+{
+    int s;
+    if ((s = check_heads(heads, false))) return s;
+    if ((s = check_rows(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, out, ld_out, heads))) return s;
+    if ((s = check_state(state, heads))) return s;
+    if (num_reqs < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "num_reqs must be >= 0");
+    if (tokens_per_req < 1 || tokens_per_req > 64)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "tokens_per_req must be in 1..64 (got %d)", tokens_per_req);
+    if (num_reqs == 0) return ok();
+    kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
+                                out, ld_out, err_flags);
+    return cuda_status(kda::launch_recurrent(p, heads->K, heads->V, 1, tokens_per_req, nullptr, 0,
+                                             num_reqs, static_cast<cudaStream_t>(stream)),
+                       "kda_spec_verify launch");
+}
+
+size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t num_seqs,
+                                         const kda_heads *heads, int32_t chunk_size)
+{
+    if (check_heads(heads, false)) return 0;
+    if (num_seqs < 0) { fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs must be >= 0"); return 0; }
+    if (num_seqs == 0) return 0;
+    if (check_cu_host(cu_seqlens_host, num_seqs)) return 0;
+    if (chunk_size != 64) { fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 64"); return 0; }
+    return kda::chunk_workspace_bytes(cu_seqlens_host, num_seqs, heads->H, heads->K, heads->V,
+                                      chunk_size);
+}
+
+static int chunk_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                        int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                        int64_t num_decodes, int64_t num_prefills, int32_t chunk_size,
+                        const kda_heads *heads, const kda_state *state, void *workspace,
+                        size_t workspace_bytes, uint16_t *out, int64_t ld_out,
+                        uint32_t *err_flags, void *stream, const char *name)
+{
+    int s;
+    if ((s = check_heads(heads, false))) return s;
+    if ((s = check_rows(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, out, ld_out, heads))) return s;
+    if ((s = check_state(state, heads))) return s;
+    if (num_decodes < 0 || num_prefills < 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "sequence counts must be >= 0");
+    if (chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 64 (got %d)", chunk_size);
+    const int64_t n = num_decodes + num_prefills;
+    if (n == 0) return ok();
+    if (!cu_seqlens) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
+    if ((s = check_cu_host(cu_seqlens_host, n))) return s;
+    for (int64_t d = 0; d < num_decodes; d++)
+        if (cu_seqlens_host[d + 1] - cu_seqlens_host[d] != 1)
+            return fail(KDA_ERR_INVALID_ARGUMENT,
+                        "decode sequence %lld of the mixed batch has length %d (must be 1)",
+                        (long long)d, cu_seqlens_host[d + 1] - cu_seqlens_host[d]);
+    const size_t need = kda::chunk_workspace_bytes(cu_seqlens_host + num_decodes, num_prefills,
+                                                   heads->H, heads->K, heads->V, chunk_size);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return fail(KDA_ERR_WORKSPACE, "%s needs a 256-byte aligned workspace of %zu bytes (got %zu)",
+                    name, need, workspace ? workspace_bytes : (size_t)0);
+    kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
+                                out, ld_out, err_flags);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (num_decodes > 0) {
+        cudaError_t e = kda::launch_recurrent(p, heads->K, heads->V, 2, 1, cu_seqlens, 0,
+                                              num_decodes, st);
+        if (e != cudaSuccess) return cuda_status(e, "decode launch");
+    }
+    if (num_prefills > 0) {
+        cudaError_t e = kda::launch_chunk_prefill(p, heads->K, heads->V, cu_seqlens,
+                                                  cu_seqlens_host, num_decodes, num_prefills,
+                                                  chunk_size, workspace, workspace_bytes, st);
+        if (e != cudaSuccess) return cuda_status(e, "chunk prefill launch");
+    }
+    return ok();
+}
+
+int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                      int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                      int64_t num_seqs, int32_t chunk_size, const kda_heads *heads,
+                      const kda_state *state, void *workspace, size_t workspace_bytes,
+                      uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream)
+{
+    return chunk_common(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, cu_seqlens,
+                        cu_seqlens_host, 0, num_seqs, chunk_size, heads, state, workspace,
+                        workspace_bytes, out, ld_out, err_flags, stream, "kda_chunk_prefill");
+}
+
+int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                    int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                    const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                    int64_t num_decodes, int64_t num_prefills, const kda_heads *heads,
+                    const kda_state *state, void *workspace, size_t workspace_bytes,
+                    uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream)
+{
+    return chunk_common(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, cu_seqlens,
+                        cu_seqlens_host, num_decodes, num_prefills, 64, heads, state, workspace,
+                        workspace_bytes, out, ld_out, err_flags, stream, "kda_mixed_batch");
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Device helpers shared by the KDA kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kda {
+
+// Kernel-side view of the per-call arguments (filled by the host entry points).
+struct Params {
+    const uint16_t *qkv;  int64_t ld_qkv;
+    const uint16_t *rg;   int64_t ld_g;
+    const uint16_t *rb;   int64_t ld_beta;
+    const float *A_log;   const float *dt_bias;
+    int has_lb;           float lb;
+    float scale;          float eps;
+    float *pool;          int64_t num_slots;   int64_t slot_stride;
+    const int32_t *indices; int64_t index_stride; int null_slot;
+    uint16_t *out;        int64_t ld_out;
+    uint32_t *err;
+    int H;
+};
+
+constexpr uint32_t kErrSlotRange = 1u;
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b)
+{
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (inputs here are finite or +-inf).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7f800000u) == 0x7f800000u)  // inf / nan: truncate, keep nan quiet
+        return static_cast<uint16_t>((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return static_cast<uint16_t>(u >> 16);
+}
+
+__device__ __forceinline__ float softplus_f(float x)
+{
+    return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+}
+
+__device__ __forceinline__ float sigmoid_f(float y)
+{
+    return 1.f / (1.f + expf(-y));
+}
+
+// Per-channel log-decay g <= 0 of the fused gate: -e^{A_log} softplus(x), or
+// lower_bound * sigmoid(e^{A_log} x) when a lower bound is set; x = raw_g + dt_bias.
+__device__ __forceinline__ float gate_log_decay(float x, float expA, int has_lb, float lb)
+{
+    return has_lb ? lb * sigmoid_f(expA * x) : -expA * softplus_f(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Slot of entry e: indices[e * index_stride] widened to 64 bits.
+__device__ __forceinline__ int64_t load_slot(const Params &p, int64_t e)
+{
+    return static_cast<int64_t>(__ldg(p.indices + e * p.index_stride));
+}
+
+}  // namespace kda

@@ -1,0 +1,28 @@
+// Internal launcher declarations (host side), shared by the entry points.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+cudaError_t launch_gate(const Params &p, int K, int64_t N, float *g_out, float *beta_out,
+                        cudaStream_t stream);
+
+// mode: 0 = one row per entry (row e), 1 = T rows per entry (rows e*T ..), 2 = rows
+// [cu[e], cu[e+1]). Entries entry_base .. entry_base + num_entries - 1.
+cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
+                             int64_t entry_base, int64_t num_entries, cudaStream_t stream);
+
+// Chunked prefill over entries entry_base .. entry_base + num_seqs - 1 (rows from cu).
+size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V,
+                             int chunk_size);
+cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *cu,
+                                 const int32_t *cu_host, int64_t entry_base, int64_t num_seqs,
+                                 int chunk_size, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+}  // namespace kda

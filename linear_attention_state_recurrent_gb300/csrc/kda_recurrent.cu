@@ -1,0 +1,251 @@
+// Recurrent (token-by-token) KDA kernels: the standalone gate, packed decode,
+// spec-verify and the recurrent path over varlen rows.
+//
+// One CTA owns one (entry, head, 32-wide V slice) state tile. The value columns
+// of S are independent in the update (column j of S_t depends only on column j
+// of S_{t-1}; the coupling is only through the K-reductions k^T S and q^T S), so
+// a K x V tile splits along V with no communication. The tile lives in registers
+// for the whole call: loaded once with 128-bit coalesced loads, advanced over the
+// entry's tokens, stored once. Gate, beta and the q/k L2 norms are fused in.
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------------------
+// Standalone gate: g (fp32 [N, H*K]) and beta (fp32 [N, H]).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gate_kernel(Params p, int K, int64_t N, float *g_out,
+                                                   float *beta_out)
+{
+    const int64_t HK = static_cast<int64_t>(p.H) * K;
+    const int64_t total = N * HK;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += stride) {
+        const int64_t t = i / HK;
+        const int64_t hc = i - t * HK;
+        const int h = static_cast<int>(hc / K);
+        float x = bf16_to_f32(p.rg[t * p.ld_g + hc]);
+        if (p.dt_bias) x += p.dt_bias[hc];
+        g_out[i] = gate_log_decay(x, expf(p.A_log[h]), p.has_lb, p.lb);
+    }
+    const int64_t totb = N * p.H;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < totb;
+         i += stride) {
+        const int64_t t = i / p.H;
+        const int h = static_cast<int>(i - t * p.H);
+        beta_out[i] = sigmoid_f(bf16_to_f32(p.rb[t * p.ld_beta + h]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Recurrent kernel.
+//
+// Thread layout (128 threads): cg = tid & 7 picks 4 value columns (one float4),
+// rg = tid >> 3 picks rows rg, rg + 16, ... (RPT = K / 16 rows per thread). A warp
+// therefore covers 4 rows x 32 columns per float4 load: four 128-byte segments.
+//
+// Per token:
+//   [A] threads c < K compute the gate alpha_c and stash alpha_c, k_c, q_c (raw)
+//       in shared memory; each warp sums |q|^2, |k|^2, q.k over its 32 channels.
+//   [B] every thread decays its rows (S <- alpha S), accumulates k^T S and q^T S
+//       over its rows, reduces over the 4 row groups of its warp by shuffles and
+//       writes per-warp partials.
+//   [C] every thread sums the 4 warps' partials for its 4 columns and forms
+//       u = beta (v - S'^T k^), o = S'^T q^ + (q^.k^) u, then S <- S' + k^ u^T.
+// ---------------------------------------------------------------------------
+enum RowMode { kRowsDecode = 0, kRowsSpec = 1, kRowsVarlen = 2 };
+
+template <int K, int V>
+__global__ void __launch_bounds__(128) recurrent_kernel(Params p, int mode, int T,
+                                                        const int32_t *cu, int64_t entry_base)
+{
+    constexpr int VT = 32;              // value columns per CTA
+    constexpr int VS = V / VT;          // V slices per (entry, head)
+    constexpr int RPT = K / 16;         // rows per thread
+    constexpr int KW = K / 32;          // warps that own channels in [A]
+
+    __shared__ float s_a[K], s_k[K], s_q[K];
+    __shared__ float s_part[KW][3];
+    __shared__ float s_red[4][2][VT];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int cg = tid & 7;
+    const int rg = tid >> 3;
+
+    const int64_t b = blockIdx.x;
+    const int vs = static_cast<int>(b % VS);
+    const int h = static_cast<int>((b / VS) % p.H);
+    const int64_t e = b / (static_cast<int64_t>(VS) * p.H) + entry_base;
+
+    int64_t row0, row1;
+    if (mode == kRowsDecode) { row0 = e; row1 = e + 1; }
+    else if (mode == kRowsSpec) { row0 = e * T; row1 = row0 + T; }
+    else { row0 = cu[e]; row1 = cu[e + 1]; }
+
+    const int j0 = vs * VT + cg * 4;                    // first of this thread's 4 columns
+    const int64_t slot = load_slot(p, e);
+
+    if (slot >= p.num_slots) {                          // out of range: flag, zero outputs
+        if (tid == 0 && p.err) atomicOr(p.err, kErrSlotRange);
+        if (rg == 0)
+            for (int64_t t = row0; t < row1; t++) {
+                uint2 z = make_uint2(0u, 0u);
+                *reinterpret_cast<uint2 *>(p.out + t * p.ld_out + static_cast<int64_t>(h) * V + j0) = z;
+            }
+        return;
+    }
+    const bool has_state = slot >= 0;
+    const bool writable = has_state && slot != p.null_slot;
+    float *tile = has_state ? p.pool + slot * p.slot_stride + static_cast<int64_t>(h) * K * V : nullptr;
+
+    // Issue the state loads first so they are in flight during the gate math.
+    float4 S[RPT];
+    if (has_state) {
+#pragma unroll
+        for (int i = 0; i < RPT; i++)
+            S[i] = *reinterpret_cast<const float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V + j0);
+    } else {
+#pragma unroll
+        for (int i = 0; i < RPT; i++) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    const float expA = expf(__ldg(p.A_log + h));
+    const bool chan = tid < K;
+    const float dtb = (chan && p.dt_bias) ? __ldg(p.dt_bias + h * K + tid) : 0.f;
+    const int64_t HK = static_cast<int64_t>(p.H) * K;
+
+    // Prefetch token row0's inputs.
+    float nq = 0.f, nk = 0.f, ng = 0.f, nb = 0.f;
+    float4 nv = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto fetch = [&](int64_t t) {
+        const uint16_t *row = p.qkv + t * p.ld_qkv;
+        if (chan) {
+            nq = bf16_to_f32(row[h * K + tid]);
+            nk = bf16_to_f32(row[HK + h * K + tid]);
+            ng = bf16_to_f32(p.rg[t * p.ld_g + h * K + tid]);
+        }
+        const uint16_t *vp = row + 2 * HK + static_cast<int64_t>(h) * V + j0;
+        nv = make_float4(bf16_to_f32(vp[0]), bf16_to_f32(vp[1]), bf16_to_f32(vp[2]), bf16_to_f32(vp[3]));
+        nb = bf16_to_f32(p.rb[t * p.ld_beta + h]);
+    };
+    if (row0 < row1) fetch(row0);
+
+    for (int64_t t = row0; t < row1; t++) {
+        // ---- [A] gate + stash ----
+        const float4 v = nv;
+        const float beta = sigmoid_f(nb);
+        if (chan) {
+            const float g = gate_log_decay(ng + dtb, expA, p.has_lb, p.lb);
+            s_a[tid] = expf(g);
+            s_k[tid] = nk;
+            s_q[tid] = nq;
+            float qq = warp_sum(nq * nq), kk = warp_sum(nk * nk), qk = warp_sum(nq * nk);
+            if (lane == 0) { s_part[warp][0] = qq; s_part[warp][1] = kk; s_part[warp][2] = qk; }
+        }
+        __syncthreads();
+        if (t + 1 < row1) fetch(t + 1);
+
+        // ---- [B] decay + partial reductions ----
+        float qq = 0.f, kk = 0.f, qk = 0.f;
+#pragma unroll
+        for (int w = 0; w < KW; w++) { qq += s_part[w][0]; kk += s_part[w][1]; qk += s_part[w][2]; }
+        const float rq = p.scale * rsqrtf(qq + p.eps);
+        const float rk = rsqrtf(kk + p.eps);
+        float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const int r = rg + 16 * i;
+            const float a = s_a[r], kr = s_k[r], qr = s_q[r];
+            S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
+            pk[0] += kr * S[i].x; pk[1] += kr * S[i].y; pk[2] += kr * S[i].z; pk[3] += kr * S[i].w;
+            pq[0] += qr * S[i].x; pq[1] += qr * S[i].y; pq[2] += qr * S[i].z; pq[3] += qr * S[i].w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 8);
+            pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 16);
+            pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 8);
+            pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 16);
+        }
+        if (lane < 8) {
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+                s_red[warp][0][cg * 4 + jj] = pk[jj];
+                s_red[warp][1][cg * 4 + jj] = pq[jj];
+            }
+        }
+        __syncthreads();
+
+        // ---- [C] u, o, rank-1 update ----
+        float u[4], o[4];
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        const float qkh = qk * rq * rk;
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            const int c = cg * 4 + jj;
+            const float ks = (s_red[0][0][c] + s_red[1][0][c] + s_red[2][0][c] + s_red[3][0][c]) * rk;
+            const float qs = (s_red[0][1][c] + s_red[1][1][c] + s_red[2][1][c] + s_red[3][1][c]) * rq;
+            u[jj] = beta * (vv[jj] - ks);
+            o[jj] = qs + qkh * u[jj];
+        }
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const float kh = s_k[rg + 16 * i] * rk;
+            S[i].x += kh * u[0]; S[i].y += kh * u[1]; S[i].z += kh * u[2]; S[i].w += kh * u[3];
+        }
+        if (rg == 0) {
+            uint2 packed;
+            packed.x = static_cast<uint32_t>(f32_to_bf16(o[0])) | (static_cast<uint32_t>(f32_to_bf16(o[1])) << 16);
+            packed.y = static_cast<uint32_t>(f32_to_bf16(o[2])) | (static_cast<uint32_t>(f32_to_bf16(o[3])) << 16);
+            *reinterpret_cast<uint2 *>(p.out + t * p.ld_out + static_cast<int64_t>(h) * V + j0) = packed;
+        }
+    }
+
+    if (writable && row0 < row1) {
+#pragma unroll
+        for (int i = 0; i < RPT; i++)
+            *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V + j0) = S[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_gate(const Params &p, int K, int64_t N, float *g_out, float *beta_out,
+                        cudaStream_t stream)
+{
+    const int64_t total = N * p.H * static_cast<int64_t>(K);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    gate_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p, K, N, g_out, beta_out);
+    return cudaGetLastError();
+}
+
+template <int K, int V>
+static cudaError_t launch_rec_kv(const Params &p, int mode, int T, const int32_t *cu,
+                                 int64_t entry_base, int64_t num_entries, cudaStream_t stream)
+{
+    const int64_t grid = num_entries * p.H * (V / 32);
+    recurrent_kernel<K, V><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, mode, T, cu, entry_base);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
+                             int64_t entry_base, int64_t num_entries, cudaStream_t stream)
+{
+    if (num_entries <= 0) return cudaSuccess;
+#define KDA_REC_CASE(KK, VV) \
+    if (K == KK && V == VV) return launch_rec_kv<KK, VV>(p, mode, T, cu, entry_base, num_entries, stream);
+    KDA_REC_CASE(32, 32) KDA_REC_CASE(32, 64) KDA_REC_CASE(32, 128)
+    KDA_REC_CASE(64, 32) KDA_REC_CASE(64, 64) KDA_REC_CASE(64, 128)
+    KDA_REC_CASE(128, 32) KDA_REC_CASE(128, 64) KDA_REC_CASE(128, 128)
+#undef KDA_REC_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

@@ -1,0 +1,280 @@
+"""Thin ctypes binding of libkda (include/kda.h). Argument marshalling only: every
+step of the computation runs in the library's CUDA kernels.
+
+The functions carry the C names and take torch tensors already on the GPU. As
+in vLLM's fused_recurrent_kda_packed_decode (PR #51682), the decode-style calls
+return (out, state_pool), with the pool updated in place, and raise ValueError
+when an argument is rejected (e.g. a state_indices view that is not 1-D).
+
+Tensor conventions:
+  mixed_qkv  bf16 [N, >= 2*H*K + H*V], unit inner stride (row = q | k | v)
+  raw_g      bf16 [N, >= H*K];  raw_beta bf16 [N, >= H]
+  A_log      fp32 [H];  dt_bias fp32 [H*K] (or [H, K]) or None
+  state_pool fp32 [num_slots, H, K, V] with contiguous inner [H, K, V]; any slot stride
+  state_indices int32 1-D, any positive stride
+  cu_seqlens int32 [num_seqs + 1] on the GPU (a host copy is taken for launch sizing)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARGUMENT = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_ERRFLAG_SLOT_RANGE = 1
+
+EXPORTED = ("kda_last_error", "kda_status_string", "kda_gate", "kda_packed_decode",
+            "kda_spec_verify", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill",
+            "kda_mixed_batch")
+
+
+class KdaHeads(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("has_lower_bound", ctypes.c_int32), ("lower_bound", ctypes.c_float),
+                ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float)]
+
+
+class KdaState(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+                ("slot_stride", ctypes.c_int64), ("indices", ctypes.c_void_p),
+                ("index_stride", ctypes.c_int64), ("null_slot", ctypes.c_int32)]
+
+
+class KdaError(RuntimeError):
+    pass
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libkda.so is not built ({_LIB_PATH}); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    HP, SP = ctypes.POINTER(KdaHeads), ctypes.POINTER(KdaState)
+    lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_last_error.argtypes = []
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_gate.restype = ctypes.c_int
+    lib.kda_gate.argtypes = [P, I64, P, I64, I64, HP, P, P, P]
+    lib.kda_packed_decode.restype = ctypes.c_int
+    lib.kda_packed_decode.argtypes = [P, I64, P, I64, P, I64, I64, HP, SP, P, I64, P, P]
+    lib.kda_spec_verify.restype = ctypes.c_int
+    lib.kda_spec_verify.argtypes = [P, I64, P, I64, P, I64, I64, I32, HP, SP, P, I64, P, P]
+    lib.kda_chunk_prefill_workspace_bytes.restype = SZ
+    lib.kda_chunk_prefill_workspace_bytes.argtypes = [P, I64, HP, I32]
+    lib.kda_chunk_prefill.restype = ctypes.c_int
+    lib.kda_chunk_prefill.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I32, HP, SP, P, SZ, P,
+                                      I64, P, P]
+    lib.kda_mixed_batch.restype = ctypes.c_int
+    lib.kda_mixed_batch.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I64, HP, SP, P, SZ, P,
+                                    I64, P, P]
+    return lib
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.kda_last_error().decode()
+
+
+def _check(status: int, what: str):
+    if status == KDA_OK:
+        return
+    msg = f"{what}: {lib.kda_status_string(status).decode()}: {last_error()}"
+    if status in (KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE):
+        raise ValueError(msg)
+    raise KdaError(msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _rows(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit inner stride")
+    return t.stride(0)
+
+
+def make_heads(A_log, dt_bias, lower_bound, K, V, scale=None, l2_eps=1e-6):
+    """Builds the kda_heads struct; keeps the tensors it points at alive via the return."""
+    if A_log.dtype != torch.float32 or not A_log.is_contiguous():
+        raise ValueError("A_log must be a contiguous fp32 tensor")
+    if dt_bias is not None and (dt_bias.dtype != torch.float32 or not dt_bias.is_contiguous()):
+        raise ValueError("dt_bias must be a contiguous fp32 tensor")
+    H = A_log.numel()
+    hd = KdaHeads(H=H, K=K, V=V, A_log=A_log.data_ptr(),
+                  dt_bias=None if dt_bias is None else dt_bias.data_ptr(),
+                  has_lower_bound=int(lower_bound is not None),
+                  lower_bound=float(lower_bound if lower_bound is not None else 0.0),
+                  scale=float(K ** -0.5 if scale is None else scale), l2_eps=float(l2_eps))
+    return hd
+
+
+def make_state(state_pool, state_indices, null_slot=-1):
+    if state_indices.dim() != 1:
+        raise ValueError("`state_indices` must be one-dimensional.")
+    if state_indices.dtype != torch.int32:
+        raise ValueError("state_indices must be int32")
+    if state_pool.dtype != torch.float32 or state_pool.dim() != 4:
+        raise ValueError("state_pool must be fp32 [num_slots, H, K, V]")
+    _, H, K, V = state_pool.shape
+    if state_pool.stride()[1:] != (K * V, V, 1):
+        raise ValueError("state_pool's [H, K, V] part must be contiguous")
+    return KdaState(pool=state_pool.data_ptr(), num_slots=state_pool.shape[0],
+                    slot_stride=state_pool.stride(0), indices=state_indices.data_ptr(),
+                    index_stride=state_indices.stride(0), null_slot=int(null_slot))
+
+
+def _out(out, N, H, V, device):
+    if out is None:
+        out = torch.empty(N, H * V, dtype=torch.bfloat16, device=device)
+    return out, _rows(out, "out")
+
+
+def kda_gate(raw_g, raw_beta, A_log, dt_bias=None, lower_bound=None, *, K=None, g_out=None,
+             beta_out=None, stream=None):
+    """Returns (g fp32 [N, H*K], beta fp32 [N, H])."""
+    N = raw_g.shape[0]
+    H = A_log.numel()
+    K = raw_g.shape[1] // H if K is None else K
+    ld_g, ld_b = _rows(raw_g, "raw_g"), _rows(raw_beta, "raw_beta")
+    hd = make_heads(A_log, dt_bias, lower_bound, K, K)
+    if g_out is None:
+        g_out = torch.empty(N, H * K, dtype=torch.float32, device=raw_g.device)
+    if beta_out is None:
+        beta_out = torch.empty(N, H, dtype=torch.float32, device=raw_g.device)
+    _check(lib.kda_gate(_ptr(raw_g), ld_g, _ptr(raw_beta), ld_b, N, ctypes.byref(hd),
+                        _ptr(g_out), _ptr(beta_out), _stream(stream)), "kda_gate")
+    return g_out, beta_out
+
+
+def kda_packed_decode(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+                      state_indices, *, scale=None, l2_eps=1e-6, null_slot=-1, out=None,
+                      err_flags=None, stream=None):
+    """One decode token per sequence; returns (out bf16 [N, H*V], initial_state)."""
+    _, H, K, V = initial_state.shape
+    N = mixed_qkv.shape[0]
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(initial_state, state_indices, null_slot)
+    if state_indices.shape[0] < N:
+        raise ValueError("state_indices has fewer entries than sequences")
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    _check(lib.kda_packed_decode(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
+                                 _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
+                                 N, ctypes.byref(hd), ctypes.byref(st), _ptr(out), ld_out,
+                                 _ptr(err_flags), _stream(stream)), "kda_packed_decode")
+    return out, initial_state
+
+
+def kda_spec_verify(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+                    state_indices, tokens_per_req, *, scale=None, l2_eps=1e-6, null_slot=-1,
+                    out=None, err_flags=None, stream=None):
+    """Requests of tokens_per_req consecutive rows; returns (out, initial_state)."""
+    _, H, K, V = initial_state.shape
+    N = mixed_qkv.shape[0]
+    if N % tokens_per_req:
+        raise ValueError("the row count must be a multiple of tokens_per_req")
+    R = N // tokens_per_req
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(initial_state, state_indices, null_slot)
+    if state_indices.shape[0] < R:
+        raise ValueError("state_indices has fewer entries than requests")
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    _check(lib.kda_spec_verify(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
+                               _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
+                               R, int(tokens_per_req), ctypes.byref(hd), ctypes.byref(st),
+                               _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
+           "kda_spec_verify")
+    return out, initial_state
+
+
+def _host_cu(cu_seqlens, cu_seqlens_host):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor")
+    if cu_seqlens_host is None:
+        cu_seqlens_host = cu_seqlens.cpu()
+    return cu_seqlens_host.to(torch.int32).contiguous()
+
+
+def kda_chunk_prefill_workspace_bytes(cu_seqlens_host, H, K, V, chunk_size=64, num_seqs=None):
+    cu = cu_seqlens_host.to(torch.int32).contiguous()
+    n = cu.numel() - 1 if num_seqs is None else num_seqs
+    hd = KdaHeads(H=H, K=K, V=V, A_log=1, dt_bias=None, has_lower_bound=0, lower_bound=0.0,
+                  scale=1.0, l2_eps=0.0)
+    return int(lib.kda_chunk_prefill_workspace_bytes(ctypes.c_void_p(cu.data_ptr()), n,
+                                                     ctypes.byref(hd), chunk_size))
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None or workspace.numel() * workspace.element_size() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def kda_chunk_prefill(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+                      state_indices, cu_seqlens, *, cu_seqlens_host=None, chunk_size=64,
+                      scale=None, l2_eps=1e-6, null_slot=-1, out=None, workspace=None,
+                      err_flags=None, stream=None):
+    """Chunked varlen prefill; returns (out, initial_state)."""
+    _, H, K, V = initial_state.shape
+    N = mixed_qkv.shape[0]
+    cu_h = _host_cu(cu_seqlens, cu_seqlens_host)
+    S = cu_h.numel() - 1
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(initial_state, state_indices, null_slot)
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    nb = kda_chunk_prefill_workspace_bytes(cu_h, H, K, V, chunk_size)
+    ws, ws_bytes = _workspace(nb, mixed_qkv.device, workspace)
+    _check(lib.kda_chunk_prefill(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
+                                 _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
+                                 _ptr(cu_seqlens), ctypes.c_void_p(cu_h.data_ptr()), S,
+                                 int(chunk_size), ctypes.byref(hd), ctypes.byref(st), _ptr(ws),
+                                 ws_bytes, _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
+           "kda_chunk_prefill")
+    return out, initial_state
+
+
+def kda_mixed_batch(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+                    state_indices, cu_seqlens, num_decodes, *, cu_seqlens_host=None, scale=None,
+                    l2_eps=1e-6, null_slot=-1, out=None, workspace=None, err_flags=None,
+                    stream=None):
+    """Mixed batch: the first num_decodes sequences (length 1) take the recurrent decode
+    path, the rest the chunked prefill path; returns (out, initial_state)."""
+    _, H, K, V = initial_state.shape
+    N = mixed_qkv.shape[0]
+    cu_h = _host_cu(cu_seqlens, cu_seqlens_host)
+    S = cu_h.numel() - 1
+    P = S - num_decodes
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(initial_state, state_indices, null_slot)
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    nb = kda_chunk_prefill_workspace_bytes(cu_h[num_decodes:], H, K, V, 64, num_seqs=P)
+    ws, ws_bytes = _workspace(nb, mixed_qkv.device, workspace)
+    _check(lib.kda_mixed_batch(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
+                               _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
+                               _ptr(cu_seqlens), ctypes.c_void_p(cu_h.data_ptr()), int(num_decodes),
+                               int(P), ctypes.byref(hd), ctypes.byref(st), _ptr(ws), ws_bytes,
+                               _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
+           "kda_mixed_batch")
+    return out, initial_state

@@ -292,3 +292,73 @@ def mixed_batch(seed: int = 5, lower_bound=None) -> Workload:
 
 def num_chunks(lengths, chunk_size: int = 64) -> int:
     return int(sum(math.ceil(int(L) / chunk_size) for L in lengths))
+
+
+# ---------------------------------------------------------------------------
+# Device upload and dispatch of a workload to the matching library call
+# (torch is imported lazily so the generators stay importable without it).
+# ---------------------------------------------------------------------------
+
+def bf16_tensor(bits: np.ndarray, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bf16_to_f64(t) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+class DeviceWorkload:
+    """A Workload's tensors on a CUDA device, laid out as the library takes them."""
+
+    def __init__(self, w, device="cuda:0"):
+        import torch
+        self.w = w
+        self.device = device
+        self.mixed_qkv = bf16_tensor(w.mixed_qkv, device)
+        self.raw_g = bf16_tensor(w.raw_g, device)
+        self.raw_beta = bf16_tensor(w.raw_beta, device)
+        self.A_log = torch.from_numpy(w.A_log).to(device)
+        self.dt_bias = None if w.dt_bias is None else torch.from_numpy(w.dt_bias).to(device)
+        self.pool_flat = torch.from_numpy(w.pool).to(device)
+        self.index_buf = torch.from_numpy(np.ascontiguousarray(w.index_buf)).to(device)
+        self.cu = None if w.cu_seqlens is None else torch.from_numpy(w.cu_seqlens).to(device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def pool_view(self):
+        w = self.w
+        return self.pool_flat.as_strided((w.num_slots, w.H, w.K, w.V),
+                                         (w.slot_stride, w.K * w.V, w.V, 1))
+
+    def indices_view(self):
+        flat = self.index_buf.reshape(-1)
+        return flat.as_strided((self.w.num_entries,), (self.w.index_stride,))
+
+    def reset_pool(self):
+        import torch
+        self.pool_flat.copy_(torch.from_numpy(self.w.pool).to(self.device))
+        self.err.zero_()
+
+
+def run_gpu(dw: DeviceWorkload, kda, out=None, stream=None, workspace=None):
+    """Runs the library call the workload's kind names; returns the bf16 output tensor."""
+    import torch
+    w = dw.w
+    args = (dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, w.lower_bound,
+            dw.pool_view(), dw.indices_view())
+    kw = dict(scale=w.scale, l2_eps=w.eps, null_slot=w.null_slot, err_flags=dw.err, out=out,
+              stream=stream)
+    if w.kind == "decode":
+        o, _ = kda.kda_packed_decode(*args, **kw)
+    elif w.kind == "spec":
+        o, _ = kda.kda_spec_verify(*args, w.tokens_per_req, **kw)
+    elif w.kind == "prefill":
+        o, _ = kda.kda_chunk_prefill(*args, dw.cu, cu_seqlens_host=torch.from_numpy(w.cu_seqlens),
+                                     workspace=workspace, **kw)
+    elif w.kind == "mixed":
+        o, _ = kda.kda_mixed_batch(*args, dw.cu, w.num_decodes,
+                                   cu_seqlens_host=torch.from_numpy(w.cu_seqlens),
+                                   workspace=workspace, **kw)
+    else:
+        raise ValueError(w.kind)
+    return o

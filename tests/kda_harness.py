@@ -1,0 +1,80 @@
+"""Helpers for the GPU parity tests: upload a Workload, run one library call through
+the C ABI (via the ctypes binding), and compare with the fp64 oracle.
+
+Tolerances (the bar stated for this path): relative L2 <= 2e-3 and max-abs <= 1e-2
+on the bf16 outputs against the exact fp64 oracle, relative L2 <= 2e-3 on the
+updated fp32 states, no NaN/Inf anywhere, untouched pool slots byte-identical.
+For the fp32 recurrent kernels a tighter element-wise bound also holds: every
+output is within one bf16 ulp of the exact value (fp32 arithmetic carries ~1e-6
+relative error, far below bf16's 2^-8 spacing), plus a small absolute slack for
+outputs that are the difference of nearly equal terms.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from linear_attention_state_recurrent_gb300.workloads import (  # noqa: F401
+    DeviceWorkload, bf16_tensor, bf16_to_f64, run_gpu)
+from oracle import kda_oracle as ko
+
+REL_L2 = 2e-3
+MAX_ABS = 1e-2
+
+
+def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+def check(dw: DeviceWorkload, out: torch.Tensor, ref: ko.OracleResult, *, fp32_path: bool,
+          rows=None, label=""):
+    """Compares one call's GPU results with the oracle. Returns a dict of measured errors."""
+    w = dw.w
+    torch.cuda.synchronize()
+    h_lo, h_hi = ref.heads
+    V = w.V
+    cols = slice(h_lo * V, h_hi * V)
+    got = bf16_to_f64(out)[:, cols]
+    exp = ref.out[:, cols]
+    if rows is not None:
+        got, exp = got[rows], exp[rows]
+    assert np.all(np.isfinite(got)), f"{label}: non-finite outputs"
+    assert np.all(np.isfinite(exp)), f"{label}: oracle produced non-finite values"
+    res = {"out_rel_l2": rel_l2(got, exp), "out_max_abs": float(np.abs(got - exp).max(initial=0.0))}
+    assert res["out_rel_l2"] <= REL_L2, f"{label}: output rel L2 {res['out_rel_l2']:.3e}"
+    assert res["out_max_abs"] <= MAX_ABS, f"{label}: output max abs {res['out_max_abs']:.3e}"
+    if fp32_path:
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exp), 1e-30))) - 7)
+        slack = 1e-5 * max(np.abs(exp).max(initial=0.0), 1e-30)
+        bad = np.abs(got - exp) > ulp + slack
+        assert not bad.any(), f"{label}: {bad.sum()} outputs more than 1 bf16 ulp off"
+    # state pool
+    pool = dw.pool_flat.cpu().numpy()
+    orig = w.pool
+    written = set()
+    HKV = w.H * w.K * w.V
+    st_got, st_exp = [], []
+    for e in range(len(ref.slots)):
+        if ref.writes[e]:
+            s = int(ref.slots[e])
+            written.add(s)
+            g = pool[s, :HKV].reshape(w.H, w.K, w.V)[h_lo:h_hi].astype(np.float64)
+            st_got.append(g.reshape(-1))
+            st_exp.append(ref.final_states[e][h_lo:h_hi].reshape(-1))
+    if st_got:
+        sg, se = np.concatenate(st_got), np.concatenate(st_exp)
+        assert np.all(np.isfinite(sg)), f"{label}: non-finite states"
+        res["state_rel_l2"] = rel_l2(sg, se)
+        assert res["state_rel_l2"] <= REL_L2, f"{label}: state rel L2 {res['state_rel_l2']:.3e}"
+        if fp32_path:
+            assert res["state_rel_l2"] <= 1e-5, f"{label}: fp32 state rel L2 {res['state_rel_l2']:.3e}"
+    untouched = np.array(sorted(set(range(w.num_slots)) - written), dtype=np.int64)
+    if untouched.size:
+        assert np.array_equal(pool[untouched].view(np.uint32), orig[untouched].view(np.uint32)), \
+            f"{label}: an untouched slot changed"
+    for s in written:  # bytes beyond H*K*V inside a written slot stay untouched too
+        assert np.array_equal(pool[s, HKV:].view(np.uint32), orig[s, HKV:].view(np.uint32))
+    err = int(dw.err.cpu().item())
+    assert err == ref.err_flags, f"{label}: err flags {err} != {ref.err_flags}"
+    return res

@@ -1,0 +1,158 @@
+"""Host-only checks of the C-ABI library: it loads, exports every function that
+include/kda.h declares, and rejects bad arguments on the host with the right status
+before launching anything (no GPU needed: every call here fails validation first)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from linear_attention_state_recurrent_gb300 import build
+    build.build()
+    from linear_attention_state_recurrent_gb300 import kda as k
+    return k
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("kda_gate", "kda_packed_decode", "kda_spec_verify", "kda_chunk_prefill",
+              "kda_mixed_batch", "kda_chunk_prefill_workspace_bytes", "kda_last_error",
+              "kda_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kda):
+    lib = ctypes.CDLL(kda._LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libkda.so does not export {name}"
+    assert set(declared_functions()) == set(kda.EXPORTED)
+
+
+def test_status_strings(kda):
+    for code, name in ((0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARGUMENT"), (2, "KDA_ERR_UNSUPPORTED"),
+                       (3, "KDA_ERR_WORKSPACE"), (4, "KDA_ERR_CUDA")):
+        assert kda.lib.kda_status_string(code).decode() == name
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails before any launch
+
+
+def _heads(kda, H=2, K=128, V=128, A_log=FAKE, lb=None, scale=0.1, eps=1e-6):
+    return kda.KdaHeads(H=H, K=K, V=V, A_log=A_log.value if A_log else None, dt_bias=None,
+                        has_lower_bound=int(lb is not None), lower_bound=float(lb or 0.0),
+                        scale=scale, l2_eps=eps)
+
+
+def _state(kda, num_slots=8, slot_stride=2 * 128 * 128, index_stride=1, null_slot=-1, pool=FAKE):
+    return kda.KdaState(pool=pool.value if pool else None, num_slots=num_slots,
+                        slot_stride=slot_stride, indices=FAKE.value, index_stride=index_stride,
+                        null_slot=null_slot)
+
+
+def _decode(kda, hd, st, N=4, ld_qkv=3 * 2 * 128, ld_out=2 * 128, out=FAKE):
+    return kda.lib.kda_packed_decode(FAKE, ld_qkv, FAKE, 2 * 128, FAKE, 2, N, ctypes.byref(hd),
+                                     ctypes.byref(st), out, ld_out, None, None)
+
+
+@pytest.mark.parametrize("case,status,pattern", [
+    (dict(index_stride=0), 1, "index_stride"),
+    (dict(index_stride=-8), 1, "index_stride"),
+    (dict(slot_stride=100), 1, "slot_stride"),
+    (dict(slot_stride=2 * 128 * 128 + 2), 1, "multiple of 4"),
+    (dict(null_slot=8), 1, "null_slot"),
+    (dict(num_slots=0), 1, "num_slots"),
+    (dict(pool=None), 1, "pool"),
+])
+def test_decode_state_validation(kda, case, status, pattern):
+    hd = _heads(kda)
+    st = _state(kda, **case)
+    assert _decode(kda, hd, st) == status
+    assert re.search(pattern, kda.last_error())
+
+
+@pytest.mark.parametrize("case,status,pattern", [
+    (dict(K=96), 2, "K and V"),
+    (dict(V=256), 2, "K and V"),
+    (dict(H=0), 1, "H must"),
+    (dict(A_log=None), 1, "A_log"),
+    (dict(lb=float("nan")), 1, "lower_bound"),
+    (dict(lb=1.0), 1, "lower_bound"),
+    (dict(eps=-1.0), 1, "l2_eps"),
+    (dict(scale=float("inf")), 1, "scale"),
+])
+def test_decode_heads_validation(kda, case, status, pattern):
+    hd = _heads(kda, **case)
+    st = _state(kda, slot_stride=max(2 * 128 * 256, 1))
+    assert _decode(kda, hd, st) == status
+    assert re.search(pattern, kda.last_error())
+
+
+def test_decode_row_validation(kda):
+    hd, st = _heads(kda), _state(kda)
+    assert _decode(kda, hd, st, ld_qkv=100) == 1 and "ld_qkv" in kda.last_error()
+    assert _decode(kda, hd, st, ld_out=10) == 1 and "ld_out" in kda.last_error()
+    assert _decode(kda, hd, st, out=None) == 1
+    assert _decode(kda, hd, st, out=ctypes.c_void_p((1 << 20) + 2)) == 1 and "aligned" in kda.last_error()
+    assert _decode(kda, hd, st, N=-1) == 1
+
+
+def test_zero_sized_calls_are_noops(kda):
+    hd, st = _heads(kda), _state(kda)
+    assert _decode(kda, hd, st, N=0) == 0
+    assert kda.last_error() == ""
+
+
+def test_spec_verify_width_validation(kda):
+    hd, st = _heads(kda), _state(kda)
+    for T in (0, 65):
+        s = kda.lib.kda_spec_verify(FAKE, 768, FAKE, 256, FAKE, 2, 4, T, ctypes.byref(hd),
+                                    ctypes.byref(st), FAKE, 256, None, None)
+        assert s == 1 and "tokens_per_req" in kda.last_error()
+
+
+def test_chunk_prefill_validation(kda):
+    hd, st = _heads(kda), _state(kda)
+    cu = np.array([0, 5, 3], np.int32)
+    args = lambda cuh, cs=64, nd=0, npf=2: (FAKE, 768, FAKE, 256, FAKE, 2, FAKE,  # noqa: E731
+                                           cuh.ctypes.data_as(ctypes.c_void_p), nd, npf,
+                                           ctypes.byref(hd), ctypes.byref(st), None, 0, FAKE,
+                                           256, None, None)
+    assert kda.lib.kda_mixed_batch(*args(cu)) == 1 and "non-decreasing" in kda.last_error()
+    cu2 = np.array([0, 1, 3, 9], np.int32)
+    assert kda.lib.kda_mixed_batch(*args(cu2, nd=2, npf=1)) == 1 and "length 2" in kda.last_error()
+    s = kda.lib.kda_chunk_prefill(FAKE, 768, FAKE, 256, FAKE, 2, FAKE,
+                                  cu2.ctypes.data_as(ctypes.c_void_p), 3, 32, ctypes.byref(hd),
+                                  ctypes.byref(st), None, 0, FAKE, 256, None, None)
+    assert s == 2 and "chunk_size" in kda.last_error()
+
+
+def test_workspace_query_is_host_only(kda):
+    cu = np.array([0, 100, 300, 301], np.int32)
+    hd = _heads(kda)
+    n = kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
+                                                  ctypes.byref(hd), 64)
+    assert n >= 0
+    assert kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
+                                                     ctypes.byref(hd), 16) == 0
+    assert "chunk_size" in kda.last_error()
+
+
+def test_binding_rejects_2d_indices_without_gpu(kda):
+    torch = pytest.importorskip("torch")
+    idx = torch.zeros(4, 2, dtype=torch.int32)
+    pool = torch.zeros(2, 1, 32, 32)
+    with pytest.raises(ValueError, match="one-dimensional"):
+        kda.make_state(pool, idx)

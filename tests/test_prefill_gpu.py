@@ -1,0 +1,131 @@
+"""GPU parity of the chunked varlen prefill and the mixed decode+prefill batch against
+the fp64 oracle, through the C ABI. Lengths cover one and several chunks of 64 with
+ragged tails, the length-1 sequences that the chunk kernel of vLLM PR #50649 turned
+into NaN, and empty sequences."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_state_recurrent_gb300 import workloads as wl
+from oracle import kda_oracle as ko
+from tests import kda_harness as hx
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from linear_attention_state_recurrent_gb300 import kda as k
+    return k
+
+
+def _run(kda, w, label, heads=None, nthreads=0):
+    dw = hx.DeviceWorkload(w)
+    out = hx.run_gpu(dw, kda)
+    ref = ko.run(w, heads=heads, nthreads=nthreads)
+    return hx.check(dw, out, ref, fp32_path=False, label=label)
+
+
+@pytest.mark.parametrize("lower_bound", [None, -5.0])
+@pytest.mark.parametrize("stride", [1, 8])
+def test_prefill_ragged(kda, lower_bound, stride):
+    lengths = [1, 2, 63, 64, 65, 127, 129, 300]
+    w = wl.varlen_case(lengths, 2, 128, 128, seed=61 + stride, lower_bound=lower_bound,
+                       index_stride=stride)
+    _run(kda, w, f"prefill lb={lower_bound} s={stride}")
+
+
+@pytest.mark.parametrize("num_seqs", [1, 8, 32])
+def test_prefill_matrix(kda, num_seqs):
+    rng = np.random.default_rng(num_seqs)
+    lengths = [int(x) for x in rng.integers(1, 200, size=num_seqs)]
+    for lb in (-5.0, None):
+        for stride in (1, 8):
+            w = wl.varlen_case(lengths, 4, 128, 128, seed=num_seqs * 10 + stride, lower_bound=lb,
+                               index_stride=stride)
+            _run(kda, w, f"prefill n={num_seqs} lb={lb} s={stride}")
+
+
+@pytest.mark.parametrize("K,V", [(32, 32), (64, 128), (128, 64)])
+def test_prefill_dims(kda, K, V):
+    w = wl.varlen_case([5, 70, 130], 3, K, V, seed=K * 3 + V)
+    _run(kda, w, f"prefill K={K} V={V}")
+
+
+def test_prefill_empty_and_length_one(kda):
+    w = wl.varlen_case([0, 1, 0, 1, 1], 2, 128, 128, seed=5)
+    r = _run(kda, w, "empty/len1")
+    assert r["out_rel_l2"] < 2e-3
+
+
+def test_length_one_prefill_equals_decode(kda):
+    """The pages' mixed-batch NaN came from length-1 sequences in the chunk kernel."""
+    w = wl.varlen_case([1, 1, 1, 1], 4, 128, 128, seed=6)
+    dw = hx.DeviceWorkload(w)
+    a = hx.run_gpu(dw, kda).clone()
+    pa = dw.pool_flat.clone()
+    dw.reset_pool()
+    d = wl.Workload(**{**w.__dict__, "kind": "decode"})
+    dd = hx.DeviceWorkload(d)
+    b = hx.run_gpu(dd, kda)
+    assert torch.isfinite(a.float()).all()
+    ref = ko.run(d)
+    hx.check(dd, b, ref, fp32_path=True, label="decode side")
+    np.testing.assert_allclose(a.float().cpu().numpy(), b.float().cpu().numpy(), atol=2e-2)
+
+
+def test_chunked_prefill_config(kda):
+    """8 sequences of the seed-1 lengths (33,494 tokens), H=32, K=V=128; the oracle
+    samples heads 0..3 of every sequence."""
+    w = wl.chunked_prefill(None)
+    _run(kda, w, "chunked prefill 8 seqs", heads=(0, 4))
+
+
+def test_chunked_prefill_config_lower_bound(kda):
+    w = wl.chunked_prefill(-5.0)
+    _run(kda, w, "chunked prefill lb", heads=(28, 32))
+
+
+def test_split_prefill_resumes_from_slot(kda):
+    """A prompt chunked across two calls equals one call (state carried in the slot)."""
+    w = wl.varlen_case([300], 2, 128, 128, seed=8)
+    dw = hx.DeviceWorkload(w)
+    one = hx.run_gpu(dw, kda).float().cpu().numpy()
+    pool_one = dw.pool_flat.clone()
+    dw.reset_pool()
+    cut = 130
+    cu_a = torch.tensor([0, cut], dtype=torch.int32)
+    cu_b = torch.tensor([0, 300 - cut], dtype=torch.int32)
+    oa, _ = kda.kda_chunk_prefill(dw.mixed_qkv[:cut], dw.raw_g[:cut], dw.raw_beta[:cut], dw.A_log,
+                                  dw.dt_bias, None, dw.pool_view(), dw.indices_view(), cu_a.cuda(),
+                                  scale=w.scale)
+    ob, _ = kda.kda_chunk_prefill(dw.mixed_qkv[cut:], dw.raw_g[cut:], dw.raw_beta[cut:], dw.A_log,
+                                  dw.dt_bias, None, dw.pool_view(), dw.indices_view(), cu_b.cuda(),
+                                  scale=w.scale)
+    two = torch.cat([oa, ob]).float().cpu().numpy()
+    assert hx.rel_l2(two, one) < 2e-3
+    s = int(w.indices()[0])
+    assert hx.rel_l2(dw.pool_flat[s].cpu().numpy(), pool_one[s].cpu().numpy()) < 2e-3
+
+
+def test_mixed_batch_config(kda):
+    """96 length-1 decodes + 4 prefills of 4096, index stride 4; the oracle samples
+    heads 0..3 and all decodes."""
+    w = wl.mixed_batch()
+    _run(kda, w, "mixed batch", heads=(0, 4))
+
+
+@pytest.mark.parametrize("lower_bound", [-5.0, None])
+@pytest.mark.parametrize("stride", [1, 8])
+def test_mixed_batch_matrix(kda, lower_bound, stride):
+    lengths = [1] * 8 + [1, 77, 200]
+    w = wl.varlen_case(lengths, 4, 128, 128, seed=90 + stride, lower_bound=lower_bound,
+                       index_stride=stride, num_decodes=8, kind="mixed")
+    _run(kda, w, f"mixed lb={lower_bound} s={stride}")
+
+
+def test_mixed_batch_rejects_long_decode(kda):
+    w = wl.varlen_case([1, 2, 5], 2, 128, 128, seed=3, num_decodes=2, kind="mixed")
+    dw = hx.DeviceWorkload(w)
+    with pytest.raises(ValueError, match="length"):
+        hx.run_gpu(dw, kda)
