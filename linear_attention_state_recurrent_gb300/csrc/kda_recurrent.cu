@@ -57,8 +57,10 @@ __global__ void __launch_bounds__(256) gate_kernel(Params p, int K, int64_t N, f
 // ---------------------------------------------------------------------------
 enum RowMode { kRowsDecode = 0, kRowsSpec = 1, kRowsVarlen = 2 };
 
+// 8 CTAs per SM (64 registers per thread): the decode is bound by how many state bytes
+// are in flight, and at 8 resident CTAs each SM keeps 128 KiB of loads outstanding.
 template <int K, int V>
-__global__ void __launch_bounds__(128) recurrent_kernel(Params p, int mode, int T,
+__global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, int T,
                                                         const int32_t *cu, int64_t entry_base)
 {
     constexpr int VT = 32;              // value columns per CTA
