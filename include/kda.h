@@ -74,6 +74,7 @@ extern "C" {
 #define KDA_ERR_CUDA 4             /* a CUDA runtime call or launch failed */
 
 #define KDA_ERRFLAG_SLOT_RANGE 1u /* bit 0 of *err_flags: a state index was >= num_slots */
+#define KDA_ERRFLAG_TIMEOUT 2u    /* bit 1: a device-side wait gave up after ~2 s (results invalid) */
 
 /* Per-layer head parameters shared by every call. */
 typedef struct kda_heads {
@@ -153,7 +154,8 @@ size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t
  * row, and written back once. cu_seqlens (device) and cu_seqlens_host (host) must
  * hold the same non-decreasing, non-negative int32 values; the host copy sizes the
  * launch; mixed_qkv, raw_g, raw_beta and out must hold cu_seqlens[num_seqs] rows.
- * chunk_size must be 64. `workspace` (device, 256-byte aligned) must
+ * chunk_size must be 64. mixed_qkv and raw_g must be 16-byte aligned with ld_qkv and
+ * ld_g multiples of 8 (the tensor-core path reads them in 16-byte vectors). `workspace` (device, 256-byte aligned) must
  * hold kda_chunk_prefill_workspace_bytes(...) bytes; it may be NULL when that is 0.
  * Zero-length sequences are allowed: their slot is left untouched.
  */

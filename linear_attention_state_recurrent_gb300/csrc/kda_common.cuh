@@ -22,6 +22,7 @@ struct Params {
 };
 
 constexpr uint32_t kErrSlotRange = 1u;
+constexpr uint32_t kErrTimeout = 2u;   // a bounded wait on the tensor cores gave up
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b)
 {

@@ -129,3 +129,34 @@ def test_mixed_batch_rejects_long_decode(kda):
     dw = hx.DeviceWorkload(w)
     with pytest.raises(ValueError, match="length"):
         hx.run_gpu(dw, kda)
+
+
+@pytest.mark.parametrize("A_log", [[3.0, -1.0, 0.5, 2.5], [4.0, 4.0, 4.0, 4.0]])
+def test_prefill_strong_decay(kda, A_log):
+    """Heads whose channels decay by more than 40 nats within 8 rows take the pairwise
+    path for the diagonal blocks; the others the tensor-core path. Both match the oracle."""
+    w = wl.varlen_case([1, 40, 64, 150, 333], 4, 128, 128, seed=17)
+    w.A_log = np.array(A_log, dtype=np.float32)
+    _run(kda, w, f"strong decay A_log={A_log}")
+
+
+def test_prefill_weak_decay_long(kda):
+    """Near-unit decay (A_log = -6) over 2000 rows: the state carries information across
+    many chunks, so errors in the chain would accumulate."""
+    w = wl.varlen_case([2000, 700], 2, 128, 128, seed=19)
+    w.A_log = np.full(2, -6.0, dtype=np.float32)
+    _run(kda, w, "weak decay long")
+
+
+def test_prefill_repeat_bit_identical(kda):
+    w = wl.varlen_case([300, 129, 64], 4, 128, 128, seed=23)
+    dw = hx.DeviceWorkload(w)
+    first = hx.run_gpu(dw, kda).clone()
+    pool_first = dw.pool_flat.clone()
+    ref_pool = torch.from_numpy(w.pool).cuda()
+    out = torch.empty_like(first)
+    for _ in range(20):
+        dw.pool_flat.copy_(ref_pool)
+        hx.run_gpu(dw, kda, out=out)
+        assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+    assert torch.equal(dw.pool_flat.view(torch.int32), pool_first.view(torch.int32))
