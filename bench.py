@@ -236,6 +236,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--workload", choices=["decode", "prefill", "spec", "mixed"], default="decode",
+                    help="decode (default) is the headline line; the others time one row alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -251,6 +253,9 @@ def main():
     dev = f"cuda:{local}"
     stream = torch.cuda.current_stream()
     pk = peaks()
+    if args.workload != "decode":
+        run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local)
+        return
 
     # ---- headline: serving decode ----
     w = wl.serving_decode(-5.0)
@@ -363,6 +368,51 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
+    """One non-headline row alone: chunked prefill, spec-verify or mixed batch, timed over
+    --steps calls after --warmup calls (the same calls the secondary fields time)."""
+    if args.workload == "prefill":
+        w = wl.chunked_prefill(None)
+        metric, unit = "chunk-prefill tokens/s", "tokens/s"
+    elif args.workload == "mixed":
+        w = wl.mixed_batch()
+        metric, unit = "mixed-batch tokens/s", "tokens/s"
+    else:
+        w = wl.spec_verify()
+        metric, unit = "spec-verify state-bytes GB/s", "GB/s"
+    dw = wl.DeviceWorkload(w, dev)
+    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        wl.run_gpu(dw, kda, out=out)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            wl.run_gpu(dw, kda, out=out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
+    if unit == "tokens/s":
+        value = w.N * world / (ms * 1e-3)
+    else:
+        value = w.state_bytes_per_call() * world / (ms * 1e-3) / 1e9
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.N, "H": w.H, "K": w.K, "V": w.V},
+            "clocks": clk.summary(), "gpu_launches": args.steps * (2 if args.workload == "mixed" else 1)}
+    if args.workload == "prefill":
+        flops = prefill_alg_flops(wl.PREFILL_LENGTHS_SEED1, w.H, w.K, w.V)
+        line["tflops_algorithmic"] = flops / (ms * 1e-3) / 1e12
+        line["frac_bf16_peak"] = line["tflops_algorithmic"] / pk["bf16_tflops"]
+        line["frac_hbm_min_bytes"] = prefill_min_bytes(w) / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def time_calls(torch, fn, stream, n, warmup=2):
