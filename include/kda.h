@@ -154,8 +154,8 @@ size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t
  * row, and written back once. cu_seqlens (device) and cu_seqlens_host (host) must
  * hold the same non-decreasing, non-negative int32 values; the host copy sizes the
  * launch; mixed_qkv, raw_g, raw_beta and out must hold cu_seqlens[num_seqs] rows.
- * chunk_size must be 64. mixed_qkv and raw_g must be 16-byte aligned with ld_qkv and
- * ld_g multiples of 8 (the tensor-core path reads them in 16-byte vectors). `workspace` (device, 256-byte aligned) must
+ * chunk_size must be 64. mixed_qkv, raw_g and out must be 16-byte aligned with ld_qkv,
+ * ld_g and ld_out multiples of 8 (the tensor-core path moves them in 16-byte vectors). `workspace` (device, 256-byte aligned) must
  * hold kda_chunk_prefill_workspace_bytes(...) bytes; it may be NULL when that is 0.
  * Zero-length sequences are allowed: their slot is left untouched.
  */

@@ -6,7 +6,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "../../include/kda.h"
+#include "kda.h"
 #include "kda_launch.h"
 
 namespace {
@@ -249,9 +249,11 @@ static int chunk_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
     if (num_decodes < 0 || num_prefills < 0)
         return fail(KDA_ERR_INVALID_ARGUMENT, "sequence counts must be >= 0");
     if (chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 64 (got %d)", chunk_size);
-    if (!aligned(mixed_qkv, 16) || !aligned(raw_g, 16) || (ld_qkv % 8) != 0 || (ld_g % 8) != 0)
+    if (!aligned(mixed_qkv, 16) || !aligned(raw_g, 16) || !aligned(out, 16) || (ld_qkv % 8) != 0 ||
+        (ld_g % 8) != 0 || (ld_out % 8) != 0)
         return fail(KDA_ERR_INVALID_ARGUMENT,
-                    "%s: mixed_qkv and raw_g must be 16-byte aligned with ld_qkv and ld_g multiples of 8", name);
+                    "%s: mixed_qkv, raw_g and out must be 16-byte aligned with ld_qkv, ld_g and ld_out "
+                    "multiples of 8", name);
     const int64_t n = num_decodes + num_prefills;
     if (n == 0) return ok();
     if (!cu_seqlens) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");

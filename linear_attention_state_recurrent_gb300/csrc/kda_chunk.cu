@@ -27,7 +27,7 @@
 // fp16 (11-bit significand, round to nearest) carries the same precision as tf32
 // with round to nearest; bf16 operands would exceed the 2e-3 relative error bar.
 //
-// One CTA (256 threads) owns one (sequence, head) chain; CTAs are ordered longest
+// One CTA (512 threads) owns one (sequence, head) chain; CTAs are ordered longest
 // sequence first.
 #include <algorithm>
 #include <numeric>
@@ -43,7 +43,7 @@ namespace chunk {
 constexpr int C = 64;
 constexpr int KD = 128;
 constexpr int VD = 128;
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr float kHalfSpan = 40.f;   // largest in-half-block decay served by the tf32 path
 constexpr int kMaxOrder = 1024;
 
@@ -62,7 +62,8 @@ constexpr uint32_t SM_GC = SM_TOT + 4096;  // fp32 [128] e^{b_last}
 constexpr uint32_t SM_BLAST = SM_GC + 512; // fp32 [128] b_last
 constexpr uint32_t SM_BETA = SM_BLAST + 512;  // fp32 [64]
 constexpr uint32_t SM_DTB = SM_BETA + 256;    // fp32 [128] dt_bias of this head
-constexpr uint32_t SM_MBAR = SM_DTB + 512;
+constexpr uint32_t SM_NRM = SM_DTB + 512;     // fp32 [2][64][2] half-row |q|^2, |k|^2
+constexpr uint32_t SM_MBAR = SM_NRM + 1024;
 constexpr uint32_t SM_TMEMP = SM_MBAR + 8;
 constexpr uint32_t SMEM_BYTES = SM_TMEMP + 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -76,6 +77,8 @@ constexpr int AP = 68;                         // fp32 row pitch of AMAT / TMAT
 constexpr uint32_t SM_SA = SM_DIAGA;           // fp16 [128 x 128] S^T
 constexpr uint32_t SM_YA = SM_DIAGA + 32768;   // fp16 [128 x 64]  (beta Y)^T
 constexpr uint32_t SM_UA = SM_DIAGA + 49152;   // fp16 [128 x 64]  U^T
+constexpr uint32_t SM_OTILE = SM_OFFB;         // bf16 [64][OT_PITCH] output rows
+constexpr int OT_PITCH = 136;                  // bf16 row pitch (272 B: 16-byte aligned rows)
 // flagged-chunk stash (fp32 [64][128] each)
 constexpr uint32_t SM_STK = SM_DIAGA;
 constexpr uint32_t SM_STQ = SM_DIAGA + 32768;
@@ -101,13 +104,16 @@ struct Args {
     int32_t order[kMaxOrder];
 };
 
-// constants table entry (block s, constant k, channel c), laid out so that the four
-// 32-channel quarters of one 4-channel group are adjacent (conflict-free LDS.128)
+// constants table entry (block s, constant k, channel c). A phase-A warp covers one
+// 64-channel half; its four 16-channel groups read the same relative 4-channel slot,
+// so those four slots sit side by side (one conflict-free LDS.128 per warp).
 __device__ __forceinline__ uint32_t tab_off(int s, int k, int c)
 {
-    const int q = c >> 5, g = (c & 31) >> 2, e = c & 3;
-    return static_cast<uint32_t>(((((s * 7 + k) * 8 + g) * 4 + q) * 4 + e) * 4);
+    const int ch = c >> 6, grp = (c >> 4) & 3, g8 = (c >> 3) & 1, h4 = (c >> 2) & 1, e = c & 3;
+    return static_cast<uint32_t>((((((s * 7 + k) * 2 + ch) * 2 + g8) * 2 + h4) * 4 + grp) * 16 + e * 4);
 }
+
+__device__ __forceinline__ uint32_t off_b_base(int R) { return R == 1 ? 0 : (R == 2 ? 16 : 48); }
 
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v)
 {
@@ -155,7 +161,7 @@ __device__ __forceinline__ uint4 pack4_tf32(const float *v)
 
 // ---------------------------------------------------------------------------
 // Phase C: T = (I + A)^-1 for the strictly lower 64x64 A in AMAT (fp32, pitch AP),
-// by 16x16 diagonal-block inverses and two levels of block doubling.
+// by 16x16 diagonal-block inverses and two levels of block doubling (512 threads).
 // ---------------------------------------------------------------------------
 __device__ void solve_T(unsigned char *smem, int tid)
 {
@@ -179,139 +185,131 @@ __device__ void solve_T(unsigned char *smem, int tid)
     __syncthreads();
     // level 2: within each 32-block p, X = A_10 T_00 then T_10 = -T_11 X (16x16)
     {
-        const int p = tid >> 7, r = (tid >> 3) & 15, j = (tid & 7) * 2, o = 32 * p;
-        float x0 = 0.f, x1 = 0.f;
+        const int p = tid >> 8, r = (tid >> 4) & 15, j = tid & 15, o = 32 * p;
+        float x = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; m++) {
-            const float a = A[(o + 16 + r) * AP + o + m];
-            x0 += a * T[(o + m) * AP + o + j];
-            x1 += a * T[(o + m) * AP + o + j + 1];
-        }
-        X[(p * 16 + r) * 17 + j] = x0;
-        X[(p * 16 + r) * 17 + j + 1] = x1;
+        for (int m = 0; m < 16; m++) x += A[(o + 16 + r) * AP + o + m] * T[(o + m) * AP + o + j];
+        X[(p * 16 + r) * 17 + j] = x;
     }
     __syncthreads();
     {
-        const int p = tid >> 7, r = (tid >> 3) & 15, j = (tid & 7) * 2, o = 32 * p;
-        float y0 = 0.f, y1 = 0.f;
+        const int p = tid >> 8, r = (tid >> 4) & 15, j = tid & 15, o = 32 * p;
+        float y = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; m++) {
-            const float t = (m <= r) ? T[(o + 16 + r) * AP + o + 16 + m] : 0.f;
-            y0 += t * X[(p * 16 + m) * 17 + j];
-            y1 += t * X[(p * 16 + m) * 17 + j + 1];
-        }
-        T[(o + 16 + r) * AP + o + j] = -y0;
-        T[(o + 16 + r) * AP + o + j + 1] = -y1;
+        for (int m = 0; m < 16; m++)
+            if (m <= r) y += T[(o + 16 + r) * AP + o + 16 + m] * X[(p * 16 + m) * 17 + j];
+        T[(o + 16 + r) * AP + o + j] = -y;
     }
     __syncthreads();
     // level 3: X = A_ba T_a (32x32), T_ba = -T_b X
     {
-        const int r = tid >> 3, j = (tid & 7) * 4;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r = tid >> 4, j = (tid & 15) * 2;
+        float x0 = 0.f, x1 = 0.f;
 #pragma unroll 8
         for (int m = 0; m < 32; m++) {
             const float a = A[(32 + r) * AP + m];
-#pragma unroll
-            for (int u = 0; u < 4; u++) x[u] += (m >= j + u) ? a * T[m * AP + j + u] : 0.f;
+            if (m >= j) x0 += a * T[m * AP + j];
+            if (m >= j + 1) x1 += a * T[m * AP + j + 1];
         }
-#pragma unroll
-        for (int u = 0; u < 4; u++) X[r * 36 + j + u] = x[u];
+        X[r * 36 + j] = x0;
+        X[r * 36 + j + 1] = x1;
     }
     __syncthreads();
     {
-        const int r = tid >> 3, j = (tid & 7) * 4;
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r = tid >> 4, j = (tid & 15) * 2;
+        float y0 = 0.f, y1 = 0.f;
 #pragma unroll 8
         for (int m = 0; m < 32; m++) {
-            const float t = (m <= r) ? T[(32 + r) * AP + 32 + m] : 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; u++) y[u] += t * X[m * 36 + j + u];
+            if (m <= r) {
+                const float t = T[(32 + r) * AP + 32 + m];
+                y0 += t * X[m * 36 + j];
+                y1 += t * X[m * 36 + j + 1];
+            }
         }
-#pragma unroll
-        for (int u = 0; u < 4; u++) T[(32 + r) * AP + j + u] = -y[u];
+        T[(32 + r) * AP + j] = -y0;
+        T[(32 + r) * AP + j + 1] = -y1;
     }
     __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
-// Phase C1 helper: assemble one row of A (K rows) or Aqk (Q rows) from the off-
-// diagonal and diagonal TMEM results. HALF 0: rows 0..31, HALF 1: rows 32..63.
+// Phase C1: one 16-column slice of one row of A (K rows, scaled by beta_r) or Aqk
+// (Q rows), from the off-diagonal and diagonal Gram results in TMEM. Thread roles:
+// TMEM lane quarter qd = warp & 3 (lanes 0..63 are the K rows, 64..127 the Q rows),
+// column slice k4 = warp >> 2.
 // ---------------------------------------------------------------------------
-template <int HALF>
-__device__ void assemble_rows(unsigned char *smem, uint32_t tmem_lane, int warp, int lane,
-                              bool flagged)
+__device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, int lane, bool flagged)
 {
-    constexpr int NXO = HALF == 0 ? 16 : 80;         // off-diagonal columns this warp reads
-    constexpr int XO0 = HALF == 0 ? 0 : 16;          // first off-diagonal column
-    const bool qpart = warp >= 2;
-    const int r = 32 * HALF + lane;                  // chunk row
-    const int s = r >> 4;                            // row block
-    float xo[NXO], xd[32];
-#pragma unroll
-    for (int cc = 0; cc < NXO; cc += 16) {
-        float v[16];
-        tc::tmem_ld16(tmem_lane + TM_XOFF + XO0 + cc, v);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 16; u++) xo[cc + u] = v[u];
-    }
-    if (!flagged) {
-#pragma unroll
-        for (int cc = 0; cc < 32; cc += 16) {
-            float v[16];
-            tc::tmem_ld16(tmem_lane + TM_XDIAG + 32 * HALF + cc, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 16; u++) xd[cc + u] = v[u];
-        }
-    } else {
-        // pairwise in fp32 from the stash: xd[i - 32*HALF] for i in row r's block
+    const int qd = warp & 3, k4 = warp >> 2;
+    const bool qpart = qd >= 2;
+    const int r = 32 * (qd & 1) + lane;   // chunk row
+    const int s = r >> 4;                 // row block of this lane
+    const int s0 = 2 * (qd & 1);          // row blocks of this warp: s0, s0 + 1
+    const int i0 = 16 * k4;               // first output column
+    float off0[16], off1[16], dg[16];
+    // warp-collective loads: every lane loads the same columns, then keeps its own
+    if (k4 < s0) tc::tmem_ld16(tlane + TM_XOFF + off_b_base(s0) + i0, off0);
+    if (k4 < s0 + 1) tc::tmem_ld16(tlane + TM_XOFF + off_b_base(s0 + 1) + i0, off1);
+    if (!flagged && (k4 == s0 || k4 == s0 + 1)) tc::tmem_ld16(tlane + TM_XDIAG + i0, dg);
+    tc::tmem_ld_wait();
+    if (flagged && k4 == s) {
+        // pairwise in fp32 from the stash for the diagonal block
         const float *stk = reinterpret_cast<const float *>(smem + SM_STK);
         const float *stq = reinterpret_cast<const float *>(smem + SM_STQ);
         const float *stb = reinterpret_cast<const float *>(smem + SM_STB);
         const float *xr = (qpart ? stq : stk) + r * KD;
         const float *br = stb + r * KD;
-#pragma unroll
-        for (int u = 0; u < 32; u++) {
-            const int i = 32 * HALF + u;
+        for (int u = 0; u < 16; u++) {
+            const int i = i0 + u;
             float acc = 0.f;
-            if ((i >> 4) == s && i <= r) {
+            if (i <= r) {
                 const float *ki = stk + i * KD;
                 const float *bi = stb + i * KD;
                 for (int c = 0; c < KD; c++) acc += xr[c] * ki[c] * __expf(br[c] - bi[c]);
             }
-            xd[u] = acc;
+            dg[u] = acc;
         }
     }
-    const float beta = reinterpret_cast<const float *>(smem + SM_BETA)[r];
-    float a[64];
+    const float beta = qpart ? 1.f : reinterpret_cast<const float *>(smem + SM_BETA)[r];
+    float a[16];
 #pragma unroll
-    for (int i = 0; i < 64; i++) {
+    for (int u = 0; u < 16; u++) {
+        const int i = i0 + u;
         float v = 0.f;
-        const bool diag_ok = qpart ? (i <= r) : (i < r);
-        if (HALF == 0) {
-            if (i < 16) v = (s == 1) ? xo[i] : (diag_ok ? xd[i] : 0.f);
-            else if (i < 32) v = (s == 1 && diag_ok) ? xd[i] : 0.f;
-        } else {
-            if (i < 32) v = (s == 2) ? xo[i] : xo[32 + i];
-            else if (i < 48) v = (s == 3) ? xo[32 + i] : (diag_ok ? xd[i - 32] : 0.f);
-            else v = (s == 3 && diag_ok) ? xd[i - 32] : 0.f;
-        }
-        a[i] = qpart ? v : v * beta;
+        if (k4 < s) v = (s == s0) ? off0[u] : off1[u];
+        else if (k4 == s) v = (qpart ? (i <= r) : (i < r)) ? dg[u] : 0.f;
+        a[u] = v * beta;
     }
     if (!qpart) {
-        float *Arow = reinterpret_cast<float *>(smem + SM_AMAT) + r * AP;
+        float *Arow = reinterpret_cast<float *>(smem + SM_AMAT) + r * AP + i0;
 #pragma unroll
-        for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(Arow + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+        for (int u = 0; u < 16; u += 4) *reinterpret_cast<float4 *>(Arow + u) = make_float4(a[u], a[u + 1], a[u + 2], a[u + 3]);
     } else {
         const uint32_t base = tc::smem_addr(smem + SM_SB);
-#pragma unroll
-        for (int i = 0; i < 64; i += 8) st_shared_u4(base + tc::core_offset(r, i, 64, 2), pack8_f16(a + i));
+        st_shared_u4(base + tc::core_offset(r, i0, 64, 2), pack8_f16(a));
+        st_shared_u4(base + tc::core_offset(r, i0 + 8, 64, 2), pack8_f16(a + 8));
     }
 }
 
+// raw phase-A inputs of one thread: 16 channels of q, k and raw_g for one row
+struct RowIn {
+    uint4 q[2], k[2], g[2];
+    uint16_t beta;
+};
+
+__device__ __forceinline__ void load_row_inputs(const Params &p, int64_t row, int h, int cb, int64_t HK, RowIn &in)
+{
+    const uint4 *qp = reinterpret_cast<const uint4 *>(p.qkv + row * p.ld_qkv + h * KD + cb);
+    const uint4 *kp = reinterpret_cast<const uint4 *>(p.qkv + row * p.ld_qkv + HK + h * KD + cb);
+    const uint4 *gp = reinterpret_cast<const uint4 *>(p.rg + row * p.ld_g + h * KD + cb);
+    in.q[0] = qp[0]; in.q[1] = qp[1];
+    in.k[0] = kp[0]; in.k[1] = kp[1];
+    in.g[0] = gp[0]; in.g[1] = gp[1];
+    in.beta = p.rb[row * p.ld_beta + h];
+}
+
 // ---------------------------------------------------------------------------
-// The kernel
+// The kernel (512 threads, one (sequence, head) chain per CTA)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Args args)
 {
@@ -352,57 +350,53 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     bool ok = true;
 
     // thread roles
-    const int jv = 32 * (warp & 3) + lane;   // phase D: value column (TMEM lane)
-    const int hv = warp >> 2;                // phase D: which half of the columns / rows
-    const int ir = lane & 7, iq = lane >> 3; // phase A: row within warp, channel quarter
-    const int ra = 8 * warp + ir;            // phase A: chunk row
+    const int jv = 32 * (warp & 3) + lane;  // TMEM lane: value column j in phase D
+    const int k4 = warp >> 2;               // column slice (0..3) of TMEM work
+    const int ir = lane & 7, iq = lane >> 3;
+    const int rga = warp & 7;               // phase A: rows 8*rga .. 8*rga+7
+    const int ra = 8 * rga + ir;            // phase A: chunk row
+    const int cb = 64 * (warp >> 3) + 16 * iq;  // phase A: first of 16 channels
+    const int sA = rga >> 1, hfA = rga & 1; // phase A: row block, half of the block
 
-    // ---- S0 -> TMEM (S^T: lane j, column c) ----
+    // ---- S0 -> TMEM (S^T: lane j, columns c in this thread's 32-column slice) ----
     {
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 16) {
+        for (int cc = 0; cc < 32; cc += 16) {
             float v[16];
+            const int c = 32 * k4 + cc;
 #pragma unroll
             for (int u = 0; u < 16; u++)
-                v[u] = has_state ? tile[static_cast<int64_t>(64 * hv + cc + u) * VD + jv] : 0.f;
-            tc::tmem_st16(tlane + TM_S + 64 * hv + cc, v);
+                v[u] = has_state ? tile[static_cast<int64_t>(c + u) * VD + jv] : 0.f;
+            tc::tmem_st16(tlane + TM_S + c, v);
         }
         tc::tmem_st_wait();
     }
 
     const float expA = __expf(p.A_log[h]);
     const float *dtb_s = reinterpret_cast<const float *>(smem + SM_DTB);
+    RowIn in;
+    if (ra < row1 - row0) load_row_inputs(p, row0 + ra, h, cb, HK, in);
 
     for (int64_t c0 = row0; c0 < row1; c0 += C) {
         const int n = static_cast<int>((row1 - c0) < C ? (row1 - c0) : C);
 
         // ================= Phase A: gate, norms, cumulative decay, operands =================
-        float qv[32], kv[32], bv[32];
+        float qv[16], kv[16], bv[16];
         float beta_r = 0.f;
         const bool valid = ra < n;
-        {
-            const int64_t row = c0 + ra;
-            if (valid) {
-                const uint4 *qp = reinterpret_cast<const uint4 *>(p.qkv + row * p.ld_qkv + h * KD + 32 * iq);
-                const uint4 *kp = reinterpret_cast<const uint4 *>(p.qkv + row * p.ld_qkv + HK + h * KD + 32 * iq);
-                const uint4 *gp = reinterpret_cast<const uint4 *>(p.rg + row * p.ld_g + h * KD + 32 * iq);
+        if (valid) {
+            unpack_bf16x8(in.q[0], qv); unpack_bf16x8(in.q[1], qv + 8);
+            unpack_bf16x8(in.k[0], kv); unpack_bf16x8(in.k[1], kv + 8);
+            unpack_bf16x8(in.g[0], bv); unpack_bf16x8(in.g[1], bv + 8);
+            beta_r = sigmoid_f(bf16_to_f32(in.beta));
+        } else {
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    unpack_bf16x8(qp[u], qv + 8 * u);
-                    unpack_bf16x8(kp[u], kv + 8 * u);
-                    unpack_bf16x8(gp[u], bv + 8 * u);
-                }
-                beta_r = sigmoid_f(bf16_to_f32(p.rb[row * p.ld_beta + h]));
-            } else {
-#pragma unroll
-                for (int u = 0; u < 32; u++) { qv[u] = 0.f; kv[u] = 0.f; bv[u] = 0.f; }
-            }
+            for (int u = 0; u < 16; u++) { qv[u] = 0.f; kv[u] = 0.f; bv[u] = 0.f; }
         }
-        // gate (g <= 0; zero on padding rows) and row norms
         float qq = 0.f, kk = 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; u++) {
-            bv[u] = valid ? gate_log_decay(bv[u] + dtb_s[32 * iq + u], expA, p.has_lb, p.lb) : 0.f;
+        for (int u = 0; u < 16; u++) {
+            bv[u] = valid ? gate_log_decay_fast(bv[u] + dtb_s[cb + u], expA, p.has_lb, p.lb) : 0.f;
             qq += qv[u] * qv[u];
             kk += kv[u] * kv[u];
         }
@@ -410,14 +404,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         qq += __shfl_xor_sync(0xffffffffu, qq, 16);
         kk += __shfl_xor_sync(0xffffffffu, kk, 8);
         kk += __shfl_xor_sync(0xffffffffu, kk, 16);
-        {
-            const float rq = p.scale * rsqrtf(qq + p.eps), rk = rsqrtf(kk + p.eps);
+        float *nrm = reinterpret_cast<float *>(smem + SM_NRM);   // [half][row][2]
+        if (iq == 0) *reinterpret_cast<float2 *>(nrm + ((warp >> 3) * 64 + ra) * 2) = make_float2(qq, kk);
+        // in-warp inclusive scan over the 8 rows (lanes ir = 0..7 of the same channel group)
 #pragma unroll
-            for (int u = 0; u < 32; u++) { qv[u] *= rq; kv[u] *= rk; }
-        }
-        // in-warp inclusive scan over the 8 rows (lanes ir = 0..7 of the same quarter)
-#pragma unroll
-        for (int u = 0; u < 32; u++) {
+        for (int u = 0; u < 16; u++) {
             float v = bv[u];
 #pragma unroll
             for (int d = 1; d < 8; d <<= 1) {
@@ -429,10 +420,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         float *tot = reinterpret_cast<float *>(smem + SM_TOT);
         if (ir == 7) {
 #pragma unroll
-            for (int u = 0; u < 32; u += 4)
-                *reinterpret_cast<float4 *>(tot + warp * KD + 32 * iq + u) = make_float4(bv[u], bv[u + 1], bv[u + 2], bv[u + 3]);
+            for (int u = 0; u < 16; u += 4)
+                *reinterpret_cast<float4 *>(tot + rga * KD + cb + u) = make_float4(bv[u], bv[u + 1], bv[u + 2], bv[u + 3]);
         }
-        if (iq == 0) reinterpret_cast<float *>(smem + SM_BETA)[ra] = beta_r;
+        if (warp < 8 && iq == 0) reinterpret_cast<float *>(smem + SM_BETA)[ra] = beta_r;
         __syncthreads();
 
         // per-channel constants (threads 0..127, one channel each)
@@ -473,91 +464,110 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         const bool flagged = __syncthreads_or(flag) != 0;
 
         {
-            const int s = warp >> 1, hf = warp & 1;
+            // full-row norms from the two channel halves
+            const float2 n0 = *reinterpret_cast<const float2 *>(nrm + ra * 2);
+            const float2 n1 = *reinterpret_cast<const float2 *>(nrm + (64 + ra) * 2);
+            const float rq = p.scale * rsqrtf(n0.x + n1.x + p.eps), rk = rsqrtf(n0.y + n1.y + p.eps);
             const uint32_t offa = sbase + SM_OFFA, offb = sbase + SM_OFFB, diaga = sbase + SM_DIAGA,
                            diagb = sbase + SM_DIAGB, pb = sbase + SM_PB, sbkd = sbase + SM_SB_KD;
-            const float *Pw = reinterpret_cast<const float *>(smem + SM_TOT);
-            const float *blast = reinterpret_cast<const float *>(smem + SM_BLAST);
+            const uint32_t tab = sbase + SM_TAB;
+            // 8 channels of table constant k for this thread's block
+            auto tab8 = [&](int k, int k0, float *dst) {
+                const float4 a = ld_shared_f4(tab + tab_off(sA, k, k0));
+                const float4 b = ld_shared_f4(tab + tab_off(sA, k, k0 + 4));
+                dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
+                dst[4] = b.x; dst[5] = b.y; dst[6] = b.z; dst[7] = b.w;
+            };
 #pragma unroll
-            for (int g8 = 0; g8 < 4; g8++) {          // 8 channels at a time
-                float ek[8], eq[8], pk[8], pq[8], lk[8], lq[8], rkv[8], kd[8], ob[3][8];
+            for (int g8 = 0; g8 < 2; g8++) {          // 8 channels at a time
+                const int k0 = cb + 8 * g8;           // first channel of the 8
+                float kh[8], qh[8], A8[8], B8[8], t8[8], v8[8];
 #pragma unroll
-                for (int half4 = 0; half4 < 2; half4++) {
-                    const int cbase = 32 * iq + 8 * g8 + 4 * half4;   // first of 4 channels
-                    const float4 sh = ld_shared_f4(sbase + SM_TAB + tab_off(s, 0, cbase));
-                    const float4 X = ld_shared_f4(sbase + SM_TAB + tab_off(s, 1, cbase));
-                    const float4 Y = ld_shared_f4(sbase + SM_TAB + tab_off(s, 2, cbase));
-                    const float4 G = ld_shared_f4(sbase + SM_TAB + tab_off(s, 3, cbase));
-                    const float4 Hh = ld_shared_f4(sbase + SM_TAB + tab_off(s, 4, cbase));
-                    const float4 D1 = ld_shared_f4(sbase + SM_TAB + tab_off(s, 5, cbase));
-                    const float4 D12 = ld_shared_f4(sbase + SM_TAB + tab_off(s, 6, cbase));
-                    const float shv[4] = {sh.x, sh.y, sh.z, sh.w}, Xv[4] = {X.x, X.y, X.z, X.w},
-                                Yv[4] = {Y.x, Y.y, Y.z, Y.w}, Gv[4] = {G.x, G.y, G.z, G.w},
-                                Hv[4] = {Hh.x, Hh.y, Hh.z, Hh.w}, D1v[4] = {D1.x, D1.y, D1.z, D1.w},
-                                D12v[4] = {D12.x, D12.y, D12.z, D12.w};
+                for (int o = 0; o < 8; o++) { kh[o] = kv[8 * g8 + o] * rk; qh[o] = qv[8 * g8 + o] * rq; }
+                if (!flagged) {
+                    // A8 = L = e^{b - b_mid}, B8 = R = 1/L  (middle-row reference of the block)
+                    tab8(0, k0, t8);
 #pragma unroll
-                    for (int e4 = 0; e4 < 4; e4++) {
-                        const int u = 8 * g8 + 4 * half4 + e4;   // index into this thread's 32 channels
-                        const int o = 4 * half4 + e4;            // index within the 8-channel group
-                        const float bl = bv[u], kh = kv[u], qh = qv[u];
-                        float L, R, eloc, F, Gam, Kdf;
-                        if (!flagged) {
-                            L = __expf(bl - (hf ? 0.f : shv[e4]));
-                            R = __fdividef(1.f, L);
-                            eloc = L * Xv[e4];
-                            F = R * Yv[e4];
-                            Gam = eloc * Gv[e4];
-                            Kdf = F * Hv[e4];
-                        } else {
-                            const int c = cbase + e4;
-                            const float pw = Pw[warp * KD + c];
-                            const float babs = pw + bl;
-                            const float pstart = Pw[(2 * s) * KD + c];
-                            const float pend = (s < 3) ? Pw[(2 * s + 2) * KD + c] : blast[c];
-                            eloc = __expf(babs - pstart);
-                            F = __expf(pend - babs);
-                            Gam = __expf(babs);
-                            Kdf = __expf(blast[c] - babs);
-                            L = 0.f; R = 0.f;
-                            // stash for the pairwise diagonal blocks
-                            reinterpret_cast<float *>(smem + SM_STK)[ra * KD + c] = kh;
-                            reinterpret_cast<float *>(smem + SM_STQ)[ra * KD + c] = qh;
-                            reinterpret_cast<float *>(smem + SM_STB)[ra * KD + c] = babs;
-                        }
-                        ek[o] = kh * eloc; eq[o] = qh * eloc;
-                        pk[o] = kh * Gam;  pq[o] = qh * Gam;
-                        lk[o] = kh * L;    lq[o] = qh * L;   rkv[o] = kh * R;
-                        kd[o] = kh * Kdf;
-                        ob[0][o] = kh * F; ob[1][o] = kh * F * D1v[e4]; ob[2][o] = kh * F * D12v[e4];
+                    for (int o = 0; o < 8; o++) {
+                        A8[o] = __expf(bv[8 * g8 + o] - (hfA ? 0.f : t8[o]));
+                        B8[o] = __fdividef(1.f, A8[o]);
+                    }
+#pragma unroll
+                    for (int o = 0; o < 8; o++) v8[o] = kh[o] * A8[o];
+                    st_shared_u4(diaga + tc::core_offset(ra, k0, KD, 4), pack4_tf32(v8));
+                    st_shared_u4(diaga + tc::core_offset(ra, k0 + 4, KD, 4), pack4_tf32(v8 + 4));
+#pragma unroll
+                    for (int o = 0; o < 8; o++) v8[o] = qh[o] * A8[o];
+                    st_shared_u4(diaga + tc::core_offset(64 + ra, k0, KD, 4), pack4_tf32(v8));
+                    st_shared_u4(diaga + tc::core_offset(64 + ra, k0 + 4, KD, 4), pack4_tf32(v8 + 4));
+#pragma unroll
+                    for (int o = 0; o < 8; o++) v8[o] = kh[o] * B8[o];
+                    st_shared_u4(diagb + tc::core_offset(ra, k0, KD, 4), pack4_tf32(v8));
+                    st_shared_u4(diagb + tc::core_offset(ra, k0 + 4, KD, 4), pack4_tf32(v8 + 4));
+                    // A8 <- e_loc = L * e^{T_first_half}, B8 <- F = R * e^{T_second_half}
+                    tab8(1, k0, t8);
+#pragma unroll
+                    for (int o = 0; o < 8; o++) A8[o] *= t8[o];
+                    tab8(2, k0, t8);
+#pragma unroll
+                    for (int o = 0; o < 8; o++) B8[o] *= t8[o];
+                } else {
+                    const float *Pw = reinterpret_cast<const float *>(smem + SM_TOT);
+                    const float *blast = reinterpret_cast<const float *>(smem + SM_BLAST);
+#pragma unroll
+                    for (int o = 0; o < 8; o++) {
+                        const int c = k0 + o;
+                        const float babs = Pw[rga * KD + c] + bv[8 * g8 + o];
+                        const float pstart = Pw[(2 * sA) * KD + c];
+                        const float pend = (sA < 3) ? Pw[(2 * sA + 2) * KD + c] : blast[c];
+                        A8[o] = __expf(babs - pstart);   // e_loc
+                        B8[o] = __expf(pend - babs);     // F
+                        // stash for the pairwise diagonal blocks
+                        reinterpret_cast<float *>(smem + SM_STK)[ra * KD + c] = kh[o];
+                        reinterpret_cast<float *>(smem + SM_STQ)[ra * KD + c] = qh[o];
+                        reinterpret_cast<float *>(smem + SM_STB)[ra * KD + c] = babs;
                     }
                 }
-                const int k0 = 32 * iq + 8 * g8;     // first channel of the 8
-                st_shared_u4(offa + tc::core_offset(ra, k0, KD, 2), pack8_f16(ek));
-                st_shared_u4(offa + tc::core_offset(64 + ra, k0, KD, 2), pack8_f16(eq));
-                st_shared_u4(pb + tc::core_offset(ra, k0, KD, 2), pack8_f16(pk));
-                st_shared_u4(pb + tc::core_offset(64 + ra, k0, KD, 2), pack8_f16(pq));
-                if (!flagged) {
-                    st_shared_u4(diaga + tc::core_offset(ra, k0, KD, 4), pack4_tf32(lk));
-                    st_shared_u4(diaga + tc::core_offset(ra, k0 + 4, KD, 4), pack4_tf32(lk + 4));
-                    st_shared_u4(diaga + tc::core_offset(64 + ra, k0, KD, 4), pack4_tf32(lq));
-                    st_shared_u4(diaga + tc::core_offset(64 + ra, k0 + 4, KD, 4), pack4_tf32(lq + 4));
-                    st_shared_u4(diagb + tc::core_offset(ra, k0, KD, 4), pack4_tf32(rkv));
-                    st_shared_u4(diagb + tc::core_offset(ra, k0 + 4, KD, 4), pack4_tf32(rkv + 4));
+                // off-diagonal A operand (K^e, Q^e)
+#pragma unroll
+                for (int o = 0; o < 8; o++) v8[o] = kh[o] * A8[o];
+                st_shared_u4(offa + tc::core_offset(ra, k0, KD, 2), pack8_f16(v8));
+#pragma unroll
+                for (int o = 0; o < 8; o++) v8[o] = qh[o] * A8[o];
+                st_shared_u4(offa + tc::core_offset(64 + ra, k0, KD, 2), pack8_f16(v8));
+                // A8 <- Gamma = e_loc * e^{b at the block start}
+                tab8(3, k0, t8);
+#pragma unroll
+                for (int o = 0; o < 8; o++) A8[o] *= t8[o];
+#pragma unroll
+                for (int o = 0; o < 8; o++) v8[o] = kh[o] * A8[o];
+                st_shared_u4(pb + tc::core_offset(ra, k0, KD, 2), pack8_f16(v8));
+#pragma unroll
+                for (int o = 0; o < 8; o++) v8[o] = qh[o] * A8[o];
+                st_shared_u4(pb + tc::core_offset(64 + ra, k0, KD, 2), pack8_f16(v8));
+                // rows of B_R for the later row blocks R = sA+1 .. 3: k^ F, k^ F D1, k^ F D12
+#pragma unroll
+                for (int o = 0; o < 8; o++) kh[o] *= B8[o];      // kh <- k^ F
+                if (sA < 3) {
+                    st_shared_u4(offb + tc::core_offset(off_b_base(sA + 1) + ra, k0, KD, 2), pack8_f16(kh));
+                    if (sA < 2) {
+                        tab8(5, k0, t8);
+#pragma unroll
+                        for (int o = 0; o < 8; o++) v8[o] = kh[o] * t8[o];
+                        st_shared_u4(offb + tc::core_offset(off_b_base(sA + 2) + ra, k0, KD, 2), pack8_f16(v8));
+                        if (sA < 1) {
+                            tab8(6, k0, t8);
+#pragma unroll
+                            for (int o = 0; o < 8; o++) v8[o] = kh[o] * t8[o];
+                            st_shared_u4(offb + tc::core_offset(off_b_base(3) + ra, k0, KD, 2), pack8_f16(v8));
+                        }
+                    }
                 }
-                // rows of B_R for the later row blocks R = s+1 .. 3
-                if (s == 0) {
-                    st_shared_u4(offb + tc::core_offset(0 + ra, k0, KD, 2), pack8_f16(ob[0]));
-                    st_shared_u4(offb + tc::core_offset(16 + ra, k0, KD, 2), pack8_f16(ob[1]));
-                    st_shared_u4(offb + tc::core_offset(48 + ra, k0, KD, 2), pack8_f16(ob[2]));
-                } else if (s == 1) {
-                    st_shared_u4(offb + tc::core_offset(16 + ra, k0, KD, 2), pack8_f16(ob[0]));
-                    st_shared_u4(offb + tc::core_offset(48 + ra, k0, KD, 2), pack8_f16(ob[1]));
-                } else if (s == 2) {
-                    st_shared_u4(offb + tc::core_offset(48 + ra, k0, KD, 2), pack8_f16(ob[0]));
-                }
+                // Kd^T = (k^ F e^{b_last - b_block_end})^T
+                tab8(4, k0, t8);
 #pragma unroll
                 for (int o = 0; o < 8; o++)
-                    st_shared_u16(sbkd + tc::core_offset(k0 + o, ra, 64, 2), f16_bits(kd[o]));
+                    st_shared_u16(sbkd + tc::core_offset(k0 + o, ra, 64, 2), f16_bits(kh[o] * t8[o]));
             }
         }
         tc::fence_proxy_async();
@@ -572,57 +582,61 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::gemm<2, 64, 128>(tmem + TM_XDIAG, sbase + SM_DIAGA, SBO128_TF32, sbase + SM_DIAGB, SBO128_TF32, false);
             tc::commit(mbar);
         }
+        // next chunk's inputs and this chunk's V column slice are loaded while the MMAs run
+        const bool has_next = c0 + C < row1;
+        if (has_next && ra < row1 - (c0 + C)) load_row_inputs(p, c0 + C + ra, h, cb, HK, in);
+        uint32_t vraw[8];   // 16 bf16 values of V[r][j], r = 16 k4 .. +15, two per register
+        {
+            const uint16_t *vp = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD + jv;
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                const int r = 16 * k4 + u;
+                const uint32_t lo = (r < n) ? vp[static_cast<int64_t>(r) * p.ld_qkv] : 0u;
+                const uint32_t hi = (r + 1 < n) ? vp[static_cast<int64_t>(r + 1) * p.ld_qkv] : 0u;
+                vraw[u >> 1] = lo | (hi << 16);
+            }
+        }
         ok &= tc::mbar_wait(mbar, phase);
         phase ^= 1;
         tc::fence_after_sync();
 
         // ================= Phase C: A, Aqk, T =================
-        if (warp < 4) {
-            if ((warp & 1) == 0) assemble_rows<0>(smem, tlane, warp, lane, flagged);
-            else assemble_rows<1>(smem, tlane, warp, lane, flagged);
-        }
+        assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
         solve_T(smem, tid);
         {
-            // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i
+            // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
             const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
-            const int r = tid >> 2, i0 = (tid & 3) * 16;
-            float v[16];
+            const int r = tid >> 3, i0 = (tid & 7) * 8;
+            float v[8];
 #pragma unroll
-            for (int u = 0; u < 16; u++) {
+            for (int u = 0; u < 8; u++) {
                 const int i = i0 + u;
                 v[u] = (i < r) ? Tm[r * AP + i] : (i == r ? 1.f : 0.f);
             }
             st_shared_u4(sbase + SM_TB + tc::core_offset(r, i0, 64, 2), pack8_f16(v));
-            st_shared_u4(sbase + SM_TB + tc::core_offset(r, i0 + 8, 64, 2), pack8_f16(v + 8));
         }
 
         // ================= Phase D: the chain step =================
-        // V values of this thread's column and row half (issued early)
-        float vv[32];
-        {
-            const uint16_t *vp = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD + jv;
-#pragma unroll
-            for (int u = 0; u < 32; u++) {
-                const int r = 32 * hv + u;
-                vv[u] = (r < n) ? bf16_to_f32(vp[static_cast<int64_t>(r) * p.ld_qkv]) : 0.f;
-            }
-        }
         // D1: S^T -> fp16 operand; TMEM S^T <- S^T Diag(e^{b_last})
         {
             const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
+            float v[2][16];
+            tc::tmem_ld16(tlane + TM_S + 32 * k4, v[0]);
+            tc::tmem_ld16(tlane + TM_S + 32 * k4 + 16, v[1]);
+            tc::tmem_ld_wait();
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 16) {
-                float v[16];
-                const int c = 64 * hv + cc;
-                tc::tmem_ld16(tlane + TM_S + c, v);
-                tc::tmem_ld_wait();
-                st_shared_u4(sbase + SM_SA + tc::core_offset(jv, c, KD, 2), pack8_f16(v));
-                st_shared_u4(sbase + SM_SA + tc::core_offset(jv, c + 8, KD, 2), pack8_f16(v + 8));
+            for (int hh = 0; hh < 2; hh++) {
+                const int c = 32 * k4 + 16 * hh;
+                st_shared_u4(sbase + SM_SA + tc::core_offset(jv, c, KD, 2), pack8_f16(v[hh]));
+                st_shared_u4(sbase + SM_SA + tc::core_offset(jv, c + 8, KD, 2), pack8_f16(v[hh] + 8));
 #pragma unroll
-                for (int u = 0; u < 16; u++) v[u] *= gc[c + u];
-                tc::tmem_st16(tlane + TM_S + c, v);
+                for (int u = 0; u < 16; u += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gc + c + u);
+                    v[hh][u] *= g4.x; v[hh][u + 1] *= g4.y; v[hh][u + 2] *= g4.z; v[hh][u + 3] *= g4.w;
+                }
+                tc::tmem_st16(tlane + TM_S + c, v[hh]);
             }
             tc::tmem_st_wait();
         }
@@ -637,20 +651,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         ok &= tc::mbar_wait(mbar, phase);
         phase ^= 1;
         tc::fence_after_sync();
-        // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 operand
+        // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 operand (rows r = 16 k4 .. +15)
         {
             const float *bet = reinterpret_cast<const float *>(smem + SM_BETA);
+            float v[16];
+            const int r0 = 16 * k4;
+            tc::tmem_ld16(tlane + TM_P + r0, v);
+            tc::tmem_ld_wait();
 #pragma unroll
-            for (int cc = 0; cc < 32; cc += 16) {
-                float v[16];
-                const int r0 = 32 * hv + cc;
-                tc::tmem_ld16(tlane + TM_P + r0, v);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 16; u++) v[u] = bet[r0 + u] * (vv[cc + u] - v[u]);
-                st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
-                st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0 + 8, 64, 2), pack8_f16(v + 8));
+            for (int u = 0; u < 16; u++) {
+                const uint32_t w2 = vraw[u >> 1];
+                const float vv = __uint_as_float((u & 1) ? (w2 & 0xffff0000u) : (w2 << 16));
+                v[u] = bet[r0 + u] * (vv - v[u]);
             }
+            st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
+            st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0 + 8, 64, 2), pack8_f16(v + 8));
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
@@ -664,10 +679,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         phase ^= 1;
         tc::fence_after_sync();
         // D5: U^T -> fp16 operand
-#pragma unroll
-        for (int cc = 0; cc < 32; cc += 16) {
+        {
             float v[16];
-            const int r0 = 32 * hv + cc;
+            const int r0 = 16 * k4;
             tc::tmem_ld16(tlane + TM_P + r0, v);
             tc::tmem_ld_wait();
             st_shared_u4(sbase + SM_UA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
@@ -684,21 +698,29 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         ok &= tc::mbar_wait(mbar, phase);
         phase ^= 1;
         tc::fence_after_sync();
-        // D7: O^T -> bf16 output rows
+        // D7: O^T -> bf16 tile [r][j] in shared memory, then 16-byte row stores
         {
-            uint16_t *op = p.out + c0 * p.ld_out + static_cast<int64_t>(h) * VD + jv;
+            uint16_t *otile = reinterpret_cast<uint16_t *>(smem + SM_OTILE);
+            float v[16];
+            const int r0 = 16 * k4;
+            tc::tmem_ld16(tlane + TM_P + 64 + r0, v);
+            tc::tmem_ld_wait();
 #pragma unroll
-            for (int cc = 0; cc < 32; cc += 16) {
-                float v[16];
-                const int r0 = 32 * hv + cc;
-                tc::tmem_ld16(tlane + TM_P + 64 + r0, v);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 16; u++)
-                    if (r0 + u < n) op[static_cast<int64_t>(r0 + u) * p.ld_out] = f32_to_bf16(v[u]);
-            }
+            for (int u = 0; u < 16; u++) otile[(r0 + u) * OT_PITCH + jv] = f32_to_bf16(v[u]);
         }
         tc::fence_before_sync();
+        __syncthreads();
+        {
+            const uint16_t *otile = reinterpret_cast<const uint16_t *>(smem + SM_OTILE);
+#pragma unroll
+            for (int x = 0; x < 2; x++) {
+                const int id = tid + NT * x, r = id >> 4, c8 = (id & 15) * 8;
+                if (r < n) {
+                    const uint4 val = *reinterpret_cast<const uint4 *>(otile + r * OT_PITCH + c8);
+                    *reinterpret_cast<uint4 *>(p.out + (c0 + r) * p.ld_out + static_cast<int64_t>(h) * VD + c8) = val;
+                }
+            }
+        }
         if (__syncthreads_or(ok ? 0 : 1)) {
             ok = false;
             break;
@@ -708,9 +730,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     // ---- final state -> pool ----
     if (ok && writable) {
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 16) {
+        for (int cc = 0; cc < 32; cc += 16) {
             float v[16];
-            const int c = 64 * hv + cc;
+            const int c = 32 * k4 + cc;
             tc::tmem_ld16(tlane + TM_S + c, v);
             tc::tmem_ld_wait();
 #pragma unroll
