@@ -381,6 +381,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         const int n = static_cast<int>((row1 - c0) < C ? (row1 - c0) : C);
 
         // ================= Phase A: gate, norms, cumulative decay, operands =================
+        // this chunk's V rows of this head go to L2 now; the chain step reads them later
+        if (tid < 2 * C) {
+            const int r = tid >> 1;
+            if (r < n)
+                asm volatile("prefetch.global.L2 [%0];" :: "l"(p.qkv + (c0 + r) * p.ld_qkv + 2 * HK +
+                                                            static_cast<int64_t>(h) * VD + 64 * (tid & 1)));
+        }
         float qv[16], kv[16], bv[16];
         float beta_r = 0.f;
         const bool valid = ra < n;
@@ -426,42 +433,57 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         if (warp < 8 && iq == 0) reinterpret_cast<float *>(smem + SM_BETA)[ra] = beta_r;
         __syncthreads();
 
-        // per-channel constants (threads 0..127, one channel each)
+        // per-(block, channel) constants: thread tid handles channel tid & 127, block tid >> 7
         int flag = 0;
-        if (tid < KD) {
-            const int c = tid;
-            float T[8], E[8], P[9];
-            P[0] = 0.f;
+        {
+            const int c = tid & (KD - 1), s = tid >> 7;
+            float T[8], E[8];
 #pragma unroll
             for (int w = 0; w < 8; w++) {
                 T[w] = tot[w * KD + c];
-                P[w + 1] = P[w] + T[w];
                 E[w] = __expf(T[w]);
-                flag |= (T[w] < -kHalfSpan) ? 1 : 0;
             }
+            // block s covers warps 2s, 2s+1 (selects keep the arrays in registers)
+            float G = 1.f, Hh = 1.f, D1 = 1.f, D12 = 1.f, T0 = 0.f, X = 1.f, Y = 1.f;
 #pragma unroll
-            for (int s = 0; s < 4; s++) {
-                float G = 1.f, Hh = 1.f;
+            for (int w = 0; w < 8; w++) {
+                if (w < 2 * s) G *= E[w];
+                if (w >= 2 * s + 2) Hh *= E[w];
+                if (w == 2 * s) { T0 = T[w]; X = E[w]; }
+                if (w == 2 * s + 1) Y = E[w];
+                if (w == 2 * s + 2 || w == 2 * s + 3) D1 *= E[w];
+                if (w >= 2 * s + 2 && w <= 2 * s + 5) D12 *= E[w];
+            }
+            if (s > 2) D1 = 0.f;
+            if (s > 1) D12 = 0.f;
+            const float vals[7] = {T0, X, Y, G, Hh, D1, D12};
+#pragma unroll
+            for (int k = 0; k < 7; k++) *reinterpret_cast<float *>(smem + SM_TAB + tab_off(s, k, c)) = vals[k];
+            if (s == 0) {
+                float P = 0.f, gc = 1.f;
 #pragma unroll
                 for (int w = 0; w < 8; w++) {
-                    if (w < 2 * s) G *= E[w];
-                    if (w >= 2 * s + 2) Hh *= E[w];
+                    flag |= (T[w] < -kHalfSpan) ? 1 : 0;
+                    gc *= E[w];
+                    P += T[w];
                 }
-                const float D1 = (s <= 2) ? E[2 * s + 2] * E[2 * s + 3] : 0.f;
-                const float D12 = (s <= 1) ? D1 * E[2 * s + 4] * E[2 * s + 5] : 0.f;
-                const float vals[7] = {T[2 * s], E[2 * s], E[2 * s + 1], G, Hh, D1, D12};
-#pragma unroll
-                for (int k = 0; k < 7; k++) *reinterpret_cast<float *>(smem + SM_TAB + tab_off(s, k, c)) = vals[k];
+                reinterpret_cast<float *>(smem + SM_GC)[c] = gc;
+                reinterpret_cast<float *>(smem + SM_BLAST)[c] = P;
             }
-            float gc = 1.f;
-#pragma unroll
-            for (int w = 0; w < 8; w++) gc *= E[w];
-            reinterpret_cast<float *>(smem + SM_GC)[c] = gc;
-            reinterpret_cast<float *>(smem + SM_BLAST)[c] = P[8];
-#pragma unroll
-            for (int w = 0; w < 8; w++) tot[w * KD + c] = P[w];  // prefixes replace the sums
         }
+        // prefixes P_w replace the per-warp sums (read only on the flagged path)
         const bool flagged = __syncthreads_or(flag) != 0;
+        if (flagged && tid < KD) {
+            float P = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; w++) {
+                const float t = tot[w * KD + tid];
+                tot[w * KD + tid] = P;
+                P += t;
+            }
+        }
+        if (flagged) __syncthreads();
+
 
         {
             // full-row norms from the two channel halves
@@ -585,17 +607,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         // next chunk's inputs and this chunk's V column slice are loaded while the MMAs run
         const bool has_next = c0 + C < row1;
         if (has_next && ra < row1 - (c0 + C)) load_row_inputs(p, c0 + C + ra, h, cb, HK, in);
-        uint32_t vraw[8];   // 16 bf16 values of V[r][j], r = 16 k4 .. +15, two per register
-        {
-            const uint16_t *vp = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD + jv;
-#pragma unroll
-            for (int u = 0; u < 16; u += 2) {
-                const int r = 16 * k4 + u;
-                const uint32_t lo = (r < n) ? vp[static_cast<int64_t>(r) * p.ld_qkv] : 0u;
-                const uint32_t hi = (r + 1 < n) ? vp[static_cast<int64_t>(r + 1) * p.ld_qkv] : 0u;
-                vraw[u >> 1] = lo | (hi << 16);
-            }
-        }
         ok &= tc::mbar_wait(mbar, phase);
         phase ^= 1;
         tc::fence_after_sync();
@@ -619,6 +630,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         }
 
         // ================= Phase D: the chain step =================
+        // V[r][j] for this thread's rows r = 16 k4 .. +15 (consumed in D3)
+        uint32_t vraw[16];
+        {
+            const uint16_t *vp = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD + jv;
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                const int r = 16 * k4 + u;
+                vraw[u] = 0u;
+                if (r < n) vraw[u] = vp[static_cast<int64_t>(r) * p.ld_qkv];
+            }
+        }
         // D1: S^T -> fp16 operand; TMEM S^T <- S^T Diag(e^{b_last})
         {
             const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
@@ -659,11 +681,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             tc::tmem_ld16(tlane + TM_P + r0, v);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; u++) {
-                const uint32_t w2 = vraw[u >> 1];
-                const float vv = __uint_as_float((u & 1) ? (w2 & 0xffff0000u) : (w2 << 16));
-                v[u] = bet[r0 + u] * (vv - v[u]);
-            }
+            for (int u = 0; u < 16; u++) v[u] = bet[r0 + u] * (__uint_as_float(vraw[u] << 16) - v[u]);
             st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
             st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0 + 8, 64, 2), pack8_f16(v + 8));
         }
