@@ -374,23 +374,26 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 
     const float expA = __expf(p.A_log[h]);
     const float *dtb_s = reinterpret_cast<const float *>(smem + SM_DTB);
-    RowIn in;
-    if (ra < row1 - row0) load_row_inputs(p, row0 + ra, h, cb, HK, in);
 
     for (int64_t c0 = row0; c0 < row1; c0 += C) {
         const int n = static_cast<int>((row1 - c0) < C ? (row1 - c0) : C);
 
         // ================= Phase A: gate, norms, cumulative decay, operands =================
-        // this chunk's V rows of this head go to L2 now; the chain step reads them later
-        if (tid < 2 * C) {
-            const int r = tid >> 1;
-            if (r < n)
-                asm volatile("prefetch.global.L2 [%0];" :: "l"(p.qkv + (c0 + r) * p.ld_qkv + 2 * HK +
-                                                            static_cast<int64_t>(h) * VD + 64 * (tid & 1)));
+        RowIn in;
+        const bool valid = ra < n;
+        if (valid) load_row_inputs(p, c0 + ra, h, cb, HK, in);
+        {
+            // the next chunk's rows of this head (q, k, v, raw_g: 2 lines each) go to L2 now
+            const int r = tid >> 3, part = (tid >> 1) & 3, half = tid & 1;
+            if (c0 + C + r < row1) {
+                const int64_t row = c0 + C + r;
+                const uint16_t *base = (part == 3) ? p.rg + row * p.ld_g + h * KD
+                                                   : p.qkv + row * p.ld_qkv + part * HK + static_cast<int64_t>(h) * KD;
+                asm volatile("prefetch.global.L2 [%0];" :: "l"(base + 64 * half));
+            }
         }
         float qv[16], kv[16], bv[16];
         float beta_r = 0.f;
-        const bool valid = ra < n;
         if (valid) {
             unpack_bf16x8(in.q[0], qv); unpack_bf16x8(in.q[1], qv + 8);
             unpack_bf16x8(in.k[0], kv); unpack_bf16x8(in.k[1], kv + 8);
@@ -604,9 +607,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::gemm<2, 64, 128>(tmem + TM_XDIAG, sbase + SM_DIAGA, SBO128_TF32, sbase + SM_DIAGB, SBO128_TF32, false);
             tc::commit(mbar);
         }
-        // next chunk's inputs and this chunk's V column slice are loaded while the MMAs run
-        const bool has_next = c0 + C < row1;
-        if (has_next && ra < row1 - (c0 + C)) load_row_inputs(p, c0 + C + ra, h, cb, HK, in);
         ok &= tc::mbar_wait(mbar, phase);
         phase ^= 1;
         tc::fence_after_sync();
