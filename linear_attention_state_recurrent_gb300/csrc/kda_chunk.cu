@@ -630,9 +630,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         }
 
         // ================= Phase D: the chain step =================
-        // V[r][j] for this thread's rows r = 16 k4 .. +15 (consumed in D3)
+        // D1: S^T -> fp16 operand; TMEM S^T <- S^T Diag(e^{b_last})
         uint32_t vraw[16];
         {
+            const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
+            float v[2][16];
+            tc::tmem_ld16(tlane + TM_S + 32 * k4, v[0]);
+            tc::tmem_ld16(tlane + TM_S + 32 * k4 + 16, v[1]);
+            tc::tmem_ld_wait();
+            // V[r][j] for this thread's rows r = 16 k4 .. +15, issued after the TMEM wait
+            // (consumed in D3)
             const uint16_t *vp = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD + jv;
 #pragma unroll
             for (int u = 0; u < 16; u++) {
@@ -640,14 +647,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 vraw[u] = 0u;
                 if (r < n) vraw[u] = vp[static_cast<int64_t>(r) * p.ld_qkv];
             }
-        }
-        // D1: S^T -> fp16 operand; TMEM S^T <- S^T Diag(e^{b_last})
-        {
-            const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
-            float v[2][16];
-            tc::tmem_ld16(tlane + TM_S + 32 * k4, v[0]);
-            tc::tmem_ld16(tlane + TM_S + 32 * k4 + 16, v[1]);
-            tc::tmem_ld_wait();
 #pragma unroll
             for (int hh = 0; hh < 2; hh++) {
                 const int c = 32 * k4 + 16 * hh;
