@@ -79,6 +79,13 @@ constexpr uint32_t SM_YA = SM_DIAGA + 32768;   // fp16 [128 x 64]  (beta Y)^T
 constexpr uint32_t SM_UA = SM_DIAGA + 49152;   // fp16 [128 x 64]  U^T
 constexpr uint32_t SM_OTILE = SM_OFFB;         // bf16 [64][OT_PITCH] output rows
 constexpr int OT_PITCH = 136;                  // bf16 row pitch (272 B: 16-byte aligned rows)
+// input staging (bf16 [64 rows][128], 16-byte chunks XOR-swizzled by row):
+// the next chunk's q, k, raw_g are copied during this chunk's chain step, this
+// chunk's V rows during its triangular solve
+constexpr uint32_t SM_QST = SM_OFFA;
+constexpr uint32_t SM_KST = SM_OFFA + 16384;
+constexpr uint32_t SM_VST = SM_DIAGB;
+constexpr uint32_t SM_GST = SM_DIAGB + 16384;
 // flagged-chunk stash (fp32 [64][128] each)
 constexpr uint32_t SM_STK = SM_DIAGA;
 constexpr uint32_t SM_STQ = SM_DIAGA + 32768;
@@ -291,21 +298,51 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
     }
 }
 
+// byte offset of 16-byte chunk `ch` (0..15) of row r in a staged [64][128] bf16 tile
+__device__ __forceinline__ uint32_t st_off(int r, int ch) { return static_cast<uint32_t>(r * 256 + ((ch ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Copies rows [c0, c0 + 64) of one 128-wide bf16 column block (base + row*ld) into a
+// staged tile; rows at or past `nrows` are zero-filled (their source is not read).
+__device__ __forceinline__ void stage_rows(uint32_t tile, const uint16_t *base, int64_t ld, int nrows, int tid)
+{
+#pragma unroll
+    for (int x = 0; x < 2; x++) {
+        const int id = tid + NT * x, r = id >> 4, ch = id & 15;
+        const bool ok = r < nrows;
+        const uint16_t *src = base + (ok ? static_cast<int64_t>(r) * ld : 0) + 8 * ch;
+        cp_async16(tile + st_off(r, ch), src, ok);
+    }
+}
+
 // raw phase-A inputs of one thread: 16 channels of q, k and raw_g for one row
 struct RowIn {
     uint4 q[2], k[2], g[2];
-    uint16_t beta;
 };
 
-__device__ __forceinline__ void load_row_inputs(const Params &p, int64_t row, int h, int cb, int64_t HK, RowIn &in)
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr)
 {
-    const uint4 *qp = reinterpret_cast<const uint4 *>(p.qkv + row * p.ld_qkv + h * KD + cb);
-    const uint4 *kp = reinterpret_cast<const uint4 *>(p.qkv + row * p.ld_qkv + HK + h * KD + cb);
-    const uint4 *gp = reinterpret_cast<const uint4 *>(p.rg + row * p.ld_g + h * KD + cb);
-    in.q[0] = qp[0]; in.q[1] = qp[1];
-    in.k[0] = kp[0]; in.k[1] = kp[1];
-    in.g[0] = gp[0]; in.g[1] = gp[1];
-    in.beta = p.rb[row * p.ld_beta + h];
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// this thread's row r and channels cb .. cb+15 from the staged q, k, raw_g tiles
+__device__ __forceinline__ void load_row_inputs(uint32_t sbase, int r, int cb, RowIn &in)
+{
+    const int ch = cb >> 3;
+    in.q[0] = ld_shared_u4(sbase + SM_QST + st_off(r, ch));
+    in.q[1] = ld_shared_u4(sbase + SM_QST + st_off(r, ch + 1));
+    in.k[0] = ld_shared_u4(sbase + SM_KST + st_off(r, ch));
+    in.k[1] = ld_shared_u4(sbase + SM_KST + st_off(r, ch + 1));
+    in.g[0] = ld_shared_u4(sbase + SM_GST + st_off(r, ch));
+    in.g[1] = ld_shared_u4(sbase + SM_GST + st_off(r, ch + 1));
 }
 
 // ---------------------------------------------------------------------------
@@ -374,31 +411,32 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 
     const float expA = __expf(p.A_log[h]);
     const float *dtb_s = reinterpret_cast<const float *>(smem + SM_DTB);
+    // stage the first chunk's q, k, raw_g rows
+    {
+        const int n0 = static_cast<int>((row1 - row0) < C ? (row1 - row0) : C);
+        stage_rows(sbase + SM_QST, p.qkv + row0 * p.ld_qkv + h * KD, p.ld_qkv, n0, tid);
+        stage_rows(sbase + SM_KST, p.qkv + row0 * p.ld_qkv + HK + h * KD, p.ld_qkv, n0, tid);
+        stage_rows(sbase + SM_GST, p.rg + row0 * p.ld_g + h * KD, p.ld_g, n0, tid);
+        cp_async_commit();
+    }
+    uint16_t beta_raw = 0;   // raw_beta of row tid of the current chunk (threads < 64)
+    if (tid < C && tid < row1 - row0) beta_raw = p.rb[(row0 + tid) * p.ld_beta + h];
 
     for (int64_t c0 = row0; c0 < row1; c0 += C) {
         const int n = static_cast<int>((row1 - c0) < C ? (row1 - c0) : C);
 
         // ================= Phase A: gate, norms, cumulative decay, operands =================
+        // staged inputs of this chunk (copied during the previous chain step)
+        cp_async_wait_all();
+        __syncthreads();
         RowIn in;
         const bool valid = ra < n;
-        if (valid) load_row_inputs(p, c0 + ra, h, cb, HK, in);
-        {
-            // the next chunk's rows of this head (q, k, v, raw_g: 2 lines each) go to L2 now
-            const int r = tid >> 3, part = (tid >> 1) & 3, half = tid & 1;
-            if (c0 + C + r < row1) {
-                const int64_t row = c0 + C + r;
-                const uint16_t *base = (part == 3) ? p.rg + row * p.ld_g + h * KD
-                                                   : p.qkv + row * p.ld_qkv + part * HK + static_cast<int64_t>(h) * KD;
-                asm volatile("prefetch.global.L2 [%0];" :: "l"(base + 64 * half));
-            }
-        }
+        load_row_inputs(sbase, ra, cb, in);
         float qv[16], kv[16], bv[16];
-        float beta_r = 0.f;
         if (valid) {
             unpack_bf16x8(in.q[0], qv); unpack_bf16x8(in.q[1], qv + 8);
             unpack_bf16x8(in.k[0], kv); unpack_bf16x8(in.k[1], kv + 8);
             unpack_bf16x8(in.g[0], bv); unpack_bf16x8(in.g[1], bv + 8);
-            beta_r = sigmoid_f(bf16_to_f32(in.beta));
         } else {
 #pragma unroll
             for (int u = 0; u < 16; u++) { qv[u] = 0.f; kv[u] = 0.f; bv[u] = 0.f; }
@@ -433,7 +471,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             for (int u = 0; u < 16; u += 4)
                 *reinterpret_cast<float4 *>(tot + rga * KD + cb + u) = make_float4(bv[u], bv[u + 1], bv[u + 2], bv[u + 3]);
         }
-        if (warp < 8 && iq == 0) reinterpret_cast<float *>(smem + SM_BETA)[ra] = beta_r;
+        if (tid < C) reinterpret_cast<float *>(smem + SM_BETA)[tid] = (tid < n) ? sigmoid_f(bf16_to_f32(beta_raw)) : 0.f;
         __syncthreads();
 
         // per-(block, channel) constants: thread tid handles channel tid & 127, block tid >> 7
@@ -615,6 +653,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
+        // this chunk's V rows -> staged tile (read in D3), overlapping the solve
+        stage_rows(sbase + SM_VST, p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD, p.ld_qkv, n, tid);
+        cp_async_commit();
         solve_T(smem, tid);
         {
             // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
@@ -630,23 +671,23 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         }
 
         // ================= Phase D: the chain step =================
+        // the next chunk's q, k, raw_g rows -> staging (the scratch of phase C is dead now)
+        if (c0 + C < row1) {
+            const int64_t nx = c0 + C;
+            const int nn = static_cast<int>((row1 - nx) < C ? (row1 - nx) : C);
+            stage_rows(sbase + SM_QST, p.qkv + nx * p.ld_qkv + h * KD, p.ld_qkv, nn, tid);
+            stage_rows(sbase + SM_KST, p.qkv + nx * p.ld_qkv + HK + h * KD, p.ld_qkv, nn, tid);
+            stage_rows(sbase + SM_GST, p.rg + nx * p.ld_g + h * KD, p.ld_g, nn, tid);
+            if (tid < nn) beta_raw = p.rb[(nx + tid) * p.ld_beta + h];
+        }
+        cp_async_commit();
         // D1: S^T -> fp16 operand; TMEM S^T <- S^T Diag(e^{b_last})
-        uint32_t vraw[16];
         {
             const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
             float v[2][16];
             tc::tmem_ld16(tlane + TM_S + 32 * k4, v[0]);
             tc::tmem_ld16(tlane + TM_S + 32 * k4 + 16, v[1]);
             tc::tmem_ld_wait();
-            // V[r][j] for this thread's rows r = 16 k4 .. +15, issued after the TMEM wait
-            // (consumed in D3)
-            const uint16_t *vp = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD + jv;
-#pragma unroll
-            for (int u = 0; u < 16; u++) {
-                const int r = 16 * k4 + u;
-                vraw[u] = 0u;
-                if (r < n) vraw[u] = vp[static_cast<int64_t>(r) * p.ld_qkv];
-            }
 #pragma unroll
             for (int hh = 0; hh < 2; hh++) {
                 const int c = 32 * k4 + 16 * hh;
@@ -673,14 +714,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         phase ^= 1;
         tc::fence_after_sync();
         // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 operand (rows r = 16 k4 .. +15)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");   // the V tile (older group) has landed
+        __syncthreads();
         {
             const float *bet = reinterpret_cast<const float *>(smem + SM_BETA);
+            const uint16_t *vt = reinterpret_cast<const uint16_t *>(smem + SM_VST);
             float v[16];
             const int r0 = 16 * k4;
             tc::tmem_ld16(tlane + TM_P + r0, v);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; u++) v[u] = bet[r0 + u] * (__uint_as_float(vraw[u] << 16) - v[u]);
+            for (int u = 0; u < 16; u++) {
+                const int r = r0 + u;
+                const float vv = bf16_to_f32(vt[(st_off(r, jv >> 3) >> 1) + (jv & 7)]);
+                v[u] = bet[r] * (vv - v[u]);
+            }
             st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
             st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0 + 8, 64, 2), pack8_f16(v + 8));
         }
