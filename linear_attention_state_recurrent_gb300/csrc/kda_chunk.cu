@@ -208,33 +208,33 @@ __device__ void solve_T(unsigned char *smem, int tid)
         T[(o + 16 + r) * AP + o + j] = -y;
     }
     __syncthreads();
-    // level 3: X = A_ba T_a (32x32), T_ba = -T_b X
-    {
-        const int r = tid >> 4, j = (tid & 15) * 2;
-        float x0 = 0.f, x1 = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < 32; m++) {
-            const float a = A[(32 + r) * AP + m];
-            if (m >= j) x0 += a * T[m * AP + j];
-            if (m >= j + 1) x1 += a * T[m * AP + j + 1];
+    // level 3: X = A_ba T_a (32x32), T_ba = -T_b X; 2x2 output tiles on 256 threads
+    if (tid < 256) {
+        const int r = (tid >> 4) * 2, j = (tid & 15) * 2;
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+        for (int m = j; m < 32; m++) {           // T_a is lower triangular: m >= j
+            const float a0 = A[(32 + r) * AP + m], a1 = A[(33 + r) * AP + m];
+            const float2 t = *reinterpret_cast<const float2 *>(T + m * AP + j);
+            const float t1 = (m >= j + 1) ? t.y : 0.f;
+            x00 += a0 * t.x; x01 += a0 * t1;
+            x10 += a1 * t.x; x11 += a1 * t1;
         }
-        X[r * 36 + j] = x0;
-        X[r * 36 + j + 1] = x1;
+        *reinterpret_cast<float2 *>(X + r * 36 + j) = make_float2(x00, x01);
+        *reinterpret_cast<float2 *>(X + (r + 1) * 36 + j) = make_float2(x10, x11);
     }
     __syncthreads();
-    {
-        const int r = tid >> 4, j = (tid & 15) * 2;
-        float y0 = 0.f, y1 = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < 32; m++) {
-            if (m <= r) {
-                const float t = T[(32 + r) * AP + 32 + m];
-                y0 += t * X[m * 36 + j];
-                y1 += t * X[m * 36 + j + 1];
-            }
+    if (tid < 256) {
+        const int r = (tid >> 4) * 2, j = (tid & 15) * 2;
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+        for (int m = 0; m <= r + 1; m++) {       // T_b is lower triangular: m <= row
+            const float t0 = (m <= r) ? T[(32 + r) * AP + 32 + m] : 0.f;
+            const float t1 = T[(33 + r) * AP + 32 + m];
+            const float2 x = *reinterpret_cast<const float2 *>(X + m * 36 + j);
+            y00 += t0 * x.x; y01 += t0 * x.y;
+            y10 += t1 * x.x; y11 += t1 * x.y;
         }
-        T[(32 + r) * AP + j] = -y0;
-        T[(32 + r) * AP + j + 1] = -y1;
+        *reinterpret_cast<float2 *>(T + (32 + r) * AP + j) = make_float2(-y00, -y01);
+        *reinterpret_cast<float2 *>(T + (33 + r) * AP + j) = make_float2(-y10, -y11);
     }
     __syncthreads();
 }
@@ -650,12 +650,20 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         tc::fence_after_sync();
 
         // ================= Phase C: A, Aqk, T =================
+        // this chunk's V rows -> staged tile (read in D3). The tile overlays the diagonal
+        // B operand (consumed by now) or, on the pairwise path, the stash read below.
+        const uint16_t *vsrc = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD;
+        if (!flagged) {
+            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
+            cp_async_commit();
+        }
         assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
-        // this chunk's V rows -> staged tile (read in D3), overlapping the solve
-        stage_rows(sbase + SM_VST, p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD, p.ld_qkv, n, tid);
-        cp_async_commit();
+        if (flagged) {
+            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
+            cp_async_commit();
+        }
         solve_T(smem, tid);
         {
             // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
