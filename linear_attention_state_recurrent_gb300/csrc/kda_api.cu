@@ -217,8 +217,8 @@ int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
     if (num_reqs == 0) return ok();
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
-    return cuda_status(kda::launch_recurrent(p, heads->K, heads->V, 1, tokens_per_req, nullptr, 0,
-                                             num_reqs, static_cast<cudaStream_t>(stream)),
+    return cuda_status(kda::launch_spec(p, heads->K, heads->V, tokens_per_req, num_reqs,
+                                        static_cast<cudaStream_t>(stream)),
                        "kda_spec_verify launch");
 }
 

@@ -17,6 +17,9 @@ cudaError_t launch_gate(const Params &p, int K, int64_t N, float *g_out, float *
 cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
                              int64_t entry_base, int64_t num_entries, cudaStream_t stream);
 
+// Spec-verify: T consecutive rows per request.
+cudaError_t launch_spec(const Params &p, int K, int V, int T, int64_t num_reqs, cudaStream_t stream);
+
 // Chunked prefill over entries entry_base .. entry_base + num_seqs - 1 (rows from cu).
 size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V,
                              int chunk_size);

@@ -215,6 +215,167 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 }
 
 // ---------------------------------------------------------------------------
+// Spec-verify kernel: T <= kSpecMaxT tokens per request. All T tokens' gates, betas
+// and q/k norms are computed up front in one parallel pass (their inputs are loaded
+// together with the state tile), so the sequential part is only the state update:
+// one barrier per token, the reduction buffers double-buffered across tokens.
+// Same tile split and thread layout as recurrent_kernel.
+// ---------------------------------------------------------------------------
+constexpr int kSpecMaxT = 16;
+
+template <int K, int V>
+__global__ void __launch_bounds__(128, 6) spec_kernel(Params p, int T)
+{
+    constexpr int VT = 32, VS = V / VT, RPT = K / 16, KW = K / 32;
+    __shared__ float s_a[kSpecMaxT][K], s_k[kSpecMaxT][K], s_q[kSpecMaxT][K];
+    __shared__ float s_part[kSpecMaxT][KW][3];
+    __shared__ float s_tok[kSpecMaxT][4];          // rq, rk, q^.k^, beta
+    __shared__ float s_red[2][4][2][VT];
+    __shared__ float4 s_v[kSpecMaxT][VT / 4];      // this CTA's value columns of every token
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, cg = tid & 7, rg = tid >> 3;
+    const int64_t b = blockIdx.x;
+    const int vs = static_cast<int>(b % VS);
+    const int h = static_cast<int>((b / VS) % p.H);
+    const int64_t e = b / (static_cast<int64_t>(VS) * p.H);
+    const int64_t row0 = e * T;
+    const int j0 = vs * VT + cg * 4;
+    const int64_t slot = load_slot(p, e);
+    if (slot >= p.num_slots) {
+        if (tid == 0 && p.err) atomicOr(p.err, kErrSlotRange);
+        if (rg == 0)
+            for (int t = 0; t < T; t++)
+                *reinterpret_cast<uint2 *>(p.out + (row0 + t) * p.ld_out + static_cast<int64_t>(h) * V + j0) = make_uint2(0u, 0u);
+        return;
+    }
+    const bool has_state = slot >= 0;
+    const bool writable = has_state && slot != p.null_slot;
+    float *tile = has_state ? p.pool + slot * p.slot_stride + static_cast<int64_t>(h) * K * V : nullptr;
+    float4 S[RPT];
+    if (has_state) {
+#pragma unroll
+        for (int i = 0; i < RPT; i++)
+            S[i] = *reinterpret_cast<const float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V + j0);
+    } else {
+#pragma unroll
+        for (int i = 0; i < RPT; i++) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int64_t HK = static_cast<int64_t>(p.H) * K;
+    // every token's gate, raw q/k and norm partials (threads c < K, one channel each)
+    if (tid < K) {
+        const float expA = expf(__ldg(p.A_log + h));
+        const float dtb = p.dt_bias ? __ldg(p.dt_bias + h * K + tid) : 0.f;
+        for (int t = 0; t < T; t++) {
+            const uint16_t *row = p.qkv + (row0 + t) * p.ld_qkv;
+            const float q = bf16_to_f32(row[h * K + tid]);
+            const float k = bf16_to_f32(row[HK + h * K + tid]);
+            const float g = gate_log_decay(bf16_to_f32(p.rg[(row0 + t) * p.ld_g + h * K + tid]) + dtb, expA, p.has_lb, p.lb);
+            s_a[t][tid] = expf(g);
+            s_k[t][tid] = k;
+            s_q[t][tid] = q;
+            const float qq = warp_sum(q * q), kk = warp_sum(k * k), qk = warp_sum(q * k);
+            if (lane == 0) { s_part[t][warp][0] = qq; s_part[t][warp][1] = kk; s_part[t][warp][2] = qk; }
+        }
+    }
+    // the CTA's value columns of every token (threads (t, cg))
+    if (rg < T) {
+        const uint16_t *vp = p.qkv + (row0 + rg) * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * V + j0;
+        s_v[rg][cg] = make_float4(bf16_to_f32(vp[0]), bf16_to_f32(vp[1]), bf16_to_f32(vp[2]), bf16_to_f32(vp[3]));
+    }
+    __syncthreads();
+    if (tid < T) {
+        float qq = 0.f, kk = 0.f, qk = 0.f;
+#pragma unroll
+        for (int w = 0; w < KW; w++) { qq += s_part[tid][w][0]; kk += s_part[tid][w][1]; qk += s_part[tid][w][2]; }
+        const float rq = p.scale * rsqrtf(qq + p.eps), rk = rsqrtf(kk + p.eps);
+        s_tok[tid][0] = rq;
+        s_tok[tid][1] = rk;
+        s_tok[tid][2] = qk * rq * rk;
+        s_tok[tid][3] = sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h]));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < kSpecMaxT; t++) {
+        if (t >= T) break;
+        const int bb = t & 1;
+        float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const int r = rg + 16 * i;
+            const float a = s_a[t][r], kr = s_k[t][r], qr = s_q[t][r];
+            S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
+            pk[0] += kr * S[i].x; pk[1] += kr * S[i].y; pk[2] += kr * S[i].z; pk[3] += kr * S[i].w;
+            pq[0] += qr * S[i].x; pq[1] += qr * S[i].y; pq[2] += qr * S[i].z; pq[3] += qr * S[i].w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 8);
+            pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 16);
+            pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 8);
+            pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 16);
+        }
+        if (lane < 8) {
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+                s_red[bb][warp][0][cg * 4 + jj] = pk[jj];
+                s_red[bb][warp][1][cg * 4 + jj] = pq[jj];
+            }
+        }
+        __syncthreads();
+        const float rq = s_tok[t][0], rk = s_tok[t][1], qkh = s_tok[t][2], beta = s_tok[t][3];
+        const float4 v4 = s_v[t][cg];
+        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+        float u[4], o[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            const int c = cg * 4 + jj;
+            const float ks = (s_red[bb][0][0][c] + s_red[bb][1][0][c] + s_red[bb][2][0][c] + s_red[bb][3][0][c]) * rk;
+            const float qs = (s_red[bb][0][1][c] + s_red[bb][1][1][c] + s_red[bb][2][1][c] + s_red[bb][3][1][c]) * rq;
+            u[jj] = beta * (vv[jj] - ks);
+            o[jj] = qs + qkh * u[jj];
+        }
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const float kh = s_k[t][rg + 16 * i] * rk;
+            S[i].x += kh * u[0]; S[i].y += kh * u[1]; S[i].z += kh * u[2]; S[i].w += kh * u[3];
+        }
+        if (rg == 0) {
+            uint2 packed;
+            packed.x = static_cast<uint32_t>(f32_to_bf16(o[0])) | (static_cast<uint32_t>(f32_to_bf16(o[1])) << 16);
+            packed.y = static_cast<uint32_t>(f32_to_bf16(o[2])) | (static_cast<uint32_t>(f32_to_bf16(o[3])) << 16);
+            *reinterpret_cast<uint2 *>(p.out + (row0 + t) * p.ld_out + static_cast<int64_t>(h) * V + j0) = packed;
+        }
+    }
+    if (writable) {
+#pragma unroll
+        for (int i = 0; i < RPT; i++)
+            *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V + j0) = S[i];
+    }
+}
+
+template <int K, int V>
+static cudaError_t launch_spec_kv(const Params &p, int T, int64_t num_reqs, cudaStream_t stream)
+{
+    const int64_t grid = num_reqs * p.H * (V / 32);
+    spec_kernel<K, V><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, T);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_spec(const Params &p, int K, int V, int T, int64_t num_reqs, cudaStream_t stream)
+{
+    if (num_reqs <= 0) return cudaSuccess;
+    if (T > kSpecMaxT)  // longer requests take the token-streaming recurrent kernel
+        return launch_recurrent(p, K, V, kRowsSpec, T, nullptr, 0, num_reqs, stream);
+#define KDA_SPEC_CASE(KK, VV) \
+    if (K == KK && V == VV) return launch_spec_kv<KK, VV>(p, T, num_reqs, stream);
+    KDA_SPEC_CASE(32, 32) KDA_SPEC_CASE(32, 64) KDA_SPEC_CASE(32, 128)
+    KDA_SPEC_CASE(64, 32) KDA_SPEC_CASE(64, 64) KDA_SPEC_CASE(64, 128)
+    KDA_SPEC_CASE(128, 32) KDA_SPEC_CASE(128, 64) KDA_SPEC_CASE(128, 128)
+#undef KDA_SPEC_CASE
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_gate(const Params &p, int K, int64_t N, float *g_out, float *beta_out,
