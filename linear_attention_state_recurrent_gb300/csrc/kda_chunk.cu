@@ -65,7 +65,8 @@ constexpr uint32_t SM_DTB = SM_BETA + 256;    // fp32 [128] dt_bias of this head
 constexpr uint32_t SM_NRM = SM_DTB + 512;     // fp32 [2][64][2] half-row |q|^2, |k|^2
 constexpr uint32_t SM_MBAR = SM_NRM + 1024;
 constexpr uint32_t SM_TMEMP = SM_MBAR + 8;
-constexpr uint32_t SMEM_BYTES = SM_TMEMP + 8;
+constexpr uint32_t SM_WAITOK = SM_TMEMP + 4;
+constexpr uint32_t SMEM_BYTES = SM_WAITOK + 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(SM_TAB + 4 * 7 * 128 * 4 <= SM_SB_KD, "constants table overlaps Kd^T");
 // phase C aliases
@@ -296,6 +297,22 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
         st_shared_u4(base + tc::core_offset(r, i0, 64, 2), pack8_f16(a));
         st_shared_u4(base + tc::core_offset(r, i0 + 8, 64, 2), pack8_f16(a + 8));
     }
+}
+
+// Waits for the MMAs tracked by `mbar`: warp 0 polls the mbarrier, the other warps park
+// on the CTA barrier instead of spinning. Returns false (on every thread) if the wait
+// gave up.
+__device__ __forceinline__ bool wait_mma(uint32_t mbar, uint32_t parity, int warp, unsigned char *smem)
+{
+    volatile int *flag = reinterpret_cast<volatile int *>(smem + SM_WAITOK);
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait(mbar, parity);
+        if ((threadIdx.x & 31) == 0) *flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    const bool ok = *flag != 0;
+    tc::fence_after_sync();
+    return ok;
 }
 
 // byte offset of 16-byte chunk `ch` (0..15) of row r in a staged [64][128] bf16 tile
@@ -645,9 +662,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::gemm<2, 64, 128>(tmem + TM_XDIAG, sbase + SM_DIAGA, SBO128_TF32, sbase + SM_DIAGB, SBO128_TF32, false);
             tc::commit(mbar);
         }
-        ok &= tc::mbar_wait(mbar, phase);
+        ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
-        tc::fence_after_sync();
 
         // ================= Phase C: A, Aqk, T =================
         // this chunk's V rows -> staged tile (read in D3). The tile overlays the diagonal
@@ -718,9 +734,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             tc::gemm<0, 128, 128>(tmem + TM_P, sbase + SM_SA, SBO128_F16, sbase + SM_PB, SBO128_F16, false);
             tc::commit(mbar);
         }
-        ok &= tc::mbar_wait(mbar, phase);
+        ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
-        tc::fence_after_sync();
         // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 operand (rows r = 16 k4 .. +15)
         asm volatile("cp.async.wait_group 1;" ::: "memory");   // the V tile (older group) has landed
         __syncthreads();
@@ -748,9 +763,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             tc::gemm<0, 64, 64>(tmem + TM_P, sbase + SM_YA, SBO64_F16, sbase + SM_TB, SBO64_F16, false);
             tc::commit(mbar);
         }
-        ok &= tc::mbar_wait(mbar, phase);
+        ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
-        tc::fence_after_sync();
         // D5: U^T -> fp16 operand
         {
             float v[16];
@@ -768,9 +782,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             tc::gemm<0, 192, 64>(tmem + TM_P + 64, sbase + SM_UA, SBO64_F16, sbase + SM_SB, SBO64_F16, true);
             tc::commit(mbar);
         }
-        ok &= tc::mbar_wait(mbar, phase);
+        ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
-        tc::fence_after_sync();
         // D7: O^T -> bf16 tile [r][j] in shared memory, then 16-byte row stores
         {
             uint16_t *otile = reinterpret_cast<uint16_t *>(smem + SM_OTILE);

@@ -265,16 +265,32 @@ __global__ void __launch_bounds__(128, 6) spec_kernel(Params p, int T)
     if (tid < K) {
         const float expA = expf(__ldg(p.A_log + h));
         const float dtb = p.dt_bias ? __ldg(p.dt_bias + h * K + tid) : 0.f;
-        for (int t = 0; t < T; t++) {
-            const uint16_t *row = p.qkv + (row0 + t) * p.ld_qkv;
-            const float q = bf16_to_f32(row[h * K + tid]);
-            const float k = bf16_to_f32(row[HK + h * K + tid]);
-            const float g = gate_log_decay(bf16_to_f32(p.rg[(row0 + t) * p.ld_g + h * K + tid]) + dtb, expA, p.has_lb, p.lb);
-            s_a[t][tid] = expf(g);
-            s_k[t][tid] = k;
-            s_q[t][tid] = q;
-            const float qq = warp_sum(q * q), kk = warp_sum(k * k), qk = warp_sum(q * k);
-            if (lane == 0) { s_part[t][warp][0] = qq; s_part[t][warp][1] = kk; s_part[t][warp][2] = qk; }
+        // batches of 8 tokens: issue the batch's loads before using any of them
+        for (int t0 = 0; t0 < T; t0 += 8) {
+            uint16_t qr[8], kr[8], gr[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                if (t0 + u < T) {
+                    const int64_t rr = row0 + t0 + u;
+                    const uint16_t *row = p.qkv + rr * p.ld_qkv;
+                    qr[u] = row[h * K + tid];
+                    kr[u] = row[HK + h * K + tid];
+                    gr[u] = p.rg[rr * p.ld_g + h * K + tid];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int t = t0 + u;
+                if (t < T) {
+                    const float q = bf16_to_f32(qr[u]), k = bf16_to_f32(kr[u]);
+                    const float g = gate_log_decay(bf16_to_f32(gr[u]) + dtb, expA, p.has_lb, p.lb);
+                    s_a[t][tid] = expf(g);
+                    s_k[t][tid] = k;
+                    s_q[t][tid] = q;
+                    const float qq = warp_sum(q * q), kk = warp_sum(k * k), qk = warp_sum(q * k);
+                    if (lane == 0) { s_part[t][warp][0] = qq; s_part[t][warp][1] = kk; s_part[t][warp][2] = qk; }
+                }
+            }
         }
     }
     // the CTA's value columns of every token (threads (t, cg))
