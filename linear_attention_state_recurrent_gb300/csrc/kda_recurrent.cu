@@ -224,11 +224,10 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 constexpr int kSpecMaxT = 16;
 
 template <int K, int V>
-__global__ void __launch_bounds__(128, 6) spec_kernel(Params p, int T)
+__global__ void __launch_bounds__(128, 7) spec_kernel(Params p, int T)
 {
-    constexpr int VT = 32, VS = V / VT, RPT = K / 16, KW = K / 32;
+    constexpr int VT = 32, VS = V / VT, RPT = K / 16;
     __shared__ float s_a[kSpecMaxT][K], s_k[kSpecMaxT][K], s_q[kSpecMaxT][K];
-    __shared__ float s_part[kSpecMaxT][KW][3];
     __shared__ float s_tok[kSpecMaxT][4];          // rq, rk, q^.k^, beta
     __shared__ float s_red[2][4][2][VT];
     __shared__ float4 s_v[kSpecMaxT][VT / 4];      // this CTA's value columns of every token
@@ -261,11 +260,17 @@ __global__ void __launch_bounds__(128, 6) spec_kernel(Params p, int T)
         for (int i = 0; i < RPT; i++) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const int64_t HK = static_cast<int64_t>(p.H) * K;
-    // every token's gate, raw q/k and norm partials (threads c < K, one channel each)
+    uint16_t braw = 0;
+    if (tid < T) braw = p.rb[(row0 + tid) * p.ld_beta + h];
+    // the CTA's value columns of every token (threads (t, cg))
+    if (rg < T) {
+        const uint16_t *vp = p.qkv + (row0 + rg) * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * V + j0;
+        s_v[rg][cg] = make_float4(bf16_to_f32(vp[0]), bf16_to_f32(vp[1]), bf16_to_f32(vp[2]), bf16_to_f32(vp[3]));
+    }
+    // every token's gate and raw q/k (threads c < K, one channel each), in batches of 8
     if (tid < K) {
         const float expA = expf(__ldg(p.A_log + h));
         const float dtb = p.dt_bias ? __ldg(p.dt_bias + h * K + tid) : 0.f;
-        // batches of 8 tokens: issue the batch's loads before using any of them
         for (int t0 = 0; t0 < T; t0 += 8) {
             uint16_t qr[8], kr[8], gr[8];
 #pragma unroll
@@ -282,32 +287,39 @@ __global__ void __launch_bounds__(128, 6) spec_kernel(Params p, int T)
             for (int u = 0; u < 8; u++) {
                 const int t = t0 + u;
                 if (t < T) {
-                    const float q = bf16_to_f32(qr[u]), k = bf16_to_f32(kr[u]);
                     const float g = gate_log_decay(bf16_to_f32(gr[u]) + dtb, expA, p.has_lb, p.lb);
                     s_a[t][tid] = expf(g);
-                    s_k[t][tid] = k;
-                    s_q[t][tid] = q;
-                    const float qq = warp_sum(q * q), kk = warp_sum(k * k), qk = warp_sum(q * k);
-                    if (lane == 0) { s_part[t][warp][0] = qq; s_part[t][warp][1] = kk; s_part[t][warp][2] = qk; }
+                    s_k[t][tid] = bf16_to_f32(kr[u]);
+                    s_q[t][tid] = bf16_to_f32(qr[u]);
                 }
             }
         }
     }
-    // the CTA's value columns of every token (threads (t, cg))
-    if (rg < T) {
-        const uint16_t *vp = p.qkv + (row0 + rg) * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * V + j0;
-        s_v[rg][cg] = make_float4(bf16_to_f32(vp[0]), bf16_to_f32(vp[1]), bf16_to_f32(vp[2]), bf16_to_f32(vp[3]));
-    }
     __syncthreads();
-    if (tid < T) {
+    // per-token |q|^2, |k|^2, q.k: 128 / kSpecMaxT threads per token, then shuffles
+    {
+        constexpr int TPT = 128 / kSpecMaxT;          // threads per token (8)
+        const int t = tid / TPT, part = tid % TPT;
         float qq = 0.f, kk = 0.f, qk = 0.f;
+        if (t < T) {
+            for (int c = part; c < K; c += TPT) {
+                const float q = s_q[t][c], k = s_k[t][c];
+                qq += q * q; kk += k * k; qk += q * k;
+            }
+        }
 #pragma unroll
-        for (int w = 0; w < KW; w++) { qq += s_part[tid][w][0]; kk += s_part[tid][w][1]; qk += s_part[tid][w][2]; }
-        const float rq = p.scale * rsqrtf(qq + p.eps), rk = rsqrtf(kk + p.eps);
-        s_tok[tid][0] = rq;
-        s_tok[tid][1] = rk;
-        s_tok[tid][2] = qk * rq * rk;
-        s_tok[tid][3] = sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h]));
+        for (int o = TPT / 2; o > 0; o >>= 1) {
+            qq += __shfl_xor_sync(0xffffffffu, qq, o);
+            kk += __shfl_xor_sync(0xffffffffu, kk, o);
+            qk += __shfl_xor_sync(0xffffffffu, qk, o);
+        }
+        if (t < T && part == 0) {
+            const float rq = p.scale * rsqrtf(qq + p.eps), rk = rsqrtf(kk + p.eps);
+            s_tok[t][0] = rq;
+            s_tok[t][1] = rk;
+            s_tok[t][2] = qk * rq * rk;
+        }
+        if (tid < T) s_tok[tid][3] = sigmoid_f(bf16_to_f32(braw));
     }
     __syncthreads();
 #pragma unroll
