@@ -665,48 +665,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
 
-        // ================= Phase C: A, Aqk, T =================
-        // this chunk's V rows -> staged tile (read in D3). The tile overlays the diagonal
-        // B operand (consumed by now) or, on the pairwise path, the stash read below.
+        // ================= Phase C (with the chain step's first product in flight) ========
+        // D1 + P: S^T -> fp16 operand SA, TMEM S^T <- S^T Diag(e^{b_last}), then issue
+        // P = S^T [K^G; Q^G]^T. Independent of A and T, so the P MMA runs while the CTA
+        // assembles A and solves for T. SA overlays the diagonal A operand (consumed by the
+        // Gram MMA) or, on the pairwise path, the stash, so that path does it after the
+        // row assembly. The V tile (read in D3) overlays the diagonal B operand.
         const uint16_t *vsrc = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD;
-        if (!flagged) {
+        auto stage_v_and_issue_p = [&]() {
             stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
             cp_async_commit();
-        }
-        assemble_slice(smem, tlane, warp, lane, flagged);
-        tc::fence_before_sync();
-        __syncthreads();
-        if (flagged) {
-            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
-            cp_async_commit();
-        }
-        solve_T(smem, tid);
-        {
-            // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
-            const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
-            const int r = tid >> 3, i0 = (tid & 7) * 8;
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int i = i0 + u;
-                v[u] = (i < r) ? Tm[r * AP + i] : (i == r ? 1.f : 0.f);
-            }
-            st_shared_u4(sbase + SM_TB + tc::core_offset(r, i0, 64, 2), pack8_f16(v));
-        }
-
-        // ================= Phase D: the chain step =================
-        // the next chunk's q, k, raw_g rows -> staging (the scratch of phase C is dead now)
-        if (c0 + C < row1) {
-            const int64_t nx = c0 + C;
-            const int nn = static_cast<int>((row1 - nx) < C ? (row1 - nx) : C);
-            stage_rows(sbase + SM_QST, p.qkv + nx * p.ld_qkv + h * KD, p.ld_qkv, nn, tid);
-            stage_rows(sbase + SM_KST, p.qkv + nx * p.ld_qkv + HK + h * KD, p.ld_qkv, nn, tid);
-            stage_rows(sbase + SM_GST, p.rg + nx * p.ld_g + h * KD, p.ld_g, nn, tid);
-            if (tid < nn) beta_raw = p.rb[(nx + tid) * p.ld_beta + h];
-        }
-        cp_async_commit();
-        // D1: S^T -> fp16 operand; TMEM S^T <- S^T Diag(e^{b_last})
-        {
             const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
             float v[2][16];
             tc::tmem_ld16(tlane + TM_S + 32 * k4, v[0]);
@@ -725,15 +693,45 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::tmem_st16(tlane + TM_S + c, v[hh]);
             }
             tc::tmem_st_wait();
-        }
-        tc::fence_proxy_async();
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
+                tc::fence_after_sync();
+                tc::gemm<0, 128, 128>(tmem + TM_P, sbase + SM_SA, SBO128_F16, sbase + SM_PB, SBO128_F16, false);
+                tc::commit(mbar);
+            }
+        };
+        if (!flagged) stage_v_and_issue_p();
+        assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            tc::gemm<0, 128, 128>(tmem + TM_P, sbase + SM_SA, SBO128_F16, sbase + SM_PB, SBO128_F16, false);
-            tc::commit(mbar);
+        if (flagged) stage_v_and_issue_p();
+        solve_T(smem, tid);
+        {
+            // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
+            const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
+            const int r = tid >> 3, i0 = (tid & 7) * 8;
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int i = i0 + u;
+                v[u] = (i < r) ? Tm[r * AP + i] : (i == r ? 1.f : 0.f);
+            }
+            st_shared_u4(sbase + SM_TB + tc::core_offset(r, i0, 64, 2), pack8_f16(v));
         }
+
+        // ================= Phase D: the rest of the chain step =================
+        // the next chunk's q, k, raw_g rows -> staging (the scratch of phase C is dead now)
+        if (c0 + C < row1) {
+            const int64_t nx = c0 + C;
+            const int nn = static_cast<int>((row1 - nx) < C ? (row1 - nx) : C);
+            stage_rows(sbase + SM_QST, p.qkv + nx * p.ld_qkv + h * KD, p.ld_qkv, nn, tid);
+            stage_rows(sbase + SM_KST, p.qkv + nx * p.ld_qkv + HK + h * KD, p.ld_qkv, nn, tid);
+            stage_rows(sbase + SM_GST, p.rg + nx * p.ld_g + h * KD, p.ld_g, nn, tid);
+            if (tid < nn) beta_raw = p.rb[(nx + tid) * p.ld_beta + h];
+        }
+        cp_async_commit();
         ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
         // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 operand (rows r = 16 k4 .. +15)
