@@ -255,16 +255,20 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
     const int s0 = 2 * (qd & 1);          // row blocks of this warp: s0, s0 + 1
     const int i0 = 16 * k4;               // first output column
     float off0[16], off1[16], dg[16];
-    // warp-collective loads: every lane loads the same columns, then keeps its own
-    if (k4 < s0) tc::tmem_ld16(tlane + TM_XOFF + off_b_base(s0) + i0, off0);
-    if (k4 < s0 + 1) tc::tmem_ld16(tlane + TM_XOFF + off_b_base(s0 + 1) + i0, off1);
-    if (!flagged && (k4 == s0 || k4 == s0 + 1)) tc::tmem_ld16(tlane + TM_XDIAG + i0, dg);
+    // warp-collective loads: every lane loads the same columns, then keeps its own. All
+    // three are loaded unconditionally (columns a lane does not need hold values it
+    // ignores) so that the arrays stay in registers.
+    tc::tmem_ld16(tlane + TM_XOFF + (k4 < s0 ? off_b_base(s0) + i0 : 0), off0);
+    tc::tmem_ld16(tlane + TM_XOFF + (k4 < s0 + 1 ? off_b_base(s0 + 1) + i0 : 0), off1);
+    tc::tmem_ld16(tlane + TM_XDIAG + i0, dg);
     tc::tmem_ld_wait();
     if (flagged && k4 == s) {
-        // pairwise in fp32 from the stash for the diagonal block
+        // pairwise in fp32 from the stash for the diagonal block; results go through a
+        // per-row shared-memory scratch so that dg[] keeps static indices (registers)
         const float *stk = reinterpret_cast<const float *>(smem + SM_STK);
         const float *stq = reinterpret_cast<const float *>(smem + SM_STQ);
         const float *stb = reinterpret_cast<const float *>(smem + SM_STB);
+        float *scratch = reinterpret_cast<float *>(smem + SM_XTMP) + ((qpart ? 64 : 0) + r) * 16;
         const float *xr = (qpart ? stq : stk) + r * KD;
         const float *br = stb + r * KD;
         for (int u = 0; u < 16; u++) {
@@ -275,8 +279,10 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
                 const float *bi = stb + i * KD;
                 for (int c = 0; c < KD; c++) acc += xr[c] * ki[c] * __expf(br[c] - bi[c]);
             }
-            dg[u] = acc;
+            scratch[u] = acc;
         }
+#pragma unroll
+        for (int u = 0; u < 16; u++) dg[u] = scratch[u];
     }
     const float beta = qpart ? 1.f : reinterpret_cast<const float *>(smem + SM_BETA)[r];
     float a[16];
@@ -495,36 +501,33 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         int flag = 0;
         {
             const int c = tid & (KD - 1), s = tid >> 7;
-            float T[8], E[8];
+            // block s covers warps 2s, 2s+1; scalars only, so everything stays in registers
+            float G = 1.f, Hh = 1.f, D1 = 1.f, D12 = 1.f, T0 = 0.f, X = 1.f, Y = 1.f, gc = 1.f, P = 0.f;
 #pragma unroll
             for (int w = 0; w < 8; w++) {
-                T[w] = tot[w * KD + c];
-                E[w] = __expf(T[w]);
-            }
-            // block s covers warps 2s, 2s+1 (selects keep the arrays in registers)
-            float G = 1.f, Hh = 1.f, D1 = 1.f, D12 = 1.f, T0 = 0.f, X = 1.f, Y = 1.f;
-#pragma unroll
-            for (int w = 0; w < 8; w++) {
-                if (w < 2 * s) G *= E[w];
-                if (w >= 2 * s + 2) Hh *= E[w];
-                if (w == 2 * s) { T0 = T[w]; X = E[w]; }
-                if (w == 2 * s + 1) Y = E[w];
-                if (w == 2 * s + 2 || w == 2 * s + 3) D1 *= E[w];
-                if (w >= 2 * s + 2 && w <= 2 * s + 5) D12 *= E[w];
+                const float t = tot[w * KD + c];
+                const float ew = __expf(t);
+                if (w < 2 * s) G *= ew;
+                if (w >= 2 * s + 2) Hh *= ew;
+                if (w == 2 * s) { T0 = t; X = ew; }
+                if (w == 2 * s + 1) Y = ew;
+                if (w == 2 * s + 2 || w == 2 * s + 3) D1 *= ew;
+                if (w >= 2 * s + 2 && w <= 2 * s + 5) D12 *= ew;
+                flag |= (t < -kHalfSpan) ? 1 : 0;
+                gc *= ew;
+                P += t;
             }
             if (s > 2) D1 = 0.f;
             if (s > 1) D12 = 0.f;
-            const float vals[7] = {T0, X, Y, G, Hh, D1, D12};
-#pragma unroll
-            for (int k = 0; k < 7; k++) *reinterpret_cast<float *>(smem + SM_TAB + tab_off(s, k, c)) = vals[k];
+            float *tabp = reinterpret_cast<float *>(smem + SM_TAB);
+            tabp[tab_off(s, 0, c) >> 2] = T0;
+            tabp[tab_off(s, 1, c) >> 2] = X;
+            tabp[tab_off(s, 2, c) >> 2] = Y;
+            tabp[tab_off(s, 3, c) >> 2] = G;
+            tabp[tab_off(s, 4, c) >> 2] = Hh;
+            tabp[tab_off(s, 5, c) >> 2] = D1;
+            tabp[tab_off(s, 6, c) >> 2] = D12;
             if (s == 0) {
-                float P = 0.f, gc = 1.f;
-#pragma unroll
-                for (int w = 0; w < 8; w++) {
-                    flag |= (T[w] < -kHalfSpan) ? 1 : 0;
-                    gc *= E[w];
-                    P += T[w];
-                }
                 reinterpret_cast<float *>(smem + SM_GC)[c] = gc;
                 reinterpret_cast<float *>(smem + SM_BLAST)[c] = P;
             }
