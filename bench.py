@@ -147,13 +147,22 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value over the ranks (the timed region's duration of the slowest rank)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def shard_units(total, world, rank):
+    """Units [lo, hi) of `total` independent units owned by `rank` (contiguous blocks)."""
+    per, extra = divmod(total, world)
+    lo = rank * per + min(rank, extra)
+    return lo, lo + per + (1 if rank < extra else 0)
 
 
 def source_sha(*names):

@@ -160,3 +160,26 @@ def test_prefill_repeat_bit_identical(kda):
         hx.run_gpu(dw, kda, out=out)
         assert torch.equal(out.view(torch.int16), first.view(torch.int16))
     assert torch.equal(dw.pool_flat.view(torch.int32), pool_first.view(torch.int32))
+
+
+def test_prefill_slot_semantics(kda):
+    """The chunk kernel's slot handling: null slot read-only, negative slot from zero,
+    out-of-range slot flagged with zero outputs and no state access."""
+    w = wl.varlen_case([70, 5, 130, 64, 1], 2, 128, 128, seed=29, num_slots=12)
+    w.index_buf = np.array([[3], [-1], [11], [40], [7]], np.int32)
+    w.null_slot = 11
+    dw = hx.DeviceWorkload(w)
+    out = hx.run_gpu(dw, kda)
+    ref = ko.run(w)
+    assert ref.err_flags == ko.ERR_SLOT_OUT_OF_RANGE
+    hx.check(dw, out, ref, fp32_path=False, label="prefill slot semantics")
+    o = out.float().cpu()
+    assert torch.all(o[205:269] == 0)
+
+
+def test_mixed_batch_null_slot_padding(kda):
+    lengths = [1, 1, 1, 100]
+    w = wl.varlen_case(lengths, 2, 128, 128, seed=33, num_decodes=3, kind="mixed", num_slots=10)
+    w.index_buf = np.array([[0], [4], [0], [6]], np.int32)
+    w.null_slot = 0
+    _run(kda, w, "mixed null slot")
