@@ -63,8 +63,9 @@ constexpr uint32_t SM_BLAST = SM_GC + 512; // fp32 [128] b_last
 constexpr uint32_t SM_BETA = SM_BLAST + 512;  // fp32 [64]
 constexpr uint32_t SM_DTB = SM_BETA + 256;    // fp32 [128] dt_bias of this head
 constexpr uint32_t SM_NRM = SM_DTB + 512;     // fp32 [2][64][2] half-row |q|^2, |k|^2
-constexpr uint32_t SM_MBAR = SM_NRM + 1024;
-constexpr uint32_t SM_TMEMP = SM_MBAR + 8;
+constexpr uint32_t SM_MBAR = SM_NRM + 1024;    // mbarrier of the Gram-block MMAs
+constexpr uint32_t SM_MBARC = SM_MBAR + 8;     // mbarrier of the chain MMAs
+constexpr uint32_t SM_TMEMP = SM_MBARC + 8;
 constexpr uint32_t SM_WAITOK = SM_TMEMP + 4;
 constexpr uint32_t SMEM_BYTES = SM_WAITOK + 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -75,9 +76,6 @@ constexpr uint32_t SM_XTMP = SM_OFFA + 17408;  // fp32 scratch (<= 15360 B)
 constexpr uint32_t SM_TMAT = SM_OFFB;          // fp32 [64][68]
 constexpr int AP = 68;                         // fp32 row pitch of AMAT / TMAT
 // phase D aliases
-constexpr uint32_t SM_SA = SM_DIAGA;           // fp16 [128 x 128] S^T
-constexpr uint32_t SM_YA = SM_DIAGA + 32768;   // fp16 [128 x 64]  (beta Y)^T
-constexpr uint32_t SM_UA = SM_DIAGA + 49152;   // fp16 [128 x 64]  U^T
 constexpr uint32_t SM_OTILE = SM_OFFB;         // bf16 [64][OT_PITCH] output rows
 constexpr int OT_PITCH = 136;                  // bf16 row pitch (272 B: 16-byte aligned rows)
 // input staging (bf16 [64 rows][128], 16-byte chunks XOR-swizzled by row):
@@ -97,11 +95,21 @@ constexpr uint32_t TM_P = 0;      // [0,64) K^G S -> U ; [64,128) O
 constexpr uint32_t TM_S = 128;    // S^T (128 columns)
 constexpr uint32_t TM_XOFF = 256; // 96 columns
 constexpr uint32_t TM_XDIAG = 352;// 64 columns
+constexpr uint32_t TM_A = 416;    // A operands of the chain MMAs, fp16 packed in pairs:
+                                  // S^T (64 columns), then (beta Y)^T at +0 and U^T at +32
 
 // stride byte offsets of the operand tiles
 constexpr uint32_t SBO128_F16 = 128 * 2 * 8;  // K = 128 fp16
 constexpr uint32_t SBO128_TF32 = 128 * 4 * 8; // K = 128 tf32
 constexpr uint32_t SBO64_F16 = 64 * 2 * 8;    // K = 64 fp16
+
+// Packs 2*n fp32 values into n fp16 pairs (element 2i in the low half).
+template <int n>
+__device__ __forceinline__ void pack_pairs(const float *v, uint32_t (&o)[n])
+{
+#pragma unroll
+    for (int i = 0; i < n; i++) o[i] = tc::pack_f16x2(v[2 * i], v[2 * i + 1]);
+}
 
 struct Args {
     Params p;
@@ -397,8 +405,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     const int64_t HK = static_cast<int64_t>(H) * KD;
 
     const uint32_t sbase = tc::smem_addr(smem);
-    const uint32_t mbar = sbase + SM_MBAR;
-    if (tid == 0) tc::mbar_init(mbar, 1);
+    const uint32_t mbar = sbase + SM_MBAR, mbarc = sbase + SM_MBARC;
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::mbar_init(mbarc, 1);
+    }
     if (tid < KD) reinterpret_cast<float *>(smem + SM_DTB)[tid] = p.dt_bias ? p.dt_bias[h * KD + tid] : 0.f;
     if (warp == 0) tc::tmem_alloc<512>(sbase + SM_TMEMP);
     tc::fence_before_sync();
@@ -406,7 +417,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEMP);
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // this warp's lanes
-    uint32_t phase = 0;
+    uint32_t phase = 0, phasec = 0;
     bool ok = true;
 
     // thread roles
@@ -665,19 +676,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::gemm<2, 64, 128>(tmem + TM_XDIAG, sbase + SM_DIAGA, SBO128_TF32, sbase + SM_DIAGB, SBO128_TF32, false);
             tc::commit(mbar);
         }
-        ok &= wait_mma(mbar, phase, warp, smem);
-        phase ^= 1;
-
-        // ================= Phase C (with the chain step's first product in flight) ========
-        // D1 + P: S^T -> fp16 operand SA, TMEM S^T <- S^T Diag(e^{b_last}), then issue
-        // P = S^T [K^G; Q^G]^T. Independent of A and T, so the P MMA runs while the CTA
-        // assembles A and solves for T. SA overlays the diagonal A operand (consumed by the
-        // Gram MMA) or, on the pairwise path, the stash, so that path does it after the
-        // row assembly. The V tile (read in D3) overlays the diagonal B operand.
-        const uint16_t *vsrc = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD;
-        auto stage_v_and_issue_p = [&]() {
-            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
-            cp_async_commit();
+        // D1 while the Gram MMAs run: S^T -> fp16 pairs in TMEM (A of P), and
+        // TMEM S^T <- S^T Diag(e^{b_last}); then issue P = S^T [K^G; Q^G]^T behind them.
+        {
             const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
             float v[2][16];
             tc::tmem_ld16(tlane + TM_S + 32 * k4, v[0]);
@@ -686,8 +687,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 #pragma unroll
             for (int hh = 0; hh < 2; hh++) {
                 const int c = 32 * k4 + 16 * hh;
-                st_shared_u4(sbase + SM_SA + tc::core_offset(jv, c, KD, 2), pack8_f16(v[hh]));
-                st_shared_u4(sbase + SM_SA + tc::core_offset(jv, c + 8, KD, 2), pack8_f16(v[hh] + 8));
+                uint32_t pk8[8];
+                pack_pairs<8>(v[hh], pk8);
+                tc::tmem_st8u(tlane + TM_A + (c >> 1), pk8);
 #pragma unroll
                 for (int u = 0; u < 16; u += 4) {
                     const float4 g4 = *reinterpret_cast<const float4 *>(gc + c + u);
@@ -696,20 +698,32 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::tmem_st16(tlane + TM_S + c, v[hh]);
             }
             tc::tmem_st_wait();
-            tc::fence_proxy_async();
-            tc::fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                tc::fence_after_sync();
-                tc::gemm<0, 128, 128>(tmem + TM_P, sbase + SM_SA, SBO128_F16, sbase + SM_PB, SBO128_F16, false);
-                tc::commit(mbar);
-            }
-        };
-        if (!flagged) stage_v_and_issue_p();
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            tc::gemm_ta<128, 128>(tmem + TM_P, tmem + TM_A, sbase + SM_PB, SBO128_F16, false);
+            tc::commit(mbarc);
+        }
+        ok &= wait_mma(mbar, phase, warp, smem);
+        phase ^= 1;
+
+        // ================= Phase C: A, Aqk, T (the P product is in flight) =================
+        // The V tile (read in D3) overlays the diagonal B operand (consumed by now) or, on
+        // the pairwise path, the stash read by the row assembly.
+        const uint16_t *vsrc = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD;
+        if (!flagged) {
+            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
+            cp_async_commit();
+        }
         assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
-        if (flagged) stage_v_and_issue_p();
+        if (flagged) {
+            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
+            cp_async_commit();
+        }
         solve_T(smem, tid);
         {
             // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
@@ -735,9 +749,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             if (tid < nn) beta_raw = p.rb[(nx + tid) * p.ld_beta + h];
         }
         cp_async_commit();
-        ok &= wait_mma(mbar, phase, warp, smem);
-        phase ^= 1;
-        // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 operand (rows r = 16 k4 .. +15)
+        ok &= wait_mma(mbarc, phasec, warp, smem);
+        phasec ^= 1;
+        // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 pairs in TMEM (rows r = 16 k4 .. +15)
         asm volatile("cp.async.wait_group 1;" ::: "memory");   // the V tile (older group) has landed
         __syncthreads();
         {
@@ -753,38 +767,40 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 const float vv = bf16_to_f32(vt[(st_off(r, jv >> 3) >> 1) + (jv & 7)]);
                 v[u] = bet[r] * (vv - v[u]);
             }
-            st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
-            st_shared_u4(sbase + SM_YA + tc::core_offset(jv, r0 + 8, 64, 2), pack8_f16(v + 8));
+            uint32_t pk8[8];
+            pack_pairs<8>(v, pk8);
+            tc::tmem_st8u(tlane + TM_A + (r0 >> 1), pk8);
+            tc::tmem_st_wait();
         }
-        tc::fence_proxy_async();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            tc::gemm<0, 64, 64>(tmem + TM_P, sbase + SM_YA, SBO64_F16, sbase + SM_TB, SBO64_F16, false);
-            tc::commit(mbar);
+            tc::gemm_ta<64, 64>(tmem + TM_P, tmem + TM_A, sbase + SM_TB, SBO64_F16, false);
+            tc::commit(mbarc);
         }
-        ok &= wait_mma(mbar, phase, warp, smem);
-        phase ^= 1;
-        // D5: U^T -> fp16 operand
+        ok &= wait_mma(mbarc, phasec, warp, smem);
+        phasec ^= 1;
+        // D5: U^T -> fp16 pairs in TMEM (A of the last product)
         {
             float v[16];
             const int r0 = 16 * k4;
             tc::tmem_ld16(tlane + TM_P + r0, v);
             tc::tmem_ld_wait();
-            st_shared_u4(sbase + SM_UA + tc::core_offset(jv, r0, 64, 2), pack8_f16(v));
-            st_shared_u4(sbase + SM_UA + tc::core_offset(jv, r0 + 8, 64, 2), pack8_f16(v + 8));
+            uint32_t pk8[8];
+            pack_pairs<8>(v, pk8);
+            tc::tmem_st8u(tlane + TM_A + 32 + (r0 >> 1), pk8);
+            tc::tmem_st_wait();
         }
-        tc::fence_proxy_async();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            tc::gemm<0, 192, 64>(tmem + TM_P + 64, sbase + SM_UA, SBO64_F16, sbase + SM_SB, SBO64_F16, true);
-            tc::commit(mbar);
+            tc::gemm_ta<192, 64>(tmem + TM_P + 64, tmem + TM_A + 32, sbase + SM_SB, SBO64_F16, true);
+            tc::commit(mbarc);
         }
-        ok &= wait_mma(mbar, phase, warp, smem);
-        phase ^= 1;
+        ok &= wait_mma(mbarc, phasec, warp, smem);
+        phasec ^= 1;
         // D7: O^T -> bf16 tile [r][j] in shared memory, then 16-byte row stores
         {
             uint16_t *otile = reinterpret_cast<uint16_t *>(smem + SM_OTILE);

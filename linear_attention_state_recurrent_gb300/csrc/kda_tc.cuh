@@ -84,6 +84,24 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_saddr, uint32_t
     }
 }
 
+// D[M=128, N] (+)= A[128, Kd] * B[N, Kd]^T with A in tensor memory (fp16 packed two per
+// 32-bit column: column c holds k = 2c in the low and 2c+1 in the high half; one K step
+// of 16 spans 8 columns) and B in shared memory.
+template <int N, int KD>
+__device__ __forceinline__ void gemm_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr, uint32_t b_sbo,
+                                        bool accumulate)
+{
+    constexpr uint32_t ID = instr_desc(0, 128, N);
+#pragma unroll
+    for (int ks = 0; ks < KD / 16; ks++) {
+        const uint64_t db = smem_desc(b_saddr + ks * 256, 128, b_sbo);
+        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+        asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                     " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+                     :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(ID), "r"(acc));
+    }
+}
+
 __device__ __forceinline__ void commit(uint32_t mbar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -162,6 +180,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
                     "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
                     "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
                     "r"(__float_as_uint(v[15]))
+                 : "memory");
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane (warp-collective)
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                    "r"(v[6]), "r"(v[7])
                  : "memory");
 }
 
