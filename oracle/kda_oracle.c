@@ -142,7 +142,7 @@ void kda_oracle_gate(const uint16_t *raw_g, int64_t ld_g, const uint16_t *raw_be
 static void recur_one(const heads_t *hp, const uint16_t *mixed_qkv, int64_t ld_qkv,
                       const uint16_t *raw_g, int64_t ld_g, const uint16_t *raw_beta,
                       int64_t ld_beta, int64_t t0, int64_t t1, int h, double *S,
-                      double *out, int64_t ld_out)
+                      double *out, int64_t ld_out, double *ckpt, int64_t ckpt_stride)
 {
     int K = hp->K, V = hp->V;
     double *qh = malloc(sizeof(double) * K), *kh = malloc(sizeof(double) * K);
@@ -176,6 +176,9 @@ static void recur_one(const heads_t *hp, const uint16_t *mixed_qkv, int64_t ld_q
                 acc += S[(size_t)c * V + j] * qh[c];
             out[t * ld_out + (int64_t)h * V + j] = acc;
         }
+        /* optional copy of the state after this token */
+        if (ckpt)
+            memcpy(ckpt + (t - t0) * ckpt_stride, S, sizeof(double) * (size_t)K * V);
     }
     free(qh); free(kh); free(g); free(v); free(u);
 }
@@ -208,7 +211,38 @@ void kda_oracle_recurrent(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint1
         int h = head_lo + (int)(w % nh);
         double *S = states + ((size_t)s * H + h) * (size_t)K * V;
         recur_one(&hp, mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, row_begin[s],
-                  row_end[s], h, S, out, ld_out);
+                  row_end[s], h, S, out, ld_out, NULL, 0);
+    }
+}
+
+/*
+ * As kda_oracle_recurrent over all heads, and also records the state after every token:
+ * ckpt is [num_seqs][Tmax][H][K][V] fp64; the state of sequence s, head h after its
+ * t-th token (t < row_end - row_begin <= Tmax) is ckpt[((s*Tmax + t)*H + h)*K*V ...].
+ */
+void kda_oracle_recurrent_ckpt(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                               int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                               const int64_t *row_begin, const int64_t *row_end, int64_t num_seqs,
+                               int H, int K, int V, const float *A_log, const float *dt_bias,
+                               int has_lower_bound, double lower_bound, double scale, double eps,
+                               double *states, double *out, int64_t ld_out, double *ckpt,
+                               int64_t Tmax, int nthreads)
+{
+    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps};
+    int64_t work = num_seqs * H;
+    size_t KV = (size_t)K * V;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t w = 0; w < work; w++) {
+        int64_t s = w / H;
+        int h = (int)(w % H);
+        double *S = states + ((size_t)s * H + h) * KV;
+        recur_one(&hp, mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, row_begin[s],
+                  row_end[s], h, S, out, ld_out, ckpt + ((size_t)s * Tmax * H + h) * KV,
+                  (int64_t)H * (int64_t)KV);
     }
 }
 

@@ -66,6 +66,9 @@ def _load():
         lib.kda_oracle_chunked.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I, I, I, P, P,
                                            I, D, D, D, I, P, P, I64, I]
         lib.kda_oracle_chunked.restype = None
+        lib.kda_oracle_recurrent_ckpt.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I, I, I, P, P,
+                                                  I, D, D, D, P, P, I64, P, I64, I]
+        lib.kda_oracle_recurrent_ckpt.restype = None
         lib.kda_oracle_max_threads.argtypes = []
         lib.kda_oracle_max_threads.restype = I
         _lib = lib
@@ -175,3 +178,78 @@ def run(w, *, heads: tuple | None = None, chunked: bool = False, chunk_size: int
             out[b0:b1, :] = 0.0
     return OracleResult(out=out, final_states=states, slots=slots, writes=writes & valid,
                         err_flags=err, heads=(h_lo, h_hi))
+
+
+@dataclasses.dataclass
+class CheckpointResult:
+    out: np.ndarray            # fp64 [N, H*V]
+    ckpt: np.ndarray           # fp64 [R, T, H, K, V] state after each token
+    slots: np.ndarray          # int64 [R, T] slot of each (request, token) column
+    writes: np.ndarray         # bool [R, T] the checkpoint is written to its slot
+    err_flags: int
+
+    def expected_pool(self, pool: np.ndarray) -> np.ndarray:
+        exp = pool.astype(np.float64)
+        R, T = self.slots.shape
+        HKV = self.ckpt[0, 0].size if self.ckpt.size else 0
+        for r in range(R):
+            for t in range(T):
+                if self.writes[r, t]:
+                    exp[self.slots[r, t], :HKV] = self.ckpt[r, t].reshape(-1)
+        return exp
+
+
+def run_spec_checkpoints(w, nthreads: int = 0) -> CheckpointResult:
+    """Spec-verify with per-token state checkpoints (a spec-verify Workload with
+    index_stride >= tokens_per_req). Request r reads its initial state from
+    index_buf[r*stride + 0] (with the slot rules of `run`) and the state after its token t
+    is written to index_buf[r*stride + t] unless that slot is negative, the null slot or
+    out of range (the last sets bit 0 of the error word). If column 0 is out of range the
+    request's outputs are zero and nothing is read or written."""
+    lib = _load()
+    H, K, V, T = w.H, w.K, w.V, w.tokens_per_req
+    R = w.num_entries
+    flat = np.asarray(w.index_buf).reshape(-1)
+    slots = np.stack([flat[r * w.index_stride: r * w.index_stride + T] for r in range(R)]).astype(np.int64) \
+        if R else np.zeros((0, T), np.int64)
+    states = np.zeros((R, H, K, V), dtype=np.float64)
+    valid = np.ones(R, dtype=bool)
+    err = 0
+    for r in range(R):
+        s0 = int(slots[r, 0])
+        if s0 >= w.num_slots:
+            valid[r] = False
+            err |= ERR_SLOT_OUT_OF_RANGE
+        elif s0 >= 0:
+            states[r] = w.pool[s0, : H * K * V].reshape(H, K, V).astype(np.float64)
+    writes = np.zeros((R, T), dtype=bool)
+    for r in range(R):
+        if not valid[r]:
+            continue
+        for t in range(T):
+            st = int(slots[r, t])
+            if st >= w.num_slots:
+                err |= ERR_SLOT_OUT_OF_RANGE
+            elif st >= 0 and st != w.null_slot:
+                writes[r, t] = True
+    out = np.zeros((w.N, H * V), dtype=np.float64)
+    ckpt = np.zeros((R, T, H, K, V), dtype=np.float64)
+    vidx = np.nonzero(valid)[0]
+    if len(vidx):
+        rb = np.array([r * T for r in vidx], dtype=np.int64)
+        re = rb + T
+        sub = np.ascontiguousarray(states[vidx])
+        subck = np.zeros((len(vidx), T, H, K, V), dtype=np.float64)
+        qkv = np.ascontiguousarray(w.mixed_qkv, dtype=np.uint16)
+        rg = np.ascontiguousarray(w.raw_g, dtype=np.uint16)
+        rbeta = np.ascontiguousarray(w.raw_beta, dtype=np.uint16)
+        A_log = np.ascontiguousarray(w.A_log, dtype=np.float32)
+        dt = None if w.dt_bias is None else np.ascontiguousarray(w.dt_bias, dtype=np.float32)
+        lb = w.lower_bound
+        lib.kda_oracle_recurrent_ckpt(_ptr(qkv), qkv.shape[1], _ptr(rg), rg.shape[1], _ptr(rbeta),
+                                      rbeta.shape[1], _ptr(rb), _ptr(re), len(vidx), H, K, V,
+                                      _ptr(A_log), _ptr(dt), int(lb is not None), float(lb or 0.0),
+                                      float(w.scale), float(w.eps), _ptr(sub), _ptr(out), H * V,
+                                      _ptr(subck), T, int(nthreads))
+        ckpt[vidx] = subck
+    return CheckpointResult(out=out, ckpt=ckpt, slots=slots, writes=writes, err_flags=err)

@@ -370,3 +370,34 @@ def test_planted_mistakes_are_caught():
     np.testing.assert_allclose(run(), gd["o"], atol=1e-15)
     for kw in ({"transpose": True}, {"sign": -1.0}, {"decay_after": True}):
         assert not np.allclose(run(**kw), gd["o"])
+
+
+def test_spec_checkpoints_pinned_to_recurrence():
+    """Checkpoint t equals the final state of running the first t+1 tokens alone (the same
+    pinned recurrence), bit-exactly; the outputs equal plain spec-verify's."""
+    s = wl.spec_verify(num_reqs=3, T=5, H=2, K=8, V=8, num_slots=64, num_padding=1, index_stride=5)
+    # distinct checkpoint slots for the real requests
+    s.index_buf = np.array([[3, 10, 11, 12, 13], [7, 20, 21, 22, 23], [0, 0, 0, 0, 0]], np.int32)
+    ck = ko.run_spec_checkpoints(s)
+    plain = ko.run(s)
+    np.testing.assert_array_equal(ck.out, plain.out)
+    np.testing.assert_array_equal(ck.ckpt[:2, -1], plain.final_states[:2])
+    for t in range(5):
+        part = wl.Workload(**{**s.__dict__, "tokens_per_req": t + 1,
+                              "mixed_qkv": s.mixed_qkv.reshape(3, 5, -1)[:, :t + 1].reshape(3 * (t + 1), -1),
+                              "raw_g": s.raw_g.reshape(3, 5, -1)[:, :t + 1].reshape(3 * (t + 1), -1),
+                              "raw_beta": s.raw_beta.reshape(3, 5, -1)[:, :t + 1].reshape(3 * (t + 1), -1)})
+        r = ko.run(part)
+        np.testing.assert_array_equal(ck.ckpt[:, t], r.final_states)
+    assert not ck.writes[2].any()          # padding request on the null slot writes nothing
+    assert ck.writes[:2].all()
+
+
+def test_spec_checkpoint_slot_rules():
+    s = wl.spec_verify(num_reqs=2, T=3, H=1, K=4, V=4, num_slots=16, num_padding=0, index_stride=4)
+    s.index_buf = np.array([[5, -1, 99, 0], [40, 1, 2, 3]], np.int32)
+    ck = ko.run_spec_checkpoints(s)
+    assert ck.err_flags == ko.ERR_SLOT_OUT_OF_RANGE
+    assert list(ck.writes[0]) == [True, False, False]
+    assert not ck.writes[1].any()
+    assert np.all(ck.out[3:6] == 0)
