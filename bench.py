@@ -245,7 +245,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--workload", choices=["decode", "prefill", "spec", "mixed"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "spec", "spec_ckpt", "mixed"], default="decode",
                     help="decode (default) is the headline line; the others time one row alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -388,12 +388,15 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
     elif args.workload == "mixed":
         w = wl.mixed_batch()
         metric, unit = "mixed-batch tokens/s", "tokens/s"
+    elif args.workload == "spec_ckpt":
+        w = wl.spec_checkpoints()
+        metric, unit = "spec-verify-checkpoints state-bytes GB/s", "GB/s"
     else:
         w = wl.spec_verify()
         metric, unit = "spec-verify state-bytes GB/s", "GB/s"
     dw = wl.DeviceWorkload(w, dev)
     out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
-    if args.workload == "spec":
+    if args.workload in ("spec", "spec_ckpt"):
         ms = time_spec_graph(torch, kda, w, dw, out, calls=20, replays=max(1, args.steps // 20))
         value = spec_state_bytes(w) * world / (ms * 1e-3) / 1e9
         line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -437,32 +440,37 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
 
 
 def spec_call_args(kda, w, dw, out, stream_handle):
-    """Pre-marshalled C-ABI arguments of one kda_spec_verify call (kept alive with the
-    structs they point to)."""
+    """Pre-marshalled C-ABI arguments of one kda_spec_verify (or, for a checkpoint
+    workload, kda_spec_verify_checkpoints) call, kept alive with the structs they point
+    to. Returns (function, args, keep-alive)."""
     hd = kda.make_heads(dw.A_log, dw.dt_bias, w.lower_bound, w.K, w.V, w.scale, w.eps)
     st = kda.make_state(dw.pool_view(), dw.indices_view(), w.null_slot)
-    args = (ctypes.c_void_p(dw.mixed_qkv.data_ptr()), dw.mixed_qkv.stride(0),
+    head = (ctypes.c_void_p(dw.mixed_qkv.data_ptr()), dw.mixed_qkv.stride(0),
             ctypes.c_void_p(dw.raw_g.data_ptr()), dw.raw_g.stride(0),
             ctypes.c_void_p(dw.raw_beta.data_ptr()), dw.raw_beta.stride(0),
-            w.num_entries, w.tokens_per_req, ctypes.byref(hd), ctypes.byref(st),
-            ctypes.c_void_p(out.data_ptr()), out.stride(0), None, ctypes.c_void_p(stream_handle))
-    return args, (hd, st)
+            w.num_entries, w.tokens_per_req)
+    tail = (ctypes.byref(hd), ctypes.byref(st), ctypes.c_void_p(out.data_ptr()), out.stride(0),
+            None, ctypes.c_void_p(stream_handle))
+    if w.kind == "spec_ckpt":
+        acc = None if dw.num_accepted is None else ctypes.c_void_p(dw.num_accepted.data_ptr())
+        return kda.lib.kda_spec_verify_checkpoints, head + (acc,) + tail, (hd, st)
+    return kda.lib.kda_spec_verify, head + tail, (hd, st)
 
 
 def time_spec_graph(torch, kda, w, dw, out, calls=20, replays=50):
     """Spec-verify calls are a few microseconds of GPU time, far below the host cost of a
     Python call, so they are timed as replays of a CUDA graph of `calls` launches."""
     cap = torch.cuda.Stream()
-    args, keep = spec_call_args(kda, w, dw, out, cap.cuda_stream)
+    fn, args, keep = spec_call_args(kda, w, dw, out, cap.cuda_stream)
     with torch.cuda.stream(cap):
         for _ in range(3):
-            if kda.lib.kda_spec_verify(*args):
+            if fn(*args):
                 raise RuntimeError(kda.last_error())
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):
         for _ in range(calls):
-            kda.lib.kda_spec_verify(*args)
+            fn(*args)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         g.replay()
@@ -479,10 +487,12 @@ def time_spec_graph(torch, kda, w, dw, out, calls=20, replays=50):
 
 def spec_state_bytes(w):
     """State bytes of one spec-verify call: each real request's tile read + written once,
-    each padding request's (null-slot) tile read only."""
+    each padding request's (null-slot) tile read only. With per-token checkpoints a real
+    request writes its tile once per token."""
     null = sum(1 for s in w.indices() if s == w.null_slot)
     real = w.num_entries - null
-    return (real * 2 + null) * 4 * w.K * w.V * w.H
+    writes = w.tokens_per_req if w.kind == "spec_ckpt" else 1
+    return (real * (1 + writes) + null) * 4 * w.K * w.V * w.H
 
 
 def time_calls(torch, fn, stream, n, warmup=2):
@@ -510,6 +520,18 @@ def measure_secondary(torch, kda, wl, dev, stream, pk):
                           "us_per_call": ms * 1e3, "state_gbs": sbytes / (ms * 1e-3) / 1e9,
                           "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                           "timing": "CUDA graph of 20 calls, 50 replays"}
+    del dw
+    # spec verify with per-token checkpoints: 16 requests x 8 tokens, 8 writes per request
+    w = wl.spec_checkpoints()
+    dw = wl.DeviceWorkload(w, dev)
+    ms = time_spec_graph(torch, kda, w, dw, out)
+    sbytes = spec_state_bytes(w)
+    res["spec_verify_checkpoints"] = {
+        "workload": "16 requests x 8 tokens, H=32, K=V=128, state stored after every token "
+                    "(block-table row of 8 slots), 2 padding requests on the null slot",
+        "us_per_call": ms * 1e3, "state_gbs": sbytes / (ms * 1e-3) / 1e9,
+        "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "timing": "CUDA graph of 20 calls, 50 replays"}
     del dw
     # chunked prefill: seed-1 lengths, 33,494 tokens
     w = wl.chunked_prefill(None)

@@ -24,8 +24,8 @@
  *  - Every tensor pointer is a DEVICE pointer owned by the caller. The library
  *    allocates nothing, keeps no state between calls, never synchronises the
  *    stream, and enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy
- *    default stream). kda_packed_decode and kda_spec_verify can be captured in a
- *    CUDA graph.
+ *    default stream). kda_packed_decode, kda_spec_verify and
+ *    kda_spec_verify_checkpoints can be captured in a CUDA graph.
  *  - bf16 values are passed as uint16_t bit patterns.
  *  - mixed_qkv: bf16 [N, ld_qkv]; row t = [ q (H*K) | k (H*K) | v (H*V) ], each
  *    part head-major ([H][K] or [H][V]). raw_g: bf16 [N, ld_g], H*K used.
@@ -137,6 +137,33 @@ int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
                     int64_t num_reqs, int32_t tokens_per_req, const kda_heads *heads,
                     const kda_state *state, uint16_t *out, int64_t ld_out,
                     uint32_t *err_flags, void *stream);
+
+/*
+ * kda_spec_verify_checkpoints — a spec-verify step that keeps the state after every
+ * draft token, so the next step can resume from whichever prefix the target model
+ * accepted. Request r owns rows [r*T, (r+1)*T) (T = tokens_per_req in 1..16) and a
+ * block-table row of at least T slots, indices[r*index_stride + c] for c < T
+ * (index_stride >= T): the mamba-group block table of 1 + num_speculative_blocks
+ * columns (vLLM PR #51682, PR body; T = k + 1). With a_r = num_accepted[r] (device
+ * int32 [num_reqs], the previous step's accepted-token count; NULL = 1 for every
+ * request; padded requests carry 1, PR #60683 "Refusal and steps", CUDA graphs):
+ *   - the initial state is read from column a_r - 1;
+ *   - the state after token t is written to column t, for every t < T;
+ *   - outputs are written for every row, as kda_spec_verify.
+ * Per column: a negative slot reads a zero state (read column) / is not written, the
+ * null slot is read but never written, a slot >= num_slots is not written and sets
+ * KDA_ERRFLAG_SLOT_RANGE. If the read column is out of range or a_r is outside
+ * [1, T], the request's outputs are zero, nothing of it is read or written, and
+ * KDA_ERRFLAG_SLOT_RANGE is set. Distinct requests must not share a written slot.
+ * indices must hold at least (num_reqs - 1)*index_stride + T entries. Writes T x
+ * the state bytes of kda_spec_verify. Can be captured in a CUDA graph.
+ */
+int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                                int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                                int64_t num_reqs, int32_t tokens_per_req,
+                                const int32_t *num_accepted, const kda_heads *heads,
+                                const kda_state *state, uint16_t *out, int64_t ld_out,
+                                uint32_t *err_flags, void *stream);
 
 /*
  * kda_chunk_prefill_workspace_bytes — device workspace kda_chunk_prefill needs for

@@ -222,6 +222,36 @@ int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
                        "kda_spec_verify launch");
 }
 
+int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                                int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                                int64_t num_reqs, int32_t tokens_per_req,
+                                const int32_t *num_accepted, const kda_heads *heads,
+                                const kda_state *state, uint16_t *out, int64_t ld_out,
+                                uint32_t *err_flags, void *stream)
+{
+    int s;
+    if ((s = check_heads(heads, false))) return s;
+    if ((s = check_rows(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, out, ld_out, heads))) return s;
+    if ((s = check_state(state, heads))) return s;
+    if (num_reqs < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "num_reqs must be >= 0");
+    if (tokens_per_req < 1 || tokens_per_req > kda::kSpecCkptMaxT)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "tokens_per_req must be in 1..%d (got %d)",
+                    kda::kSpecCkptMaxT, tokens_per_req);
+    if (state->index_stride < tokens_per_req)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "index_stride (%lld) must be >= tokens_per_req (%d): one slot per token",
+                    static_cast<long long>(state->index_stride), tokens_per_req);
+    if (num_accepted && !aligned(num_accepted, 4))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "num_accepted must be 4-byte aligned");
+    if (num_reqs == 0) return ok();
+    kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
+                                out, ld_out, err_flags);
+    return cuda_status(kda::launch_spec_checkpoints(p, heads->K, heads->V, tokens_per_req,
+                                                    num_reqs, num_accepted,
+                                                    static_cast<cudaStream_t>(stream)),
+                       "kda_spec_verify_checkpoints launch");
+}
+
 size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t num_seqs,
                                          const kda_heads *heads, int32_t chunk_size)
 {

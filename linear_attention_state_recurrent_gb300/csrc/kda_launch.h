@@ -19,6 +19,9 @@ cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, con
 
 // Spec-verify: T consecutive rows per request.
 cudaError_t launch_spec(const Params &p, int K, int V, int T, int64_t num_reqs, cudaStream_t stream);
+constexpr int kSpecCkptMaxT = 16;   // longest request the checkpointing verify kernel takes
+cudaError_t launch_spec_checkpoints(const Params &p, int K, int V, int T, int64_t num_reqs,
+                                    const int32_t *num_accepted, cudaStream_t stream);
 
 // Chunked prefill over entries entry_base .. entry_base + num_seqs - 1 (rows from cu).
 size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V,

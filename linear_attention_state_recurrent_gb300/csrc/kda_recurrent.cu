@@ -221,16 +221,23 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 // one barrier per token, the reduction buffers double-buffered across tokens.
 // Same tile split and thread layout as recurrent_kernel.
 // ---------------------------------------------------------------------------
+//
+// CKPT = true is the checkpointing variant: the request's block-table row holds one slot
+// per token; the state is read from column num_accepted[e] - 1 and the state after token
+// t is stored to column t (the stores of token t overlap the reductions of token t + 1).
+// ---------------------------------------------------------------------------
 constexpr int kSpecMaxT = 16;
+static_assert(kSpecCkptMaxT <= kSpecMaxT, "checkpointing requests run in the spec kernel");
 
-template <int K, int V>
-__global__ void __launch_bounds__(128, 7) spec_kernel(Params p, int T)
+template <int K, int V, bool CKPT>
+__global__ void __launch_bounds__(128, CKPT ? 6 : 7) spec_kernel(Params p, int T, const int32_t *num_accepted)
 {
     constexpr int VT = 32, VS = V / VT, RPT = K / 16;
     __shared__ float s_a[kSpecMaxT][K], s_k[kSpecMaxT][K], s_q[kSpecMaxT][K];
     __shared__ float s_tok[kSpecMaxT][4];          // rq, rk, q^.k^, beta
     __shared__ float s_red[2][4][2][VT];
     __shared__ float4 s_v[kSpecMaxT][VT / 4];      // this CTA's value columns of every token
+    __shared__ int64_t s_col[CKPT ? kSpecMaxT : 1]; // checkpoint slot of every token
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, cg = tid & 7, rg = tid >> 3;
     const int64_t b = blockIdx.x;
@@ -239,7 +246,16 @@ __global__ void __launch_bounds__(128, 7) spec_kernel(Params p, int T)
     const int64_t e = b / (static_cast<int64_t>(VS) * p.H);
     const int64_t row0 = e * T;
     const int j0 = vs * VT + cg * 4;
-    const int64_t slot = load_slot(p, e);
+    int64_t slot;
+    if (CKPT) {
+        const int acc = num_accepted ? __ldg(num_accepted + e) : 1;
+        slot = (acc >= 1 && acc <= T)
+                   ? static_cast<int64_t>(__ldg(p.indices + e * p.index_stride + (acc - 1)))
+                   : p.num_slots;                    // a bad count is treated as a bad slot
+        if (tid < T) s_col[tid] = static_cast<int64_t>(__ldg(p.indices + e * p.index_stride + tid));
+    } else {
+        slot = load_slot(p, e);
+    }
     if (slot >= p.num_slots) {
         if (tid == 0 && p.err) atomicOr(p.err, kErrSlotRange);
         if (rg == 0)
@@ -322,7 +338,9 @@ __global__ void __launch_bounds__(128, 7) spec_kernel(Params p, int T)
         if (tid < T) s_tok[tid][3] = sigmoid_f(bf16_to_f32(braw));
     }
     __syncthreads();
-#pragma unroll
+    // offset of this thread's first state element inside a slot (checkpoint stores)
+    const int64_t tile_off = CKPT ? static_cast<int64_t>(h) * K * V + static_cast<int64_t>(rg) * V + j0 : 0;
+#pragma unroll(CKPT ? 2 : kSpecMaxT)
     for (int t = 0; t < kSpecMaxT; t++) {
         if (t >= T) break;
         const int bb = t & 1;
@@ -373,20 +391,45 @@ __global__ void __launch_bounds__(128, 7) spec_kernel(Params p, int T)
             packed.y = static_cast<uint32_t>(f32_to_bf16(o[2])) | (static_cast<uint32_t>(f32_to_bf16(o[3])) << 16);
             *reinterpret_cast<uint2 *>(p.out + (row0 + t) * p.ld_out + static_cast<int64_t>(h) * V + j0) = packed;
         }
+        if (CKPT) {
+            const int64_t cs = s_col[t];
+            if (cs >= p.num_slots) {
+                if (tid == 0 && p.err) atomicOr(p.err, kErrSlotRange);
+            } else if (cs >= 0 && cs != p.null_slot) {
+                float *ct = p.pool + cs * p.slot_stride + tile_off;
+#pragma unroll
+                for (int i = 0; i < RPT; i++)
+                    *reinterpret_cast<float4 *>(ct + 16 * i * V) = S[i];
+            }
+        }
     }
-    if (writable) {
+    if (!CKPT && writable) {
 #pragma unroll
         for (int i = 0; i < RPT; i++)
             *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V + j0) = S[i];
     }
 }
 
-template <int K, int V>
-static cudaError_t launch_spec_kv(const Params &p, int T, int64_t num_reqs, cudaStream_t stream)
+template <int K, int V, bool CKPT>
+static cudaError_t launch_spec_kv(const Params &p, int T, int64_t num_reqs,
+                                  const int32_t *num_accepted, cudaStream_t stream)
 {
     const int64_t grid = num_reqs * p.H * (V / 32);
-    spec_kernel<K, V><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, T);
+    spec_kernel<K, V, CKPT><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, T, num_accepted);
     return cudaGetLastError();
+}
+
+template <bool CKPT>
+static cudaError_t launch_spec_dims(const Params &p, int K, int V, int T, int64_t num_reqs,
+                                    const int32_t *num_accepted, cudaStream_t stream)
+{
+#define KDA_SPEC_CASE(KK, VV) \
+    if (K == KK && V == VV) return launch_spec_kv<KK, VV, CKPT>(p, T, num_reqs, num_accepted, stream);
+    KDA_SPEC_CASE(32, 32) KDA_SPEC_CASE(32, 64) KDA_SPEC_CASE(32, 128)
+    KDA_SPEC_CASE(64, 32) KDA_SPEC_CASE(64, 64) KDA_SPEC_CASE(64, 128)
+    KDA_SPEC_CASE(128, 32) KDA_SPEC_CASE(128, 64) KDA_SPEC_CASE(128, 128)
+#undef KDA_SPEC_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_spec(const Params &p, int K, int V, int T, int64_t num_reqs, cudaStream_t stream)
@@ -394,13 +437,15 @@ cudaError_t launch_spec(const Params &p, int K, int V, int T, int64_t num_reqs, 
     if (num_reqs <= 0) return cudaSuccess;
     if (T > kSpecMaxT)  // longer requests take the token-streaming recurrent kernel
         return launch_recurrent(p, K, V, kRowsSpec, T, nullptr, 0, num_reqs, stream);
-#define KDA_SPEC_CASE(KK, VV) \
-    if (K == KK && V == VV) return launch_spec_kv<KK, VV>(p, T, num_reqs, stream);
-    KDA_SPEC_CASE(32, 32) KDA_SPEC_CASE(32, 64) KDA_SPEC_CASE(32, 128)
-    KDA_SPEC_CASE(64, 32) KDA_SPEC_CASE(64, 64) KDA_SPEC_CASE(64, 128)
-    KDA_SPEC_CASE(128, 32) KDA_SPEC_CASE(128, 64) KDA_SPEC_CASE(128, 128)
-#undef KDA_SPEC_CASE
-    return cudaErrorInvalidValue;
+    return launch_spec_dims<false>(p, K, V, T, num_reqs, nullptr, stream);
+}
+
+cudaError_t launch_spec_checkpoints(const Params &p, int K, int V, int T, int64_t num_reqs,
+                                    const int32_t *num_accepted, cudaStream_t stream)
+{
+    if (num_reqs <= 0) return cudaSuccess;
+    if (T < 1 || T > kSpecCkptMaxT) return cudaErrorInvalidValue;
+    return launch_spec_dims<true>(p, K, V, T, num_reqs, num_accepted, stream);
 }
 
 // ---------------------------------------------------------------------------

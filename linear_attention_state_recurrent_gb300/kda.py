@@ -31,8 +31,8 @@ KDA_ERR_CUDA = 4
 KDA_ERRFLAG_SLOT_RANGE = 1
 
 EXPORTED = ("kda_last_error", "kda_status_string", "kda_gate", "kda_packed_decode",
-            "kda_spec_verify", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill",
-            "kda_mixed_batch")
+            "kda_spec_verify", "kda_spec_verify_checkpoints", "kda_chunk_prefill_workspace_bytes",
+            "kda_chunk_prefill", "kda_mixed_batch")
 
 
 class KdaHeads(ctypes.Structure):
@@ -69,6 +69,9 @@ def _load():
     lib.kda_packed_decode.argtypes = [P, I64, P, I64, P, I64, I64, HP, SP, P, I64, P, P]
     lib.kda_spec_verify.restype = ctypes.c_int
     lib.kda_spec_verify.argtypes = [P, I64, P, I64, P, I64, I64, I32, HP, SP, P, I64, P, P]
+    lib.kda_spec_verify_checkpoints.restype = ctypes.c_int
+    lib.kda_spec_verify_checkpoints.argtypes = [P, I64, P, I64, P, I64, I64, I32, P, HP, SP, P, I64,
+                                                P, P]
     lib.kda_chunk_prefill_workspace_bytes.restype = SZ
     lib.kda_chunk_prefill_workspace_bytes.argtypes = [P, I64, HP, I32]
     lib.kda_chunk_prefill.restype = ctypes.c_int
@@ -205,6 +208,38 @@ def kda_spec_verify(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, ini
                                _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
            "kda_spec_verify")
     return out, initial_state
+
+
+def kda_spec_verify_checkpoints(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound,
+                                state_pool, block_table, tokens_per_req, num_accepted=None, *,
+                                scale=None, l2_eps=1e-6, null_slot=-1, out=None, err_flags=None,
+                                stream=None):
+    """Spec-verify that stores the state after every token: request r reads column
+    num_accepted[r] - 1 of block_table row r (int32 [num_reqs, >= tokens_per_req], unit
+    inner stride) and writes the state after token t to column t. Returns
+    (out, state_pool)."""
+    _, H, K, V = state_pool.shape
+    N = mixed_qkv.shape[0]
+    T = int(tokens_per_req)
+    if N % T:
+        raise ValueError("the row count must be a multiple of tokens_per_req")
+    R = N // T
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be int32 [num_reqs, width] with unit inner stride")
+    if block_table.shape[0] < R or block_table.shape[1] < T:
+        raise ValueError("block_table must have a row per request and a column per token")
+    if num_accepted is not None and (num_accepted.dtype != torch.int32 or num_accepted.numel() < R
+                                     or not num_accepted.is_contiguous()):
+        raise ValueError("num_accepted must be a contiguous int32 tensor with a count per request")
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(state_pool, block_table[:, 0], null_slot)
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    _check(lib.kda_spec_verify_checkpoints(
+        _ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g), _rows(raw_g, "raw_g"),
+        _ptr(raw_beta), _rows(raw_beta, "raw_beta"), R, T, _ptr(num_accepted),
+        ctypes.byref(hd), ctypes.byref(st), _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
+        "kda_spec_verify_checkpoints")
+    return out, state_pool
 
 
 def _host_cu(cu_seqlens, cu_seqlens_host):

@@ -87,6 +87,7 @@ class Workload:
     tokens_per_req: int = 1
     num_decodes: int = 0
     chunk_size: int = 64
+    num_accepted: np.ndarray | None = None   # int32 [num_entries], spec checkpoints only
 
     @property
     def N(self) -> int:
@@ -110,7 +111,7 @@ class Workload:
         """[start, end) rows of each addressed entry, in entry order."""
         if self.kind == "decode":
             return [(n, n + 1) for n in range(self.num_entries)]
-        if self.kind == "spec":
+        if self.kind in ("spec", "spec_ckpt"):
             T = self.tokens_per_req
             return [(r * T, (r + 1) * T) for r in range(self.num_entries)]
         cu = self.cu_seqlens
@@ -118,8 +119,12 @@ class Workload:
 
     def state_bytes_per_call(self) -> int:
         """fp32 state bytes read + written, counting each addressed (entry, head) tile
-        once each way (the unit of the decode metric)."""
-        return 2 * 4 * self.K * self.V * self.H * self.num_entries
+        once each way (the unit of the decode metric); with per-token checkpoints, one
+        read and tokens_per_req writes per tile."""
+        tile = 4 * self.K * self.V * self.H * self.num_entries
+        if self.kind == "spec_ckpt":
+            return tile * (1 + self.tokens_per_req)
+        return 2 * tile
 
 
 def _heads(rng, H, K, dt_std=0.1):
@@ -246,6 +251,37 @@ def spec_verify(seed: int = 3, num_reqs: int = 16, T: int = 8, H: int = 32, K: i
                     null_slot=0, tokens_per_req=T)
 
 
+def spec_checkpoints(seed: int = 6, num_reqs: int = 16, T: int = 8, H: int = 32, K: int = 128,
+                     V: int = 128, num_slots: int = 256, num_padding: int = 2,
+                     lower_bound=None, index_stride: int | None = None) -> Workload:
+    """Spec-verify with per-token state checkpoints: each real request owns a block-table
+    row of T distinct slots (columns beyond T, if index_stride > T, hold other slots) and
+    a number of accepted tokens in [1, T] from the previous step; padding requests point
+    every column at the null slot 0 with one accepted token."""
+    stride = T if index_stride is None else index_stride
+    assert stride >= T
+    nreal = num_reqs - num_padding
+    assert nreal * T <= num_slots - 1
+    rng = np.random.default_rng(seed)
+    N = num_reqs * T
+    mixed_qkv = _normal_bf16(rng, (N, 2 * H * K + H * V))
+    raw_g = _normal_bf16(rng, (N, H * K))
+    raw_beta = _normal_bf16(rng, (N, H))
+    A_log, dt_bias = _heads(rng, H, K)
+    buf = np.zeros((num_reqs, stride), dtype=np.int32)
+    buf[:nreal, :T] = (rng.permutation(num_slots - 1)[: nreal * T] + 1).reshape(nreal, T)
+    if stride > T:
+        buf[:, T:] = rng.integers(0, num_slots, size=(num_reqs, stride - T), dtype=np.int32)
+    acc = np.ones(num_reqs, dtype=np.int32)
+    acc[:nreal] = rng.integers(1, T + 1, size=nreal, dtype=np.int32)
+    pool = _pool(rng, num_slots, H * K * V, 0.05)
+    return Workload(name="spec_checkpoints", kind="spec_ckpt", H=H, K=K, V=V, mixed_qkv=mixed_qkv,
+                    raw_g=raw_g, raw_beta=raw_beta, A_log=A_log, dt_bias=dt_bias,
+                    lower_bound=lower_bound, scale=K ** -0.5, eps=1e-6, pool=pool,
+                    index_buf=buf, index_stride=stride, num_entries=num_reqs,
+                    null_slot=0, tokens_per_req=T, num_accepted=acc)
+
+
 def varlen_case(lengths, H: int, K: int, V: int, *, seed: int, lower_bound=None,
                 index_stride: int = 1, num_slots: int | None = None, pool_std: float = 0.05,
                 num_decodes: int = 0, scale: float | None = None, eps: float = 1e-6,
@@ -324,6 +360,8 @@ class DeviceWorkload:
         self.index_buf = torch.from_numpy(np.ascontiguousarray(w.index_buf)).to(device)
         self.cu = None if w.cu_seqlens is None else torch.from_numpy(w.cu_seqlens).to(device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.num_accepted = None if w.num_accepted is None else \
+            torch.from_numpy(np.ascontiguousarray(w.num_accepted, dtype=np.int32)).to(device)
 
     def pool_view(self):
         w = self.w
@@ -352,6 +390,10 @@ def run_gpu(dw: DeviceWorkload, kda, out=None, stream=None, workspace=None):
         o, _ = kda.kda_packed_decode(*args, **kw)
     elif w.kind == "spec":
         o, _ = kda.kda_spec_verify(*args, w.tokens_per_req, **kw)
+    elif w.kind == "spec_ckpt":
+        table = dw.index_buf.reshape(w.num_entries, w.index_stride)
+        o, _ = kda.kda_spec_verify_checkpoints(*args[:7], table, w.tokens_per_req,
+                                               dw.num_accepted, **kw)
     elif w.kind == "prefill":
         o, _ = kda.kda_chunk_prefill(*args, dw.cu, cu_seqlens_host=torch.from_numpy(w.cu_seqlens),
                                      workspace=workspace, **kw)

@@ -200,23 +200,35 @@ class CheckpointResult:
 
 
 def run_spec_checkpoints(w, nthreads: int = 0) -> CheckpointResult:
-    """Spec-verify with per-token state checkpoints (a spec-verify Workload with
-    index_stride >= tokens_per_req). Request r reads its initial state from
-    index_buf[r*stride + 0] (with the slot rules of `run`) and the state after its token t
-    is written to index_buf[r*stride + t] unless that slot is negative, the null slot or
-    out of range (the last sets bit 0 of the error word). If column 0 is out of range the
-    request's outputs are zero and nothing is read or written."""
+    """Spec-verify with per-token state checkpoints, on a spec Workload whose block-table
+    rows are at least T wide (index_stride >= tokens_per_req).
+
+    Request r with a_r = num_accepted[r] accepted tokens from the previous step (1 when
+    `w.num_accepted` is None) reads its initial state from column a_r - 1 of its row,
+    index_buf[r*stride + a_r - 1], and writes the state after its token t to column t,
+    index_buf[r*stride + t]: the block table of `1 + num_speculative_blocks` columns
+    (vLLM PR #51682, body) with the accepted-token count the padded requests carry (PR
+    #60683, section "Refusal and steps", CUDA graphs). Slot rules per column are those of
+    `run`: negative -> zero state (column a_r - 1) / no write, the null slot -> read but
+    never written, >= num_slots -> bit 0 of the error word and no write; if the read column
+    is out of range, or a_r is outside [1, T], the request's outputs are zero and nothing
+    of it is read or written (bit 0 set)."""
     lib = _load()
     H, K, V, T = w.H, w.K, w.V, w.tokens_per_req
     R = w.num_entries
     flat = np.asarray(w.index_buf).reshape(-1)
     slots = np.stack([flat[r * w.index_stride: r * w.index_stride + T] for r in range(R)]).astype(np.int64) \
         if R else np.zeros((0, T), np.int64)
+    acc = np.ones(R, dtype=np.int64) if w.num_accepted is None else np.asarray(w.num_accepted, np.int64)
     states = np.zeros((R, H, K, V), dtype=np.float64)
     valid = np.ones(R, dtype=bool)
     err = 0
     for r in range(R):
-        s0 = int(slots[r, 0])
+        if not 1 <= acc[r] <= T:
+            valid[r] = False
+            err |= ERR_SLOT_OUT_OF_RANGE
+            continue
+        s0 = int(slots[r, acc[r] - 1])
         if s0 >= w.num_slots:
             valid[r] = False
             err |= ERR_SLOT_OUT_OF_RANGE

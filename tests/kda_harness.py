@@ -78,3 +78,45 @@ def check(dw: DeviceWorkload, out: torch.Tensor, ref: ko.OracleResult, *, fp32_p
     err = int(dw.err.cpu().item())
     assert err == ref.err_flags, f"{label}: err flags {err} != {ref.err_flags}"
     return res
+
+
+def check_ckpt(dw: DeviceWorkload, out: torch.Tensor, ref: ko.CheckpointResult, label=""):
+    """Spec-verify with checkpoints: outputs within the bf16 tolerances and 1 bf16 ulp
+    (fp32 path), every written checkpoint slot within 1e-5 relative L2 of the oracle's
+    state after its token, every other slot byte-identical, the error word equal."""
+    w = dw.w
+    torch.cuda.synchronize()
+    got = bf16_to_f64(out)
+    exp = ref.out
+    assert np.all(np.isfinite(got)), f"{label}: non-finite outputs"
+    res = {"out_rel_l2": rel_l2(got, exp), "out_max_abs": float(np.abs(got - exp).max(initial=0.0))}
+    assert res["out_rel_l2"] <= REL_L2, f"{label}: output rel L2 {res['out_rel_l2']:.3e}"
+    assert res["out_max_abs"] <= MAX_ABS, f"{label}: output max abs {res['out_max_abs']:.3e}"
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exp), 1e-30))) - 7)
+    slack = 1e-5 * max(np.abs(exp).max(initial=0.0), 1e-30)
+    bad = np.abs(got - exp) > ulp + slack
+    assert not bad.any(), f"{label}: {bad.sum()} outputs more than 1 bf16 ulp off"
+    pool = dw.pool_flat.cpu().numpy()
+    HKV = w.H * w.K * w.V
+    written = {}
+    R, T = ref.slots.shape
+    for r in range(R):
+        for t in range(T):
+            if ref.writes[r, t]:
+                written[int(ref.slots[r, t])] = ref.ckpt[r, t].reshape(-1)
+    if written:
+        sl = sorted(written)
+        sg = pool[sl, :HKV].astype(np.float64).reshape(-1)
+        se = np.concatenate([written[s] for s in sl])
+        assert np.all(np.isfinite(sg)), f"{label}: non-finite checkpoints"
+        res["state_rel_l2"] = rel_l2(sg, se)
+        assert res["state_rel_l2"] <= 1e-5, f"{label}: checkpoint rel L2 {res['state_rel_l2']:.3e}"
+    untouched = np.array(sorted(set(range(w.num_slots)) - set(written)), dtype=np.int64)
+    if untouched.size:
+        assert np.array_equal(pool[untouched].view(np.uint32), w.pool[untouched].view(np.uint32)), \
+            f"{label}: a slot that is not a checkpoint changed"
+    for s in written:
+        assert np.array_equal(pool[s, HKV:].view(np.uint32), w.pool[s, HKV:].view(np.uint32))
+    err = int(dw.err.cpu().item())
+    assert err == ref.err_flags, f"{label}: err flags {err} != {ref.err_flags}"
+    return res

@@ -373,31 +373,43 @@ def test_planted_mistakes_are_caught():
 
 
 def test_spec_checkpoints_pinned_to_recurrence():
-    """Checkpoint t equals the final state of running the first t+1 tokens alone (the same
-    pinned recurrence), bit-exactly; the outputs equal plain spec-verify's."""
-    s = wl.spec_verify(num_reqs=3, T=5, H=2, K=8, V=8, num_slots=64, num_padding=1, index_stride=5)
-    # distinct checkpoint slots for the real requests
-    s.index_buf = np.array([[3, 10, 11, 12, 13], [7, 20, 21, 22, 23], [0, 0, 0, 0, 0]], np.int32)
+    """Checkpoint t equals the final state of running the first t+1 tokens alone from the
+    accepted column's state (the pinned recurrence), bit-exactly; the outputs equal plain
+    spec-verify's from the same initial state; writes go to columns 0..T-1."""
+    s = wl.spec_checkpoints(num_reqs=3, T=5, H=2, K=8, V=8, num_slots=64, num_padding=1)
+    s.num_accepted = np.array([3, 1, 1], np.int32)
     ck = ko.run_spec_checkpoints(s)
-    plain = ko.run(s)
+    init = np.array([s.index_buf[0, 2], s.index_buf[1, 0], 0])
+    plain = ko.run(s, slots=init)
     np.testing.assert_array_equal(ck.out, plain.out)
-    np.testing.assert_array_equal(ck.ckpt[:2, -1], plain.final_states[:2])
     for t in range(5):
         part = wl.Workload(**{**s.__dict__, "tokens_per_req": t + 1,
                               "mixed_qkv": s.mixed_qkv.reshape(3, 5, -1)[:, :t + 1].reshape(3 * (t + 1), -1),
                               "raw_g": s.raw_g.reshape(3, 5, -1)[:, :t + 1].reshape(3 * (t + 1), -1),
                               "raw_beta": s.raw_beta.reshape(3, 5, -1)[:, :t + 1].reshape(3 * (t + 1), -1)})
-        r = ko.run(part)
+        r = ko.run(part, slots=init)
         np.testing.assert_array_equal(ck.ckpt[:, t], r.final_states)
     assert not ck.writes[2].any()          # padding request on the null slot writes nothing
     assert ck.writes[:2].all()
+    exp = ck.expected_pool(s.pool)
+    np.testing.assert_array_equal(exp[s.index_buf[0, 4]], ck.ckpt[0, 4].reshape(-1))
+    np.testing.assert_array_equal(exp[s.index_buf[1, 0]], ck.ckpt[1, 0].reshape(-1))
 
 
 def test_spec_checkpoint_slot_rules():
-    s = wl.spec_verify(num_reqs=2, T=3, H=1, K=4, V=4, num_slots=16, num_padding=0, index_stride=4)
-    s.index_buf = np.array([[5, -1, 99, 0], [40, 1, 2, 3]], np.int32)
+    s = wl.spec_checkpoints(num_reqs=3, T=3, H=1, K=4, V=4, num_slots=16, num_padding=0,
+                            index_stride=4)
+    s.index_buf = np.array([[5, -1, 99, 0], [40, 1, 2, 3], [6, 7, 8, 9]], np.int32)
+    s.num_accepted = np.array([1, 1, 4], np.int32)
     ck = ko.run_spec_checkpoints(s)
     assert ck.err_flags == ko.ERR_SLOT_OUT_OF_RANGE
     assert list(ck.writes[0]) == [True, False, False]
-    assert not ck.writes[1].any()
-    assert np.all(ck.out[3:6] == 0)
+    assert not ck.writes[1].any() and not ck.writes[2].any()
+    assert np.all(ck.out[3:9] == 0)
+    # a negative accepted column starts from zero
+    s.index_buf = np.array([[-1, 3, 4, 0], [5, 6, 7, 0], [8, 9, 10, 0]], np.int32)
+    s.num_accepted = np.array([1, 2, 3], np.int32)
+    ck = ko.run_spec_checkpoints(s)
+    assert ck.err_flags == 0 and ck.writes[0, 0] is np.False_ and ck.writes[0, 1:].all()
+    zero = wl.Workload(**{**s.__dict__, "pool": np.zeros_like(s.pool)})
+    np.testing.assert_array_equal(ko.run_spec_checkpoints(zero).out[:3], ck.out[:3])
