@@ -88,6 +88,16 @@ class Workload:
     num_decodes: int = 0
     chunk_size: int = 64
     num_accepted: np.ndarray | None = None   # int32 [num_entries], spec checkpoints only
+    # fused layer tail (short causal conv in front, gated RMSNorm behind); `fused` routes the
+    # call through the fused entry points even when both parts are off
+    fused: bool = False
+    conv_width: int = 0
+    conv_weight: np.ndarray | None = None    # bf16 bits [2HK+HV, conv_width]
+    conv_bias: np.ndarray | None = None      # bf16 bits [2HK+HV]
+    conv_pool: np.ndarray | None = None      # bf16 bits [num_slots, conv_slot_stride]
+    out_gate: np.ndarray | None = None       # bf16 bits [N, H*V]
+    norm_weight: np.ndarray | None = None    # fp32 [V]
+    norm_eps: float = 1e-5
 
     @property
     def N(self) -> int:
@@ -169,6 +179,28 @@ def decode_case(num_seqs: int, H: int, K: int, V: int, *, seed: int, lower_bound
                     lower_bound=lower_bound,
                     scale=(K ** -0.5) if scale is None else scale, eps=eps, pool=pool,
                     index_buf=table, index_stride=index_stride, num_entries=num_seqs)
+
+
+def with_layer_tail(w: Workload, seed: int, conv_width: int | None = 4, norm: bool = True,
+                    conv_bias: bool = True, conv_slot_extra: int = 8) -> Workload:
+    """A copy of a decode or spec Workload whose mixed_qkv rows are the inputs of a
+    depthwise short causal convolution (width conv_width, None = no convolution) and whose
+    outputs go through a gated RMSNorm (norm=True). Conv weights N(0, 0.5), bias N(0, 0.1),
+    conv-state pool N(0, 1) (past inputs) with conv_slot_extra spare elements per slot,
+    output gate N(0, 1), norm weight 1 + N(0, 0.1), all bf16 except the fp32 norm weight."""
+    rng = np.random.default_rng(seed)
+    C = 2 * w.H * w.K + w.H * w.V
+    kw = dict(w.__dict__)
+    kw["fused"] = True
+    if conv_width is not None:
+        kw["conv_width"] = conv_width
+        kw["conv_weight"] = _normal_bf16(rng, (C, conv_width), 0.5)
+        kw["conv_bias"] = _normal_bf16(rng, (C,), 0.1) if conv_bias else None
+        kw["conv_pool"] = _normal_bf16(rng, (w.num_slots, (conv_width - 1) * C + conv_slot_extra))
+    if norm:
+        kw["out_gate"] = _normal_bf16(rng, (w.N, w.H * w.V))
+        kw["norm_weight"] = (1.0 + 0.1 * rng.standard_normal(w.V)).astype(np.float32)
+    return Workload(**kw)
 
 
 def _block_table(rng, rows, width, num_slots):

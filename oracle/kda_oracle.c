@@ -80,21 +80,31 @@ typedef struct {
     const float *dt_bias;
     int has_lower_bound;
     double lower_bound, scale, eps;
+    const double *qkv64;   /* if set: q/k/v rows are fp64 values here (pitch ld64), not bf16 */
+    int64_t ld64;
 } heads_t;
 
+/* Element `i` of the q|k|v row of token t: bf16 bits, or fp64 when hp->qkv64 is set. */
+static double qkv_at(const heads_t *hp, const uint16_t *mixed_qkv, int64_t ld_qkv, int64_t t,
+                     size_t i)
+{
+    if (hp->qkv64)
+        return hp->qkv64[t * hp->ld64 + (int64_t)i];
+    return bf16_to_f64(mixed_qkv[t * ld_qkv + (int64_t)i]);
+}
+
 /* Reads one token's q^, k^ (normalised, q^ scaled), v, g, beta for head h. */
-static void load_token(const heads_t *hp, const uint16_t *qkv_row, const uint16_t *g_row,
-                       const uint16_t *beta_row, int h, double *qh, double *kh, double *v,
-                       double *g, double *beta)
+static void load_token(const heads_t *hp, const uint16_t *mixed_qkv, int64_t ld_qkv, int64_t t,
+                       const uint16_t *g_row, const uint16_t *beta_row, int h, double *qh,
+                       double *kh, double *v, double *g, double *beta)
 {
     int K = hp->K, V = hp->V, H = hp->H;
-    const uint16_t *q = qkv_row + (size_t)h * K;
-    const uint16_t *k = qkv_row + (size_t)H * K + (size_t)h * K;
-    const uint16_t *vv = qkv_row + 2 * (size_t)H * K + (size_t)h * V;
+    size_t q0 = (size_t)h * K, k0 = (size_t)H * K + (size_t)h * K;
+    size_t v0 = 2 * (size_t)H * K + (size_t)h * V;
     double qn = 0.0, kn = 0.0;
     for (int c = 0; c < K; c++) {
-        qh[c] = bf16_to_f64(q[c]);
-        kh[c] = bf16_to_f64(k[c]);
+        qh[c] = qkv_at(hp, mixed_qkv, ld_qkv, t, q0 + c);
+        kh[c] = qkv_at(hp, mixed_qkv, ld_qkv, t, k0 + c);
         qn += qh[c] * qh[c];
         kn += kh[c] * kh[c];
     }
@@ -105,7 +115,7 @@ static void load_token(const heads_t *hp, const uint16_t *qkv_row, const uint16_
         kh[c] *= ks;
     }
     for (int j = 0; j < V; j++)
-        v[j] = bf16_to_f64(vv[j]);
+        v[j] = qkv_at(hp, mixed_qkv, ld_qkv, t, v0 + j);
     for (int c = 0; c < K; c++) {
         double db = hp->dt_bias ? (double)hp->dt_bias[(size_t)h * K + c] : 0.0;
         g[c] = gate_log_decay(bf16_to_f64(g_row[(size_t)h * K + c]), db,
@@ -150,7 +160,7 @@ static void recur_one(const heads_t *hp, const uint16_t *mixed_qkv, int64_t ld_q
     double *u = malloc(sizeof(double) * V);
     double beta;
     for (int64_t t = t0; t < t1; t++) {
-        load_token(hp, mixed_qkv + t * ld_qkv, raw_g + t * ld_g, raw_beta + t * ld_beta, h,
+        load_token(hp, mixed_qkv, ld_qkv, t, raw_g + t * ld_g, raw_beta + t * ld_beta, h,
                    qh, kh, v, g, &beta);
         /* S <- Diag(exp(g)) S */
         for (int c = 0; c < K; c++) {
@@ -198,7 +208,7 @@ void kda_oracle_recurrent(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint1
                           double *states, double *out, int64_t ld_out, int head_lo,
                           int head_hi, int nthreads)
 {
-    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps};
+    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps, NULL, 0};
     int64_t nh = head_hi - head_lo;
     int64_t work = num_seqs * nh;
 #ifdef _OPENMP
@@ -228,7 +238,7 @@ void kda_oracle_recurrent_ckpt(const uint16_t *mixed_qkv, int64_t ld_qkv, const 
                                double *states, double *out, int64_t ld_out, double *ckpt,
                                int64_t Tmax, int nthreads)
 {
-    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps};
+    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps, NULL, 0};
     int64_t work = num_seqs * H;
     size_t KV = (size_t)K * V;
 #ifdef _OPENMP
@@ -243,6 +253,34 @@ void kda_oracle_recurrent_ckpt(const uint16_t *mixed_qkv, int64_t ld_qkv, const 
         recur_one(&hp, mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, row_begin[s],
                   row_end[s], h, S, out, ld_out, ckpt + ((size_t)s * Tmax * H + h) * KV,
                   (int64_t)H * (int64_t)KV);
+    }
+}
+
+/*
+ * kda_oracle_recurrent with fp64 q|k|v rows (qkv64 [N][ld64]) instead of bf16 bits: the
+ * inputs of the recurrence when the short causal convolution runs in front of it.
+ */
+void kda_oracle_recurrent_f64in(const double *qkv64, int64_t ld64, const uint16_t *raw_g,
+                                int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                                const int64_t *row_begin, const int64_t *row_end,
+                                int64_t num_seqs, int H, int K, int V, const float *A_log,
+                                const float *dt_bias, int has_lower_bound, double lower_bound,
+                                double scale, double eps, double *states, double *out,
+                                int64_t ld_out, int nthreads)
+{
+    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps, qkv64, ld64};
+    int64_t work = num_seqs * H;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t w = 0; w < work; w++) {
+        int64_t s = w / H;
+        int h = (int)(w % H);
+        double *S = states + ((size_t)s * H + h) * (size_t)K * V;
+        recur_one(&hp, NULL, 0, raw_g, ld_g, raw_beta, ld_beta, row_begin[s], row_end[s], h, S,
+                  out, ld_out, NULL, 0);
     }
 }
 
@@ -276,7 +314,7 @@ static void chunk_one(const heads_t *hp, const uint16_t *mixed_qkv, int64_t ld_q
     for (int64_t c0 = t0; c0 < t1; c0 += C) {
         int n = (int)((t1 - c0) < C ? (t1 - c0) : C);
         for (int r = 0; r < n; r++)
-            load_token(hp, mixed_qkv + (c0 + r) * ld_qkv, raw_g + (c0 + r) * ld_g,
+            load_token(hp, mixed_qkv, ld_qkv, c0 + r, raw_g + (c0 + r) * ld_g,
                        raw_beta + (c0 + r) * ld_beta, h, Q + (size_t)r * K, Kh + (size_t)r * K,
                        Vv + (size_t)r * V, G + (size_t)r * K, &beta[r]);
         /* b_r = sum_{i<=r} g_i (in-chunk cumulative log-decay) */
@@ -370,7 +408,7 @@ void kda_oracle_chunked(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
                         int has_lower_bound, double lower_bound, double scale, double eps,
                         int C, double *states, double *out, int64_t ld_out, int nthreads)
 {
-    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps};
+    heads_t hp = {H, K, V, A_log, dt_bias, has_lower_bound, lower_bound, scale, eps, NULL, 0};
     int64_t work = num_seqs * H;
 #ifdef _OPENMP
     if (nthreads > 0)
