@@ -24,8 +24,9 @@
  *  - Every tensor pointer is a DEVICE pointer owned by the caller. The library
  *    allocates nothing, keeps no state between calls, never synchronises the
  *    stream, and enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy
- *    default stream). kda_packed_decode, kda_spec_verify and
- *    kda_spec_verify_checkpoints can be captured in a CUDA graph.
+ *    default stream). kda_packed_decode, kda_spec_verify,
+ *    kda_spec_verify_checkpoints, kda_fused_decode and kda_fused_spec_verify can be
+ *    captured in a CUDA graph.
  *  - bf16 values are passed as uint16_t bit patterns.
  *  - mixed_qkv: bf16 [N, ld_qkv]; row t = [ q (H*K) | k (H*K) | v (H*V) ], each
  *    part head-major ([H][K] or [H][V]). raw_g: bf16 [N, ld_g], H*K used.
@@ -97,6 +98,41 @@ typedef struct kda_state {
     int32_t null_slot;      /* slot that is read but never written; -1 = none */
 } kda_state;
 
+/*
+ * The two steps around the recurrence in the Kimi-K3 decode layer ("spec conv, KDA
+ * recurrence, gated RMSNorm", vLLM PR #60683, section Purpose, whole-layer list), fused
+ * into kda_fused_decode / kda_fused_spec_verify. The pages name the steps only; the
+ * definitions below are this library's readings.
+ *
+ * Short causal convolution, depthwise over the C = 2*H*K + H*V channels of the q|k|v row
+ * (mixed_qkv then holds the convolution's INPUTS), width W in 1..4:
+ *   y_t[ch] = sum_{w<W} weight[ch*W + w] * hist[t + w][ch] + bias[ch],   x'_t = y_t * sigmoid(y_t)
+ * where hist = [the W-1 stored previous inputs of the slot, oldest first; the call's rows].
+ * After the call the slot's conv state holds the last W-1 rows of hist (bit-exact bf16).
+ * The conv state shares the KDA state's slot index and slot rules (negative: zero history,
+ * not written; null slot: read, not written; out of range: untouched).
+ */
+typedef struct kda_short_conv {
+    const uint16_t *weight;   /* device bf16 [C][W] */
+    const uint16_t *bias;     /* device bf16 [C], or NULL */
+    uint16_t *state;          /* device bf16 conv-state pool of num_slots slots (the kda_state's):
+                                 slot s at state + s*slot_stride, [W-1][C] row-major (oldest
+                                 input first), updated in place; may be NULL when W == 1 */
+    int64_t slot_stride;      /* bf16 elements between slots, >= (W-1)*C */
+    int32_t width;            /* W, 1..4 */
+} kda_short_conv;
+
+/*
+ * Gated RMSNorm of each (token, head)'s V outputs:
+ *   o'_j = o_j / sqrt(mean_j o_j^2 + eps) * weight[j] * sigmoid(gate[t*ld_gate + h*V + j])
+ */
+typedef struct kda_gated_norm {
+    const uint16_t *gate;     /* device bf16 [N, ld_gate], H*V used; 4-byte aligned */
+    int64_t ld_gate;          /* >= H*V, even */
+    const float *weight;      /* device fp32 [V] */
+    float eps;                /* >= 0 */
+} kda_gated_norm;
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char *kda_last_error(void);
 
@@ -164,6 +200,32 @@ int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const
                                 const int32_t *num_accepted, const kda_heads *heads,
                                 const kda_state *state, uint16_t *out, int64_t ld_out,
                                 uint32_t *err_flags, void *stream);
+
+/*
+ * kda_fused_decode — kda_packed_decode with the short convolution in front and the gated
+ * RMSNorm behind, in one kernel (one CTA per (sequence, head)). conv == NULL skips the
+ * convolution (mixed_qkv are then the recurrence's inputs, as in kda_packed_decode);
+ * norm == NULL skips the norm. Outputs, KDA state and error word follow kda_packed_decode.
+ * Can be captured in a CUDA graph.
+ */
+int kda_fused_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                     int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta, int64_t num_seqs,
+                     const kda_heads *heads, const kda_state *state, const kda_short_conv *conv,
+                     const kda_gated_norm *norm, uint16_t *out, int64_t ld_out,
+                     uint32_t *err_flags, void *stream);
+
+/*
+ * kda_fused_spec_verify — kda_spec_verify (T = tokens_per_req in 1..16 rows per request,
+ * state read once and written once) with the convolution over the request's T rows in
+ * front (its conv state advances by T inputs) and the gated RMSNorm behind. NULL conv /
+ * norm skip those steps. Can be captured in a CUDA graph.
+ */
+int kda_fused_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                          int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                          int64_t num_reqs, int32_t tokens_per_req, const kda_heads *heads,
+                          const kda_state *state, const kda_short_conv *conv,
+                          const kda_gated_norm *norm, uint16_t *out, int64_t ld_out,
+                          uint32_t *err_flags, void *stream);
 
 /*
  * kda_chunk_prefill_workspace_bytes — device workspace kda_chunk_prefill needs for

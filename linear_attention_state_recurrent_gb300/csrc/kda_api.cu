@@ -138,6 +138,41 @@ kda::Params make_params(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
     return p;
 }
 
+// Fills the fused-tail parameters; validates the optional conv / norm arguments.
+int make_tail(const kda_short_conv *cv, const kda_gated_norm *nm, const kda_heads *hd,
+              kda::TailParams *tp)
+{
+    *tp = kda::TailParams{};
+    const int64_t C = 2 * static_cast<int64_t>(hd->H) * hd->K + static_cast<int64_t>(hd->H) * hd->V;
+    if (cv) {
+        if (cv->width < 1 || cv->width > 4)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "conv width must be in 1..4 (got %d)", cv->width);
+        if (!cv->weight || (cv->width > 1 && !cv->state))
+            return fail(KDA_ERR_INVALID_ARGUMENT, "conv weight and conv state must be non-NULL");
+        if (cv->width > 1 && cv->slot_stride < (cv->width - 1) * C)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "conv slot_stride (%lld) < (W-1)*C (%lld)",
+                        (long long)cv->slot_stride, (long long)((cv->width - 1) * C));
+        if (!aligned(cv->weight, 2) || !aligned(cv->bias, 2) || !aligned(cv->state, 2))
+            return fail(KDA_ERR_INVALID_ARGUMENT, "conv tensors must be 2-byte aligned");
+        tp->conv_w = cv->weight; tp->conv_b = cv->bias;
+        tp->conv_state = cv->state; tp->conv_slot_stride = cv->slot_stride;
+        tp->conv_width = cv->width;
+    }
+    if (nm) {
+        if (!nm->gate || !nm->weight)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "norm gate and weight must be non-NULL");
+        if (nm->ld_gate < static_cast<int64_t>(hd->H) * hd->V || (nm->ld_gate % 2) != 0 ||
+            !aligned(nm->gate, 4))
+            return fail(KDA_ERR_INVALID_ARGUMENT,
+                        "norm gate must be 4-byte aligned with an even ld_gate >= H*V");
+        if (!(nm->eps >= 0.f) || !std::isfinite(nm->eps))
+            return fail(KDA_ERR_INVALID_ARGUMENT, "norm eps must be finite and >= 0");
+        tp->gate = nm->gate; tp->ld_gate = nm->ld_gate;
+        tp->norm_w = nm->weight; tp->norm_eps = nm->eps;
+    }
+    return KDA_OK;
+}
+
 int check_cu_host(const int32_t *cu_host, int64_t n)
 {
     if (!cu_host) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens_host is NULL");
@@ -250,6 +285,51 @@ int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const
                                                     num_reqs, num_accepted,
                                                     static_cast<cudaStream_t>(stream)),
                        "kda_spec_verify_checkpoints launch");
+}
+
+static int fused_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                        int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                        int64_t num_entries, int32_t T, const kda_heads *heads,
+                        const kda_state *state, const kda_short_conv *conv,
+                        const kda_gated_norm *norm, uint16_t *out, int64_t ld_out,
+                        uint32_t *err_flags, void *stream, const char *name)
+{
+    int s;
+    if ((s = check_heads(heads, false))) return s;
+    if ((s = check_rows(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, out, ld_out, heads))) return s;
+    if ((s = check_state(state, heads))) return s;
+    if (num_entries < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "the entry count must be >= 0");
+    if (T < 1 || T > 16)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "tokens_per_req must be in 1..16 (got %d)", T);
+    kda::TailParams tp;
+    if ((s = make_tail(conv, norm, heads, &tp))) return s;
+    if (num_entries == 0) return ok();
+    kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
+                                out, ld_out, err_flags);
+    return cuda_status(kda::launch_fused(p, tp, heads->K, heads->V, T, num_entries,
+                                         static_cast<cudaStream_t>(stream)), name);
+}
+
+int kda_fused_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                     int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta, int64_t num_seqs,
+                     const kda_heads *heads, const kda_state *state, const kda_short_conv *conv,
+                     const kda_gated_norm *norm, uint16_t *out, int64_t ld_out,
+                     uint32_t *err_flags, void *stream)
+{
+    return fused_common(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, num_seqs, 1, heads,
+                        state, conv, norm, out, ld_out, err_flags, stream, "kda_fused_decode launch");
+}
+
+int kda_fused_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                          int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                          int64_t num_reqs, int32_t tokens_per_req, const kda_heads *heads,
+                          const kda_state *state, const kda_short_conv *conv,
+                          const kda_gated_norm *norm, uint16_t *out, int64_t ld_out,
+                          uint32_t *err_flags, void *stream)
+{
+    return fused_common(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, num_reqs,
+                        tokens_per_req, heads, state, conv, norm, out, ld_out, err_flags, stream,
+                        "kda_fused_spec_verify launch");
 }
 
 size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t num_seqs,

@@ -21,6 +21,15 @@ struct Params {
     int H;
 };
 
+// The steps around the recurrence in the fused decode / spec-verify calls. conv_width 0 =
+// no convolution; gate == nullptr = no gated RMSNorm.
+struct TailParams {
+    const uint16_t *conv_w;   const uint16_t *conv_b;
+    uint16_t *conv_state;     int64_t conv_slot_stride;  int conv_width;
+    const uint16_t *gate;     int64_t ld_gate;
+    const float *norm_w;      float norm_eps;
+};
+
 constexpr uint32_t kErrSlotRange = 1u;
 constexpr uint32_t kErrTimeout = 2u;   // a bounded wait on the tensor cores gave up
 

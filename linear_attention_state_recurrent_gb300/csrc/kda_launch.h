@@ -23,6 +23,10 @@ constexpr int kSpecCkptMaxT = 16;   // longest request the checkpointing verify 
 cudaError_t launch_spec_checkpoints(const Params &p, int K, int V, int T, int64_t num_reqs,
                                     const int32_t *num_accepted, cudaStream_t stream);
 
+// Fused layer tail (conv -> recurrence -> gated norm): T (1..16) consecutive rows per entry.
+cudaError_t launch_fused(const Params &p, const TailParams &tp, int K, int V, int T,
+                         int64_t num_entries, cudaStream_t stream);
+
 // Chunked prefill over entries entry_base .. entry_base + num_seqs - 1 (rows from cu).
 size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V,
                              int chunk_size);

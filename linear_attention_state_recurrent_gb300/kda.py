@@ -31,8 +31,9 @@ KDA_ERR_CUDA = 4
 KDA_ERRFLAG_SLOT_RANGE = 1
 
 EXPORTED = ("kda_last_error", "kda_status_string", "kda_gate", "kda_packed_decode",
-            "kda_spec_verify", "kda_spec_verify_checkpoints", "kda_chunk_prefill_workspace_bytes",
-            "kda_chunk_prefill", "kda_mixed_batch")
+            "kda_spec_verify", "kda_spec_verify_checkpoints", "kda_fused_decode",
+            "kda_fused_spec_verify", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill",
+            "kda_mixed_batch")
 
 
 class KdaHeads(ctypes.Structure):
@@ -46,6 +47,16 @@ class KdaState(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
                 ("slot_stride", ctypes.c_int64), ("indices", ctypes.c_void_p),
                 ("index_stride", ctypes.c_int64), ("null_slot", ctypes.c_int32)]
+
+
+class KdaShortConv(ctypes.Structure):
+    _fields_ = [("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("state", ctypes.c_void_p),
+                ("slot_stride", ctypes.c_int64), ("width", ctypes.c_int32)]
+
+
+class KdaGatedNorm(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("ld_gate", ctypes.c_int64), ("weight", ctypes.c_void_p),
+                ("eps", ctypes.c_float)]
 
 
 class KdaError(RuntimeError):
@@ -72,6 +83,12 @@ def _load():
     lib.kda_spec_verify_checkpoints.restype = ctypes.c_int
     lib.kda_spec_verify_checkpoints.argtypes = [P, I64, P, I64, P, I64, I64, I32, P, HP, SP, P, I64,
                                                 P, P]
+    CP, NP = ctypes.POINTER(KdaShortConv), ctypes.POINTER(KdaGatedNorm)
+    lib.kda_fused_decode.restype = ctypes.c_int
+    lib.kda_fused_decode.argtypes = [P, I64, P, I64, P, I64, I64, HP, SP, CP, NP, P, I64, P, P]
+    lib.kda_fused_spec_verify.restype = ctypes.c_int
+    lib.kda_fused_spec_verify.argtypes = [P, I64, P, I64, P, I64, I64, I32, HP, SP, CP, NP, P, I64,
+                                          P, P]
     lib.kda_chunk_prefill_workspace_bytes.restype = SZ
     lib.kda_chunk_prefill_workspace_bytes.argtypes = [P, I64, HP, I32]
     lib.kda_chunk_prefill.restype = ctypes.c_int
@@ -240,6 +257,77 @@ def kda_spec_verify_checkpoints(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lowe
         ctypes.byref(hd), ctypes.byref(st), _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
         "kda_spec_verify_checkpoints")
     return out, state_pool
+
+
+def make_conv(weight, bias, conv_state):
+    """kda_short_conv from weight bf16 [C, W], bias bf16 [C] or None, and the conv-state
+    pool bf16 [num_slots, >= (W-1)*C] (unit inner stride)."""
+    if weight.dtype != torch.bfloat16 or weight.dim() != 2 or not weight.is_contiguous():
+        raise ValueError("conv weight must be a contiguous bf16 [C, W] tensor")
+    if bias is not None and (bias.dtype != torch.bfloat16 or not bias.is_contiguous()):
+        raise ValueError("conv bias must be a contiguous bf16 tensor")
+    if conv_state.dtype != torch.bfloat16 or conv_state.dim() != 2 or conv_state.stride(1) != 1:
+        raise ValueError("conv_state must be bf16 [num_slots, slot] with unit inner stride")
+    return KdaShortConv(weight=weight.data_ptr(), bias=None if bias is None else bias.data_ptr(),
+                        state=conv_state.data_ptr(), slot_stride=conv_state.stride(0),
+                        width=weight.shape[1])
+
+
+def make_norm(gate, weight, eps=1e-5):
+    """kda_gated_norm from gate bf16 [N, >= H*V] and weight fp32 [V]."""
+    if weight.dtype != torch.float32 or not weight.is_contiguous():
+        raise ValueError("norm weight must be a contiguous fp32 tensor")
+    return KdaGatedNorm(gate=gate.data_ptr(), ld_gate=_rows(gate, "gate"), weight=weight.data_ptr(),
+                        eps=float(eps))
+
+
+def _fused(name, mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+           state_indices, T, conv, norm, scale, l2_eps, null_slot, out, err_flags, stream):
+    _, H, K, V = initial_state.shape
+    N = mixed_qkv.shape[0]
+    if N % T:
+        raise ValueError("the row count must be a multiple of tokens_per_req")
+    E = N // T
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(initial_state, state_indices, null_slot)
+    if state_indices.shape[0] < E:
+        raise ValueError("state_indices has fewer entries than requests")
+    if conv is not None and conv[2].shape[0] < initial_state.shape[0]:
+        raise ValueError("conv_state must have a slot for every state slot")
+    cv = None if conv is None else make_conv(*conv)
+    nm = None if norm is None else make_norm(*norm)
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    head = (_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g), _rows(raw_g, "raw_g"),
+            _ptr(raw_beta), _rows(raw_beta, "raw_beta"), E)
+    tail = (ctypes.byref(hd), ctypes.byref(st), None if cv is None else ctypes.byref(cv),
+            None if nm is None else ctypes.byref(nm), _ptr(out), ld_out, _ptr(err_flags),
+            _stream(stream))
+    if name == "kda_fused_decode":
+        _check(lib.kda_fused_decode(*head, *tail), name)
+    else:
+        _check(lib.kda_fused_spec_verify(*head, int(T), *tail), name)
+    return out, initial_state
+
+
+def kda_fused_decode(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+                     state_indices, *, conv=None, norm=None, scale=None, l2_eps=1e-6,
+                     null_slot=-1, out=None, err_flags=None, stream=None):
+    """Packed decode with the short conv in front (conv = (weight, bias, conv_state) or None;
+    mixed_qkv then holds the conv inputs) and the gated RMSNorm behind (norm = (gate,
+    weight, eps) or None). Returns (out, initial_state)."""
+    return _fused("kda_fused_decode", mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound,
+                  initial_state, state_indices, 1, conv, norm, scale, l2_eps, null_slot, out,
+                  err_flags, stream)
+
+
+def kda_fused_spec_verify(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initial_state,
+                          state_indices, tokens_per_req, *, conv=None, norm=None, scale=None,
+                          l2_eps=1e-6, null_slot=-1, out=None, err_flags=None, stream=None):
+    """Spec-verify of tokens_per_req rows per request with the conv / gated norm of
+    kda_fused_decode. Returns (out, initial_state)."""
+    return _fused("kda_fused_spec_verify", mixed_qkv, raw_g, raw_beta, A_log, dt_bias,
+                  lower_bound, initial_state, state_indices, int(tokens_per_req), conv, norm,
+                  scale, l2_eps, null_slot, out, err_flags, stream)
 
 
 def _host_cu(cu_seqlens, cu_seqlens_host):

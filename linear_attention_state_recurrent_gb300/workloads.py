@@ -392,6 +392,11 @@ class DeviceWorkload:
         self.index_buf = torch.from_numpy(np.ascontiguousarray(w.index_buf)).to(device)
         self.cu = None if w.cu_seqlens is None else torch.from_numpy(w.cu_seqlens).to(device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.conv_weight = None if w.conv_weight is None else bf16_tensor(w.conv_weight, device)
+        self.conv_bias = None if w.conv_bias is None else bf16_tensor(w.conv_bias, device)
+        self.conv_pool = None if w.conv_pool is None else bf16_tensor(w.conv_pool, device)
+        self.out_gate = None if w.out_gate is None else bf16_tensor(w.out_gate, device)
+        self.norm_weight = None if w.norm_weight is None else torch.from_numpy(w.norm_weight).to(device)
         self.num_accepted = None if w.num_accepted is None else \
             torch.from_numpy(np.ascontiguousarray(w.num_accepted, dtype=np.int32)).to(device)
 
@@ -407,6 +412,8 @@ class DeviceWorkload:
     def reset_pool(self):
         import torch
         self.pool_flat.copy_(torch.from_numpy(self.w.pool).to(self.device))
+        if self.conv_pool is not None:
+            self.conv_pool.copy_(bf16_tensor(self.w.conv_pool, self.device))
         self.err.zero_()
 
 
@@ -418,7 +425,14 @@ def run_gpu(dw: DeviceWorkload, kda, out=None, stream=None, workspace=None):
             dw.pool_view(), dw.indices_view())
     kw = dict(scale=w.scale, l2_eps=w.eps, null_slot=w.null_slot, err_flags=dw.err, out=out,
               stream=stream)
-    if w.kind == "decode":
+    if w.fused:
+        conv = None if w.conv_weight is None else (dw.conv_weight, dw.conv_bias, dw.conv_pool)
+        norm = None if w.norm_weight is None else (dw.out_gate, dw.norm_weight, w.norm_eps)
+        if w.kind == "decode":
+            o, _ = kda.kda_fused_decode(*args, conv=conv, norm=norm, **kw)
+        else:
+            o, _ = kda.kda_fused_spec_verify(*args, w.tokens_per_req, conv=conv, norm=norm, **kw)
+    elif w.kind == "decode":
         o, _ = kda.kda_packed_decode(*args, **kw)
     elif w.kind == "spec":
         o, _ = kda.kda_spec_verify(*args, w.tokens_per_req, **kw)
