@@ -245,7 +245,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--workload", choices=["decode", "prefill", "spec", "spec_ckpt", "mixed"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "spec", "spec_ckpt", "fused_decode", "fused_spec", "mixed"], default="decode",
                     help="decode (default) is the headline line; the others time one row alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -391,12 +391,18 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
     elif args.workload == "spec_ckpt":
         w = wl.spec_checkpoints()
         metric, unit = "spec-verify-checkpoints state-bytes GB/s", "GB/s"
+    elif args.workload == "fused_decode":
+        w = wl.with_layer_tail(wl.serving_decode(-5.0), seed=99)
+        metric, unit = "fused-decode state-bytes GB/s", "GB/s"
+    elif args.workload == "fused_spec":
+        w = wl.with_layer_tail(wl.spec_verify(), seed=99)
+        metric, unit = "fused-spec-verify state-bytes GB/s", "GB/s"
     else:
         w = wl.spec_verify()
         metric, unit = "spec-verify state-bytes GB/s", "GB/s"
     dw = wl.DeviceWorkload(w, dev)
     out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
-    if args.workload in ("spec", "spec_ckpt"):
+    if args.workload in ("spec", "spec_ckpt", "fused_decode", "fused_spec"):
         ms = time_spec_graph(torch, kda, w, dw, out, calls=20, replays=max(1, args.steps // 20))
         value = spec_state_bytes(w) * world / (ms * 1e-3) / 1e9
         line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -440,9 +446,9 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
 
 
 def spec_call_args(kda, w, dw, out, stream_handle):
-    """Pre-marshalled C-ABI arguments of one kda_spec_verify (or, for a checkpoint
-    workload, kda_spec_verify_checkpoints) call, kept alive with the structs they point
-    to. Returns (function, args, keep-alive)."""
+    """Pre-marshalled C-ABI arguments of one kda_spec_verify call (kda_spec_verify_checkpoints
+    for a checkpoint workload, kda_fused_decode / kda_fused_spec_verify for a fused one),
+    kept alive with the structs they point to. Returns (function, args, keep-alive)."""
     hd = kda.make_heads(dw.A_log, dw.dt_bias, w.lower_bound, w.K, w.V, w.scale, w.eps)
     st = kda.make_state(dw.pool_view(), dw.indices_view(), w.null_slot)
     head = (ctypes.c_void_p(dw.mixed_qkv.data_ptr()), dw.mixed_qkv.stride(0),
@@ -451,6 +457,14 @@ def spec_call_args(kda, w, dw, out, stream_handle):
             w.num_entries, w.tokens_per_req)
     tail = (ctypes.byref(hd), ctypes.byref(st), ctypes.c_void_p(out.data_ptr()), out.stride(0),
             None, ctypes.c_void_p(stream_handle))
+    if w.fused:
+        cv = None if w.conv_weight is None else kda.make_conv(dw.conv_weight, dw.conv_bias, dw.conv_pool)
+        nm = None if w.norm_weight is None else kda.make_norm(dw.out_gate, dw.norm_weight, w.norm_eps)
+        ext = (None if cv is None else ctypes.byref(cv), None if nm is None else ctypes.byref(nm))
+        tail = tail[:2] + ext + tail[2:]
+        if w.kind == "decode":
+            return kda.lib.kda_fused_decode, head[:7] + tail, (hd, st, cv, nm)
+        return kda.lib.kda_fused_spec_verify, head + tail, (hd, st, cv, nm)
     if w.kind == "spec_ckpt":
         acc = None if dw.num_accepted is None else ctypes.c_void_p(dw.num_accepted.data_ptr())
         return kda.lib.kda_spec_verify_checkpoints, head + (acc,) + tail, (hd, st)
@@ -492,7 +506,11 @@ def spec_state_bytes(w):
     null = sum(1 for s in w.indices() if s == w.null_slot)
     real = w.num_entries - null
     writes = w.tokens_per_req if w.kind == "spec_ckpt" else 1
-    return (real * (1 + writes) + null) * 4 * w.K * w.V * w.H
+    total = (real * (1 + writes) + null) * 4 * w.K * w.V * w.H
+    if w.conv_weight is not None:   # the conv state: W-1 bf16 inputs per channel, read + written
+        C = 2 * w.H * w.K + w.H * w.V
+        total += (real * 2 + null) * (w.conv_width - 1) * C * 2
+    return total
 
 
 def time_calls(torch, fn, stream, n, warmup=2):
@@ -533,6 +551,23 @@ def measure_secondary(torch, kda, wl, dev, stream, pk):
         "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
         "timing": "CUDA graph of 20 calls, 50 replays"}
     del dw
+    # fused layer tail (conv W=4 -> recurrence -> gated RMSNorm): serving decode, spec 16x8
+    for key, base, desc in (
+            ("fused_decode", wl.serving_decode(-5.0),
+             "128 seqs, H=32, K=V=128, conv width 4, gated RMSNorm, index stride 8"),
+            ("fused_spec_verify", wl.spec_verify(),
+             "16 requests x 8 tokens, H=32, K=V=128, conv width 4, gated RMSNorm, 2 padding")):
+        w = wl.with_layer_tail(base, seed=99)
+        dw = wl.DeviceWorkload(w, dev)
+        fo = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+        ms = time_spec_graph(torch, kda, w, dw, fo)
+        sbytes = spec_state_bytes(w)
+        res[key] = {"workload": desc, "us_per_call": ms * 1e3,
+                    "state_gbs": sbytes / (ms * 1e-3) / 1e9,
+                    "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                    "bytes": "KDA state and conv state, read + written (null slot read only)",
+                    "timing": "CUDA graph of 20 calls, 50 replays"}
+        del dw, fo
     # chunked prefill: seed-1 lengths, 33,494 tokens
     w = wl.chunked_prefill(None)
     dw = wl.DeviceWorkload(w, dev)

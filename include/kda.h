@@ -113,12 +113,12 @@ typedef struct kda_state {
  * not written; null slot: read, not written; out of range: untouched).
  */
 typedef struct kda_short_conv {
-    const uint16_t *weight;   /* device bf16 [C][W] */
-    const uint16_t *bias;     /* device bf16 [C], or NULL */
+    const uint16_t *weight;   /* device bf16 [C][W]; 8-byte aligned */
+    const uint16_t *bias;     /* device bf16 [C], or NULL; 8-byte aligned */
     uint16_t *state;          /* device bf16 conv-state pool of num_slots slots (the kda_state's):
                                  slot s at state + s*slot_stride, [W-1][C] row-major (oldest
                                  input first), updated in place; may be NULL when W == 1 */
-    int64_t slot_stride;      /* bf16 elements between slots, >= (W-1)*C */
+    int64_t slot_stride;      /* bf16 elements between slots, >= (W-1)*C, multiple of 4 */
     int32_t width;            /* W, 1..4 */
 } kda_short_conv;
 
@@ -206,6 +206,10 @@ int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const
  * RMSNorm behind, in one kernel (one CTA per (sequence, head)). conv == NULL skips the
  * convolution (mixed_qkv are then the recurrence's inputs, as in kda_packed_decode);
  * norm == NULL skips the norm. Outputs, KDA state and error word follow kda_packed_decode.
+ * Layout requirements beyond kda_packed_decode's (the kernel moves 4 channels per load):
+ * mixed_qkv and raw_g 8-byte aligned with ld_qkv and ld_g multiples of 4, dt_bias 16-byte
+ * aligned, conv weight, bias and state 8-byte aligned with a conv slot_stride multiple of 4.
+ * The V / 32 column slices of one (sequence, head) run as one thread-block cluster.
  * Can be captured in a CUDA graph.
  */
 int kda_fused_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,

@@ -152,8 +152,11 @@ int make_tail(const kda_short_conv *cv, const kda_gated_norm *nm, const kda_head
         if (cv->width > 1 && cv->slot_stride < (cv->width - 1) * C)
             return fail(KDA_ERR_INVALID_ARGUMENT, "conv slot_stride (%lld) < (W-1)*C (%lld)",
                         (long long)cv->slot_stride, (long long)((cv->width - 1) * C));
-        if (!aligned(cv->weight, 2) || !aligned(cv->bias, 2) || !aligned(cv->state, 2))
-            return fail(KDA_ERR_INVALID_ARGUMENT, "conv tensors must be 2-byte aligned");
+        if (!aligned(cv->weight, 8) || !aligned(cv->bias, 8) || !aligned(cv->state, 8) ||
+            (cv->width > 1 && cv->slot_stride % 4 != 0))
+            return fail(KDA_ERR_INVALID_ARGUMENT,
+                        "conv weight, bias and state must be 8-byte aligned, "
+                        "and the conv slot_stride a multiple of 4");
         tp->conv_w = cv->weight; tp->conv_b = cv->bias;
         tp->conv_state = cv->state; tp->conv_slot_stride = cv->slot_stride;
         tp->conv_width = cv->width;
@@ -301,6 +304,11 @@ static int fused_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
     if (num_entries < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "the entry count must be >= 0");
     if (T < 1 || T > 16)
         return fail(KDA_ERR_INVALID_ARGUMENT, "tokens_per_req must be in 1..16 (got %d)", T);
+    if (!aligned(mixed_qkv, 8) || !aligned(raw_g, 8) || ld_qkv % 4 != 0 || ld_g % 4 != 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "mixed_qkv and raw_g must be 8-byte aligned with ld_qkv and ld_g multiples of 4");
+    if (!aligned(heads->dt_bias, 16))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "dt_bias must be 16-byte aligned");
     kda::TailParams tp;
     if ((s = make_tail(conv, norm, heads, &tp))) return s;
     if (num_entries == 0) return ok();

@@ -332,13 +332,6 @@ __device__ __forceinline__ bool wait_mma(uint32_t mbar, uint32_t parity, int war
 // byte offset of 16-byte chunk `ch` (0..15) of row r in a staged [64][128] bf16 tile
 __device__ __forceinline__ uint32_t st_off(int r, int ch) { return static_cast<uint32_t>(r * 256 + ((ch ^ (r & 7)) << 4)); }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // Copies rows [c0, c0 + 64) of one 128-wide bf16 column block (base + row*ld) into a
 // staged tile; rows at or past `nrows` are zero-filled (their source is not read).
 __device__ __forceinline__ void stage_rows(uint32_t tile, const uint16_t *base, int64_t ld, int nrows, int tid)

@@ -48,6 +48,15 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f)
     return static_cast<uint16_t>(u >> 16);
 }
 
+// Two fp32 values to packed bf16 (lo in the low half), round to nearest even, one
+// hardware conversion.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 __device__ __forceinline__ float softplus_f(float x)
 {
     return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
@@ -82,6 +91,15 @@ __device__ __forceinline__ float warp_sum(float v)
         v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+
+// 16-byte asynchronous global -> shared copy (L2 only); `valid` false zero-fills the
+// destination without reading the source.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Slot of entry e: indices[e * index_stride] widened to 64 bits.
 __device__ __forceinline__ int64_t load_slot(const Params &p, int64_t e)
