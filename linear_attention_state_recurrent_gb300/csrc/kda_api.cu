@@ -389,18 +389,9 @@ static int chunk_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (num_decodes > 0) {
-        cudaError_t e = kda::launch_recurrent(p, heads->K, heads->V, 2, 1, cu_seqlens, 0,
-                                              num_decodes, st);
-        if (e != cudaSuccess) return cuda_status(e, "decode launch");
-    }
-    if (num_prefills > 0) {
-        cudaError_t e = kda::launch_chunk_prefill(p, heads->K, heads->V, cu_seqlens,
-                                                  cu_seqlens_host, num_decodes, num_prefills,
-                                                  chunk_size, workspace, workspace_bytes, st);
-        if (e != cudaSuccess) return cuda_status(e, "chunk prefill launch");
-    }
-    return ok();
+    return cuda_status(kda::launch_mixed(p, heads->K, heads->V, cu_seqlens, cu_seqlens_host,
+                                         num_decodes, num_prefills, st),
+                       "mixed batch launch");
 }
 
 int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,

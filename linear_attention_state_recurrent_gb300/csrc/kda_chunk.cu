@@ -116,6 +116,8 @@ struct Args {
     const int32_t *cu;
     int64_t entry_base;
     int32_t num_seqs;
+    int32_t n_chunk;       // CTAs [0, n_chunk) run prefill chains; the rest are decode workers
+    int32_t num_decodes;   // mixed batch: entries [0, num_decodes) are length-1 decodes
     int32_t order_n;
     int32_t order[kMaxOrder];
 };
@@ -372,9 +374,173 @@ __device__ __forceinline__ void load_row_inputs(uint32_t sbase, int r, int cb, R
 // ---------------------------------------------------------------------------
 // The kernel (512 threads, one (sequence, head) chain per CTA)
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// Decode workers of a mixed batch: the CTAs after the prefill chains. Each of the four
+// 128-thread groups of such a CTA walks (decode, head, 32-column slice) tiles with a grid
+// stride and runs the decode step of the recurrent kernel on each (same thread layout:
+// thread (rg, cg) holds rows rg, rg + 16, ... of columns 4cg .. 4cg + 3), with group-local
+// named barriers; the next tile's state streams into shared memory (cp.async) and its
+// inputs into registers while the current one is computed. They run on the SMs the chains leave free (the chain CTAs come
+// first in the grid and need the whole SM), so the decode state stream overlaps the
+// prefill in one launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void group_bar(int g) { asm volatile("bar.sync %0, 128;" :: "r"(g + 1) : "memory"); }
+
+struct DecodeIn {
+    int64_t slot, row;
+    int h, j0;
+    float q, k, gr, b;
+    float4 v;
+};
+
+// Loads tile `tile`'s inputs into registers and starts its state slice on its way into this
+// thread's staging slots (cp.async; each thread stages exactly what it will hold).
+__device__ __forceinline__ void decode_load(const Args &args, uint32_t tile, int gt, uint32_t stage,
+                                            DecodeIn &in)
+{
+    constexpr int VS = VD / 32;
+    const Params &p = args.p;
+    const uint32_t per_e = static_cast<uint32_t>(p.H) * VS;
+    const uint32_t e = tile / per_e, rem = tile - e * per_e;
+    in.h = static_cast<int>(rem / VS);
+    in.j0 = static_cast<int>(rem % VS) * 32 + (gt & 7) * 4;
+    in.row = args.cu[e];
+    in.slot = load_slot(p, e);
+    const int rg = gt >> 3;
+    if (in.slot >= 0 && in.slot < p.num_slots) {
+        const float *src = p.pool + in.slot * p.slot_stride + static_cast<int64_t>(in.h) * KD * VD + in.j0;
+#pragma unroll
+        for (int i = 0; i < KD / 16; i++)
+            cp_async16(stage + static_cast<uint32_t>(i * 128 * 16), src + static_cast<int64_t>(rg + 16 * i) * VD, true);
+    }
+    cp_async_commit();
+    const int64_t HK = static_cast<int64_t>(p.H) * KD;
+    const uint16_t *row = p.qkv + in.row * p.ld_qkv;
+    in.q = bf16_to_f32(row[in.h * KD + gt]);
+    in.k = bf16_to_f32(row[HK + in.h * KD + gt]);
+    in.gr = bf16_to_f32(p.rg[in.row * p.ld_g + in.h * KD + gt]);
+    in.b = bf16_to_f32(p.rb[in.row * p.ld_beta + in.h]);
+    const uint16_t *vp = row + 2 * HK + static_cast<int64_t>(in.h) * VD + in.j0;
+    in.v = make_float4(bf16_to_f32(vp[0]), bf16_to_f32(vp[1]), bf16_to_f32(vp[2]), bf16_to_f32(vp[3]));
+}
+
+__device__ __noinline__ void decode_worker(const Args &args, unsigned char *smem)
+{
+    constexpr int RPT = KD / 16;
+    const Params &p = args.p;
+    const int tid = threadIdx.x, g = tid >> 7, gt = tid & 127, lane = tid & 31, gw = gt >> 5;
+    const int cg = gt & 7, rg = gt >> 3;
+    // per group: s_a [KD], s_k [2][KD] (by tile parity: it is read after the group's second
+    // barrier), s_q [KD], s_part [4][3], s_red [4][2][32]; then the staging slots
+    // [RPT][128] float4 of every group
+    float *fs = reinterpret_cast<float *>(smem) + g * 1024;
+    float *s_a = fs, *s_k = fs + KD, *s_q = fs + 3 * KD, *s_part = fs + 4 * KD, *s_red = fs + 4 * KD + 16;
+    const float4 *stage_ptr = reinterpret_cast<const float4 *>(smem + 16384 + g * RPT * 128 * 16) + gt;
+    const uint32_t stage = tc::smem_addr(stage_ptr);
+    const uint32_t ntiles = static_cast<uint32_t>(args.num_decodes) * static_cast<uint32_t>(p.H) * (VD / 32);
+    const uint32_t step = (gridDim.x - static_cast<uint32_t>(args.n_chunk)) * 4u;
+    uint32_t tile = (blockIdx.x - static_cast<uint32_t>(args.n_chunk)) * 4u + static_cast<uint32_t>(g);
+    if (tile >= ntiles) return;
+    DecodeIn cur, nxt;
+    decode_load(args, tile, gt, stage, cur);
+    int kb = 0;
+    for (; tile < ntiles; tile += step) {
+        const bool more = tile + step < ntiles;
+        if (cur.slot >= p.num_slots) {                // out of range: flag, zero outputs
+            if (more) decode_load(args, tile + step, gt, stage, nxt);
+            if (gt == 0 && p.err) atomicOr(p.err, kErrSlotRange);
+            if (rg == 0)
+                *reinterpret_cast<uint2 *>(p.out + cur.row * p.ld_out + static_cast<int64_t>(cur.h) * VD + cur.j0) =
+                    make_uint2(0u, 0u);
+        } else {
+            float4 S[RPT];
+            cp_async_wait_all();
+#pragma unroll
+            for (int i = 0; i < RPT; i++) S[i] = cur.slot >= 0 ? stage_ptr[i * 128] : make_float4(0.f, 0.f, 0.f, 0.f);
+            // ---- [A] gate + stash ----
+            const float expA = expf(__ldg(p.A_log + cur.h));
+            const float dtb = p.dt_bias ? __ldg(p.dt_bias + cur.h * KD + gt) : 0.f;
+            s_a[gt] = expf(gate_log_decay(cur.gr + dtb, expA, p.has_lb, p.lb));
+            s_k[kb * KD + gt] = cur.k;
+            s_q[gt] = cur.q;
+            {
+                const float qq = warp_sum(cur.q * cur.q), kk = warp_sum(cur.k * cur.k), qk = warp_sum(cur.q * cur.k);
+                if (lane == 0) { s_part[gw * 3] = qq; s_part[gw * 3 + 1] = kk; s_part[gw * 3 + 2] = qk; }
+            }
+            group_bar(g);
+            // the group's reads of its staging slots are ordered before this barrier: the
+            // next tile's copies may start
+            if (more) decode_load(args, tile + step, gt, stage, nxt);
+            // ---- [B] decay + partial reductions ----
+            float qq = 0.f, kk = 0.f, qk = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; w++) { qq += s_part[w * 3]; kk += s_part[w * 3 + 1]; qk += s_part[w * 3 + 2]; }
+            const float rq = p.scale * rsqrtf(qq + p.eps), rk = rsqrtf(kk + p.eps);
+            float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < RPT; i++) {
+                const int r = rg + 16 * i;
+                const float a = s_a[r], kr = s_k[kb * KD + r], qr = s_q[r];
+                S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
+                pk[0] += kr * S[i].x; pk[1] += kr * S[i].y; pk[2] += kr * S[i].z; pk[3] += kr * S[i].w;
+                pq[0] += qr * S[i].x; pq[1] += qr * S[i].y; pq[2] += qr * S[i].z; pq[3] += qr * S[i].w;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+                pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 8);
+                pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 16);
+                pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 8);
+                pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 16);
+            }
+            if (lane < 8) {
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    s_red[(gw * 2) * 32 + cg * 4 + jj] = pk[jj];
+                    s_red[(gw * 2 + 1) * 32 + cg * 4 + jj] = pq[jj];
+                }
+            }
+            group_bar(g);
+            // ---- [C] u, o, rank-1 update ----
+            const float beta = sigmoid_f(cur.b), qkh = qk * rq * rk;
+            const float vv[4] = {cur.v.x, cur.v.y, cur.v.z, cur.v.w};
+            float u[4], o[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+                const int c = cg * 4 + jj;
+                const float ks = (s_red[0 * 32 + c] + s_red[2 * 32 + c] + s_red[4 * 32 + c] + s_red[6 * 32 + c]) * rk;
+                const float qs = (s_red[1 * 32 + c] + s_red[3 * 32 + c] + s_red[5 * 32 + c] + s_red[7 * 32 + c]) * rq;
+                u[jj] = beta * (vv[jj] - ks);
+                o[jj] = qs + qkh * u[jj];
+            }
+            const bool writable = cur.slot >= 0 && cur.slot != p.null_slot;
+            float *tile_ptr = writable ? p.pool + cur.slot * p.slot_stride + static_cast<int64_t>(cur.h) * KD * VD : nullptr;
+#pragma unroll
+            for (int i = 0; i < RPT; i++) {
+                const float kh = s_k[kb * KD + rg + 16 * i] * rk;
+                S[i].x += kh * u[0]; S[i].y += kh * u[1]; S[i].z += kh * u[2]; S[i].w += kh * u[3];
+                if (writable)
+                    *reinterpret_cast<float4 *>(tile_ptr + static_cast<int64_t>(rg + 16 * i) * VD + cur.j0) = S[i];
+            }
+            if (rg == 0) {
+                uint2 packed;
+                packed.x = pack_bf16x2(o[0], o[1]);
+                packed.y = pack_bf16x2(o[2], o[3]);
+                *reinterpret_cast<uint2 *>(p.out + cur.row * p.ld_out + static_cast<int64_t>(cur.h) * VD + cur.j0) = packed;
+            }
+            kb ^= 1;
+        }
+        if (more) cur = nxt;
+    }
+    cp_async_wait_all();
+}
+
 __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Args args)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
+    if (static_cast<int>(blockIdx.x) >= args.n_chunk) {
+        decode_worker(args, smem);
+        return;
+    }
     const Params &p = args.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
@@ -845,13 +1011,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 
 size_t chunk_workspace_bytes(const int32_t *, int64_t, int, int, int, int) { return 0; }
 
-cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *cu,
-                                 const int32_t *cu_host, int64_t entry_base, int64_t num_seqs,
-                                 int, void *, size_t, cudaStream_t stream)
+// One launch: the prefill chains of entries [entry_base, entry_base + num_seqs), ordered
+// longest first, then (num_decodes > 0) decode-worker CTAs for the length-1 entries
+// [0, num_decodes) of a mixed batch.
+static cudaError_t launch_chunk_grid(const Params &p, const int32_t *cu, const int32_t *cu_host,
+                                     int64_t entry_base, int64_t num_seqs, int64_t num_decodes,
+                                     cudaStream_t stream)
 {
-    if (num_seqs <= 0) return cudaSuccess;
-    if (K != chunk::KD || V != chunk::VD)  // other head sizes take the token-recurrent kernel
-        return launch_recurrent(p, K, V, 2, 1, cu, entry_base, num_seqs, stream);
     cudaError_t err = cudaFuncSetAttribute(chunk::chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(chunk::SMEM_BYTES));
     if (err != cudaSuccess) return err;
@@ -860,6 +1026,8 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
     a.cu = cu;
     a.entry_base = entry_base;
     a.num_seqs = static_cast<int32_t>(num_seqs);
+    a.n_chunk = static_cast<int32_t>(num_seqs * p.H);
+    a.num_decodes = static_cast<int32_t>(num_decodes);
     a.order_n = 0;
     if (num_seqs <= chunk::kMaxOrder) {
         // longest sequence first, so the longest chains start in the first wave
@@ -872,9 +1040,46 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
         for (int64_t i = 0; i < num_seqs; i++) a.order[i] = ord[static_cast<size_t>(i)];
         a.order_n = static_cast<int32_t>(num_seqs);
     }
-    const int64_t grid = num_seqs * p.H;
+    int64_t workers = 0;
+    if (num_decodes > 0) {
+        // one worker CTA per SM the chains leave free, at least a quarter of the SMs (they
+        // also take over SMs whose chains finish early), at most one tile per group
+        int dev = 0, sms = 0;
+        if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        const int64_t tiles = num_decodes * p.H * (chunk::VD / 32);
+        workers = sms - static_cast<int64_t>(a.n_chunk);
+        if (workers < sms / 4) workers = sms / 4;
+        if (workers < 1) workers = 1;
+        if (workers > (tiles + 3) / 4) workers = (tiles + 3) / 4;
+    }
+    const int64_t grid = static_cast<int64_t>(a.n_chunk) + workers;
+    if (grid <= 0) return cudaSuccess;
     chunk::chunk_kernel<<<static_cast<unsigned>(grid), chunk::NT, chunk::SMEM_BYTES, stream>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *cu,
+                                 const int32_t *cu_host, int64_t entry_base, int64_t num_seqs,
+                                 int, void *, size_t, cudaStream_t stream)
+{
+    if (num_seqs <= 0) return cudaSuccess;
+    if (K != chunk::KD || V != chunk::VD)  // other head sizes take the token-recurrent kernel
+        return launch_recurrent(p, K, V, 2, 1, cu, entry_base, num_seqs, stream);
+    return launch_chunk_grid(p, cu, cu_host, entry_base, num_seqs, 0, stream);
+}
+
+cudaError_t launch_mixed(const Params &p, int K, int V, const int32_t *cu, const int32_t *cu_host,
+                         int64_t num_decodes, int64_t num_prefills, cudaStream_t stream)
+{
+    if (K != chunk::KD || V != chunk::VD || num_decodes <= 0 || num_prefills <= 0) {
+        if (num_decodes > 0) {
+            cudaError_t e = launch_recurrent(p, K, V, 2, 1, cu, 0, num_decodes, stream);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_chunk_prefill(p, K, V, cu, cu_host, num_decodes, num_prefills, 64, nullptr, 0, stream);
+    }
+    return launch_chunk_grid(p, cu, cu_host, num_decodes, num_prefills, num_decodes, stream);
 }
 
 }  // namespace kda

@@ -68,7 +68,10 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     constexpr int RPT = K / 16;         // rows per thread
     constexpr int KW = K / 32;          // warps that own channels in [A]
 
-    __shared__ float s_a[K], s_k[K], s_q[K];
+    // s_k is read again in [C], after the second barrier, so it alternates between two
+    // buffers by token parity: token t+1's [A] may run while slower warps are still in
+    // token t's [C]. The other arrays are last read before the second barrier.
+    __shared__ float s_a[K], s_k[2][K], s_q[K];
     __shared__ float s_part[KW][3];
     __shared__ float s_red[4][2][VT];
 
@@ -137,13 +140,14 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     if (row0 < row1) fetch(row0);
 
     for (int64_t t = row0; t < row1; t++) {
+        const int kb = static_cast<int>((t - row0) & 1);
         // ---- [A] gate + stash ----
         const float4 v = nv;
         const float beta = sigmoid_f(nb);
         if (chan) {
             const float g = gate_log_decay(ng + dtb, expA, p.has_lb, p.lb);
             s_a[tid] = expf(g);
-            s_k[tid] = nk;
+            s_k[kb][tid] = nk;
             s_q[tid] = nq;
             float qq = warp_sum(nq * nq), kk = warp_sum(nk * nk), qk = warp_sum(nq * nk);
             if (lane == 0) { s_part[warp][0] = qq; s_part[warp][1] = kk; s_part[warp][2] = qk; }
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + 16 * i;
-            const float a = s_a[r], kr = s_k[r], qr = s_q[r];
+            const float a = s_a[r], kr = s_k[kb][r], qr = s_q[r];
             S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
             pk[0] += kr * S[i].x; pk[1] += kr * S[i].y; pk[2] += kr * S[i].z; pk[3] += kr * S[i].w;
             pq[0] += qr * S[i].x; pq[1] += qr * S[i].y; pq[2] += qr * S[i].z; pq[3] += qr * S[i].w;
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
         }
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
-            const float kh = s_k[rg + 16 * i] * rk;
+            const float kh = s_k[kb][rg + 16 * i] * rk;
             S[i].x += kh * u[0]; S[i].y += kh * u[1]; S[i].z += kh * u[2]; S[i].w += kh * u[3];
         }
         if (rg == 0) {

@@ -183,3 +183,44 @@ def test_mixed_batch_null_slot_padding(kda):
     w.index_buf = np.array([[0], [4], [0], [6]], np.int32)
     w.null_slot = 0
     _run(kda, w, "mixed null slot")
+
+
+@pytest.mark.parametrize("num_decodes,H", [(1, 1), (3, 2), (300, 4)])
+def test_mixed_batch_decode_workers(kda, num_decodes, H):
+    """At K = V = 128 the decodes of a mixed batch run on worker CTAs of the chunk launch,
+    each 128-thread group walking (decode, head, slice) tiles with the next tile staged
+    ahead: few tiles (groups with nothing to do) and many (long grid-stride walks)."""
+    lengths = [1] * num_decodes + [130, 64]
+    w = wl.varlen_case(lengths, H, 128, 128, seed=200 + num_decodes, index_stride=3,
+                       num_decodes=num_decodes, kind="mixed", num_slots=2 * len(lengths) + 8)
+    _run(kda, w, f"mixed workers d={num_decodes} H={H}")
+
+
+def test_mixed_batch_decode_worker_slot_semantics(kda):
+    """Decode slots out of range (error bit, zero outputs), negative (zero state, no write)
+    and the null slot (read, not written) among valid ones, on the worker path."""
+    lengths = [1] * 40 + [90]
+    w = wl.varlen_case(lengths, 2, 128, 128, seed=210, num_decodes=40, kind="mixed",
+                       num_slots=64)
+    idx = np.arange(1, 42, dtype=np.int32).reshape(41, 1)
+    idx[3] = -1
+    idx[7] = 64            # out of range
+    idx[11] = 0            # null slot
+    idx[12] = 1 << 30      # out of range
+    w.index_buf = idx
+    w.null_slot = 0
+    _run(kda, w, "mixed worker slots")
+
+
+def test_mixed_batch_repeat_bit_identical(kda):
+    w = wl.varlen_case([1] * 50 + [200, 70], 4, 128, 128, seed=220, num_decodes=50, kind="mixed")
+    dw = hx.DeviceWorkload(w)
+    first = None
+    for _ in range(5):
+        dw.reset_pool()
+        out = hx.run_gpu(dw, kda)
+        torch.cuda.synchronize()
+        snap = (out.clone(), dw.pool_flat.clone())
+        if first is None:
+            first = snap
+        assert torch.equal(snap[0], first[0]) and torch.equal(snap[1], first[1])
