@@ -209,7 +209,6 @@ int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const
  * Layout requirements beyond kda_packed_decode's (the kernel moves 4 channels per load):
  * mixed_qkv and raw_g 8-byte aligned with ld_qkv and ld_g multiples of 4, dt_bias 16-byte
  * aligned, conv weight, bias and state 8-byte aligned with a conv slot_stride multiple of 4.
- * The V / 32 column slices of one (sequence, head) run as one thread-block cluster.
  * Can be captured in a CUDA graph.
  */
 int kda_fused_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
