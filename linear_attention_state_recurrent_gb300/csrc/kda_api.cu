@@ -255,6 +255,15 @@ int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
     if (num_reqs == 0) return ok();
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
+    // Rows laid out for 8-byte channel loads take the one-CTA-per-head kernel (the fused
+    // kernel with no conv and no norm); others the V-split spec kernel.
+    if (tokens_per_req <= 16 && aligned(mixed_qkv, 8) && aligned(raw_g, 8) && ld_qkv % 4 == 0 &&
+        ld_g % 4 == 0 && aligned(heads->dt_bias, 16)) {
+        const kda::TailParams none{};
+        return cuda_status(kda::launch_fused(p, none, heads->K, heads->V, tokens_per_req, num_reqs,
+                                             static_cast<cudaStream_t>(stream)),
+                           "kda_spec_verify launch");
+    }
     return cuda_status(kda::launch_spec(p, heads->K, heads->V, tokens_per_req, num_reqs,
                                         static_cast<cudaStream_t>(stream)),
                        "kda_spec_verify launch");

@@ -175,3 +175,14 @@ def test_cuda_graph_replay(kda):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
         assert torch.equal(dw.pool_flat.view(torch.int32), eager_pool.view(torch.int32))
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_spec_verify_unaligned_rows(kda, T):
+    """Rows whose pitch is not a multiple of 4 elements take the V-split spec kernel (the
+    one-CTA-per-head kernel needs 8-byte channel loads); both give the same results."""
+    w = wl.spec_verify(seed=700 + T, num_reqs=6, T=T, H=3, num_slots=16, num_padding=1)
+    pad = np.zeros((w.N, 1), np.uint16)
+    w.mixed_qkv = np.concatenate([w.mixed_qkv, pad], axis=1)
+    w.raw_g = np.concatenate([w.raw_g, pad], axis=1)
+    _run_and_check(kda, w, f"spec unaligned T={T}")
