@@ -186,3 +186,33 @@ def test_spec_verify_unaligned_rows(kda, T):
     w.mixed_qkv = np.concatenate([w.mixed_qkv, pad], axis=1)
     w.raw_g = np.concatenate([w.raw_g, pad], axis=1)
     _run_and_check(kda, w, f"spec unaligned T={T}")
+
+
+@pytest.mark.parametrize("K,V", [(32, 32), (32, 128), (64, 64), (128, 32), (128, 64)])
+@pytest.mark.parametrize("T", [3, 8])
+def test_spec_verify_dims(kda, K, V, T):
+    w = wl.spec_verify(seed=800 + K + V + T, num_reqs=5, T=T, H=3, K=K, V=V, num_slots=16,
+                       num_padding=1, index_stride=2)
+    _run_and_check(kda, w, f"spec K={K} V={V} T={T}")
+
+
+def test_spec_verify_without_dt_bias_scale_one(kda):
+    w = wl.spec_verify(seed=810, num_reqs=4, T=5, H=2, num_slots=16, num_padding=1)
+    w.dt_bias = None
+    w.scale = 1.0
+    _run_and_check(kda, w, "spec no dt_bias, scale 1")
+
+
+def test_spec_verify_slot_semantics(kda):
+    """Spec-verify requests on out-of-range slots (error bit, zero outputs), a negative
+    slot (zero state, no write) and the null slot (read, never written)."""
+    w = wl.spec_verify(seed=820, num_reqs=6, T=4, H=2, num_slots=10, num_padding=0)
+    w.index_buf = np.array([[3], [-1], [10], [7], [1 << 30], [5]], np.int32)
+    w.null_slot = 7
+    dw = hx.DeviceWorkload(w)
+    out = hx.run_gpu(dw, kda)
+    ref = ko.run(w)
+    assert ref.err_flags == ko.ERR_SLOT_OUT_OF_RANGE
+    hx.check(dw, out, ref, fp32_path=True, label="spec slot semantics")
+    o = out.float().cpu()
+    assert torch.all(o[8:12] == 0) and torch.all(o[16:20] == 0)

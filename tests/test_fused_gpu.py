@@ -141,3 +141,11 @@ def test_fused_graph_replay_and_repeat(kda):
         if first is None:
             first = out.clone()
         assert torch.equal(out, first)
+
+
+def test_fused_without_dt_bias_scale_one(kda):
+    base = wl.decode_case(7, 3, 128, 128, seed=95, index_stride=2, scale=1.0, with_dt_bias=False)
+    _run(kda, wl.with_layer_tail(base, seed=96), "fused decode no dt_bias, scale 1")
+    s = wl.spec_verify(seed=97, num_reqs=3, T=6, H=2, num_slots=16, num_padding=1)
+    s.dt_bias = None
+    _run(kda, wl.with_layer_tail(s, seed=98, conv_width=3), "fused spec no dt_bias")
