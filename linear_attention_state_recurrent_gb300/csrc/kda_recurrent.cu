@@ -59,7 +59,9 @@ enum RowMode { kRowsDecode = 0, kRowsSpec = 1, kRowsVarlen = 2 };
 
 // 8 CTAs per SM (64 registers per thread): the decode is bound by how many state bytes
 // are in flight, and at 8 resident CTAs each SM keeps 128 KiB of loads outstanding.
-template <int K, int V>
+// ONE: every entry is a single token (decode mode), so nothing is reused across tokens
+// and s_k needs no second buffer.
+template <int K, int V, bool ONE>
 __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, int T,
                                                         const int32_t *cu, int64_t entry_base)
 {
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     // s_k is read again in [C], after the second barrier, so it alternates between two
     // buffers by token parity: token t+1's [A] may run while slower warps are still in
     // token t's [C]. The other arrays are last read before the second barrier.
-    __shared__ float s_a[K], s_k[2][K], s_q[K];
+    __shared__ float s_a[K], s_k[ONE ? 1 : 2][K], s_q[K];
     __shared__ float s_part[KW][3];
     __shared__ float s_red[4][2][VT];
 
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     if (row0 < row1) fetch(row0);
 
     for (int64_t t = row0; t < row1; t++) {
-        const int kb = static_cast<int>((t - row0) & 1);
+        const int kb = ONE ? 0 : static_cast<int>((t - row0) & 1);
         // ---- [A] gate + stash ----
         const float4 v = nv;
         const float beta = sigmoid_f(nb);
@@ -471,7 +473,10 @@ static cudaError_t launch_rec_kv(const Params &p, int mode, int T, const int32_t
                                  int64_t entry_base, int64_t num_entries, cudaStream_t stream)
 {
     const int64_t grid = num_entries * p.H * (V / 32);
-    recurrent_kernel<K, V><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, mode, T, cu, entry_base);
+    if (mode == kRowsDecode)
+        recurrent_kernel<K, V, true><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, mode, T, cu, entry_base);
+    else
+        recurrent_kernel<K, V, false><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, mode, T, cu, entry_base);
     return cudaGetLastError();
 }
 
