@@ -231,6 +231,15 @@ int kda_fused_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint1
                           uint32_t *err_flags, void *stream);
 
 /*
+ * kda_selftest_bounded_wait — exercises the error path of the bounded waits that the
+ * tensor-core kernels use on their mbarriers, without a fault: one CTA waits on an
+ * mbarrier that nothing arrives at, gives up after ~2 s, sets KDA_ERRFLAG_TIMEOUT in
+ * *err_flags (device uint32, required) and returns. The CUDA context stays usable; the
+ * call is asynchronous like every other.
+ */
+int kda_selftest_bounded_wait(uint32_t *err_flags, void *stream);
+
+/*
  * kda_chunk_prefill_workspace_bytes — device workspace kda_chunk_prefill needs for
  * these sequence lengths (cu_seqlens_host: host int32 [num_seqs+1]). Returns 0 on
  * invalid arguments (and sets kda_last_error) or when no workspace is needed.

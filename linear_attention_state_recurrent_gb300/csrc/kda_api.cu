@@ -349,6 +349,13 @@ int kda_fused_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint1
                         "kda_fused_spec_verify launch");
 }
 
+int kda_selftest_bounded_wait(uint32_t *err_flags, void *stream)
+{
+    if (!err_flags) return fail(KDA_ERR_INVALID_ARGUMENT, "err_flags is NULL");
+    return cuda_status(kda::launch_bounded_wait_selftest(err_flags, static_cast<cudaStream_t>(stream)),
+                       "kda_selftest_bounded_wait launch");
+}
+
 size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t num_seqs,
                                          const kda_heads *heads, int32_t chunk_size)
 {

@@ -1009,7 +1009,32 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 
 }  // namespace chunk
 
+// One CTA of NT threads waits, as the chain CTAs do (one warp polls, the rest park on the
+// barrier), on an mbarrier that nothing arrives at. The bounded wait gives up after ~2 s;
+// the kernel then records the timeout in the error word and returns normally.
+__global__ void __launch_bounds__(chunk::NT, 1) bounded_wait_selftest_kernel(uint32_t *err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int waitok;
+    const uint32_t mbar = tc::smem_addr(&bar);
+    if (threadIdx.x == 0) tc::mbar_init(mbar, 1);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait(mbar, 0);
+        if ((threadIdx.x & 31) == 0) waitok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !waitok && err) atomicOr(err, kErrTimeout);
+}
+
 size_t chunk_workspace_bytes(const int32_t *, int64_t, int, int, int, int) { return 0; }
+
+cudaError_t launch_bounded_wait_selftest(uint32_t *err, cudaStream_t stream)
+{
+    bounded_wait_selftest_kernel<<<1, chunk::NT, 0, stream>>>(err);
+    return cudaGetLastError();
+}
 
 // One launch: the prefill chains of entries [entry_base, entry_base + num_seqs), ordered
 // longest first, then (num_decodes > 0) decode-worker CTAs for the length-1 entries

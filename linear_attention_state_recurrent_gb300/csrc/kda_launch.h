@@ -35,6 +35,9 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
                                  int chunk_size, void *workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+// The bounded-wait self-test (one CTA waits on an mbarrier nothing arrives at).
+cudaError_t launch_bounded_wait_selftest(uint32_t *err, cudaStream_t stream);
+
 // Mixed batch: decodes are entries [0, num_decodes) (length 1), prefills the next
 // num_prefills entries. At K = V = 128 one launch runs both (the decodes on worker CTAs
 // beside the prefill chains); otherwise the recurrent and chunk launches run in turn.

@@ -29,11 +29,12 @@ KDA_ERR_UNSUPPORTED = 2
 KDA_ERR_WORKSPACE = 3
 KDA_ERR_CUDA = 4
 KDA_ERRFLAG_SLOT_RANGE = 1
+KDA_ERRFLAG_TIMEOUT = 2
 
 EXPORTED = ("kda_last_error", "kda_status_string", "kda_gate", "kda_packed_decode",
             "kda_spec_verify", "kda_spec_verify_checkpoints", "kda_fused_decode",
-            "kda_fused_spec_verify", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill",
-            "kda_mixed_batch")
+            "kda_fused_spec_verify", "kda_selftest_bounded_wait", "kda_chunk_prefill_workspace_bytes",
+            "kda_chunk_prefill", "kda_mixed_batch")
 
 
 class KdaHeads(ctypes.Structure):
@@ -89,6 +90,8 @@ def _load():
     lib.kda_fused_spec_verify.restype = ctypes.c_int
     lib.kda_fused_spec_verify.argtypes = [P, I64, P, I64, P, I64, I64, I32, HP, SP, CP, NP, P, I64,
                                           P, P]
+    lib.kda_selftest_bounded_wait.restype = ctypes.c_int
+    lib.kda_selftest_bounded_wait.argtypes = [P, P]
     lib.kda_chunk_prefill_workspace_bytes.restype = SZ
     lib.kda_chunk_prefill_workspace_bytes.argtypes = [P, I64, HP, I32]
     lib.kda_chunk_prefill.restype = ctypes.c_int
@@ -328,6 +331,12 @@ def kda_fused_spec_verify(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_boun
     return _fused("kda_fused_spec_verify", mixed_qkv, raw_g, raw_beta, A_log, dt_bias,
                   lower_bound, initial_state, state_indices, int(tokens_per_req), conv, norm,
                   scale, l2_eps, null_slot, out, err_flags, stream)
+
+
+def kda_selftest_bounded_wait(err_flags, stream=None):
+    """Runs the bounded-wait self-test; err_flags (int32/uint32 device tensor) receives
+    KDA_ERRFLAG_TIMEOUT once the wait has given up (after ~2 s)."""
+    _check(lib.kda_selftest_bounded_wait(_ptr(err_flags), _stream(stream)), "kda_selftest_bounded_wait")
 
 
 def _host_cu(cu_seqlens, cu_seqlens_host):

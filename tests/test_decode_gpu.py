@@ -3,6 +3,8 @@ run through the C ABI. The parameter matrix is the one the vLLM packed-decode te
 runs for every implementation of the call (PR #51682: num_seqs in {1, 8, 32},
 lower_bound in {-5.0, None}, state index stride in {1, 8}); here every entry point
 runs it."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -216,3 +218,15 @@ def test_spec_verify_slot_semantics(kda):
     hx.check(dw, out, ref, fp32_path=True, label="spec slot semantics")
     o = out.float().cpu()
     assert torch.all(o[8:12] == 0) and torch.all(o[16:20] == 0)
+
+
+def test_bounded_wait_gives_up_and_context_stays_usable(kda):
+    """The tensor-core kernels' bounded mbarrier wait, made to run out (nothing arrives):
+    the kernel sets the timeout bit and returns; later calls on the context still work."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    kda.kda_selftest_bounded_wait(err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == kda.KDA_ERRFLAG_TIMEOUT
+    assert time.perf_counter() - t0 >= 1.5
+    _run_and_check(kda, wl.tiny_decode(), "decode after a timed-out wait")
