@@ -256,8 +256,9 @@ size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t
  * hold the same non-decreasing, non-negative int32 values; the host copy sizes the
  * launch; mixed_qkv, raw_g, raw_beta and out must hold cu_seqlens[num_seqs] rows.
  * chunk_size must be 64. mixed_qkv, raw_g and out must be 16-byte aligned with ld_qkv,
- * ld_g and ld_out multiples of 8 (the tensor-core path moves them in 16-byte vectors). `workspace` (device, 256-byte aligned) must
- * hold kda_chunk_prefill_workspace_bytes(...) bytes; it may be NULL when that is 0.
+ * ld_g and ld_out multiples of 8 (the tensor-core path moves them in 16-byte vectors).
+ * `workspace` (device, 256-byte aligned) must hold kda_chunk_prefill_workspace_bytes(...)
+ * bytes; it may be NULL when that is 0 (this version's kernels need none).
  * Zero-length sequences are allowed: their slot is left untouched.
  */
 int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
@@ -273,8 +274,9 @@ int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t 
  * length-1 sequences). Sequences 0..num_decodes-1 must have length 1 and take the
  * recurrent decode path; sequences num_decodes..num_decodes+num_prefills-1 take
  * the chunked prefill path. One cu_seqlens (device + host copies) and one strided
- * index view cover all of them, decodes first. Workspace as for
- * kda_chunk_prefill over the prefill sequences:
+ * index view cover all of them, decodes first. At K = V = 128 both run in one launch
+ * (the decodes on worker CTAs beside the prefill chains); other head sizes take two
+ * launches in turn. Workspace as for kda_chunk_prefill over the prefill sequences:
  * kda_chunk_prefill_workspace_bytes(cu_seqlens_host + num_decodes, num_prefills, ...).
  */
 int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
