@@ -55,9 +55,13 @@ constexpr uint32_t SM_DIAGB = 122880;      // tf32 [64 x 128]  K^R
 constexpr uint32_t SM_PB = 155648;         // fp16 [128 x 128] K^G rows 0..63, Q^G rows 64..127
 constexpr uint32_t SM_TB = 188416;         // fp16 [64 x 64]   T
 constexpr uint32_t SM_SB = 196608;         // fp16 [192 x 64]  Aqk rows 0..63, Kd^T rows 64..191
-constexpr uint32_t SM_SB_KD = SM_SB + 8192;
+// SB's 8-row core-matrix blocks sit SBO_SB = 1040 bytes apart (16 bytes of padding per
+// block): the transposed Kd^T stores of a warp's four 16-channel groups land 2 blocks
+// apart, which with a 1024-byte stride would put them in the same banks
+constexpr uint32_t SBO_SB = 64 * 2 * 8 + 16;
+constexpr uint32_t SM_SB_KD = SM_SB + 8 * SBO_SB;
 constexpr uint32_t SM_TAB = SM_TB;         // phase A only: per (block, channel) constants (14336 B)
-constexpr uint32_t SM_TOT = 221184;        // fp32 [8][128] per-warp sums of g, then prefixes P_w
+constexpr uint32_t SM_TOT = SM_SB + 24 * SBO_SB;   // fp32 [8][128] per-warp sums of g, then prefixes P_w
 constexpr uint32_t SM_GC = SM_TOT + 4096;  // fp32 [128] e^{b_last}
 constexpr uint32_t SM_BLAST = SM_GC + 512; // fp32 [128] b_last
 constexpr uint32_t SM_BETA = SM_BLAST + 512;  // fp32 [64]
@@ -102,6 +106,12 @@ constexpr uint32_t TM_A = 416;    // A operands of the chain MMAs, fp16 packed i
 constexpr uint32_t SBO128_F16 = 128 * 2 * 8;  // K = 128 fp16
 constexpr uint32_t SBO128_TF32 = 128 * 4 * 8; // K = 128 tf32
 constexpr uint32_t SBO64_F16 = 64 * 2 * 8;    // K = 64 fp16
+
+// byte offset of fp16 element (row, k) of SB (K = 64, padded block stride SBO_SB)
+__device__ __forceinline__ uint32_t sb_offset(int row, int k)
+{
+    return static_cast<uint32_t>((row >> 3) * SBO_SB + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
 
 // Packs 2*n fp32 values into n fp16 pairs (element 2i in the low half).
 template <int n>
@@ -310,8 +320,8 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
         for (int u = 0; u < 16; u += 4) *reinterpret_cast<float4 *>(Arow + u) = make_float4(a[u], a[u + 1], a[u + 2], a[u + 3]);
     } else {
         const uint32_t base = tc::smem_addr(smem + SM_SB);
-        st_shared_u4(base + tc::core_offset(r, i0, 64, 2), pack8_f16(a));
-        st_shared_u4(base + tc::core_offset(r, i0 + 8, 64, 2), pack8_f16(a + 8));
+        st_shared_u4(base + sb_offset(r, i0), pack8_f16(a));
+        st_shared_u4(base + sb_offset(r, i0 + 8), pack8_f16(a + 8));
     }
 }
 
@@ -820,7 +830,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tab8(4, k0, t8);
 #pragma unroll
                 for (int o = 0; o < 8; o++)
-                    st_shared_u16(sbkd + tc::core_offset(k0 + o, ra, 64, 2), f16_bits(kh[o] * t8[o]));
+                    st_shared_u16(sbkd + sb_offset(k0 + o, ra), f16_bits(kh[o] * t8[o]));
             }
         }
         tc::fence_proxy_async();
@@ -955,7 +965,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            tc::gemm_ta<192, 64>(tmem + TM_P + 64, tmem + TM_A + 32, sbase + SM_SB, SBO64_F16, true);
+            tc::gemm_ta<192, 64>(tmem + TM_P + 64, tmem + TM_A + 32, sbase + SM_SB, SBO_SB, true);
             tc::commit(mbarc);
         }
         ok &= wait_mma(mbarc, phasec, warp, smem);
