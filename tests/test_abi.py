@@ -156,3 +156,62 @@ def test_binding_rejects_2d_indices_without_gpu(kda):
     pool = torch.zeros(2, 1, 32, 32)
     with pytest.raises(ValueError, match="one-dimensional"):
         kda.make_state(pool, idx)
+
+
+def _fused(kda, hd, st, conv=None, norm=None, T=1, N=4, ld_qkv=768, ld_g=256, qkv=FAKE):
+    c = ctypes.byref(conv) if conv is not None else None
+    n = ctypes.byref(norm) if norm is not None else None
+    if T == 1:
+        return kda.lib.kda_fused_decode(qkv, ld_qkv, FAKE, ld_g, FAKE, 2, N, ctypes.byref(hd),
+                                        ctypes.byref(st), c, n, FAKE, 256, None, None)
+    return kda.lib.kda_fused_spec_verify(qkv, ld_qkv, FAKE, ld_g, FAKE, 2, N, T, ctypes.byref(hd),
+                                         ctypes.byref(st), c, n, FAKE, 256, None, None)
+
+
+@pytest.mark.parametrize("conv_kw,pattern", [
+    (dict(width=0), "conv width"),
+    (dict(width=5), "conv width"),
+    (dict(weight=None), "conv weight"),
+    (dict(slot_stride=10), "slot_stride"),
+    (dict(slot_stride=3 * 768 + 2), "multiple of 4"),
+    (dict(state=(1 << 20) + 2), "8-byte aligned"),
+])
+def test_fused_conv_validation(kda, conv_kw, pattern):
+    hd, st = _heads(kda), _state(kda)
+    kw = dict(weight=FAKE.value, bias=None, state=FAKE.value, slot_stride=3 * 768, width=4)
+    kw.update(conv_kw)
+    conv = kda.KdaShortConv(**kw)
+    assert _fused(kda, hd, st, conv=conv) == 1
+    assert re.search(pattern, kda.last_error())
+
+
+def test_fused_norm_and_row_validation(kda):
+    hd, st = _heads(kda), _state(kda)
+    bad_ld = kda.KdaGatedNorm(gate=FAKE.value, ld_gate=255, weight=FAKE.value, eps=1e-5)
+    assert _fused(kda, hd, st, norm=bad_ld) == 1 and "ld_gate" in kda.last_error()
+    bad_eps = kda.KdaGatedNorm(gate=FAKE.value, ld_gate=256, weight=FAKE.value, eps=-1.0)
+    assert _fused(kda, hd, st, norm=bad_eps) == 1 and "eps" in kda.last_error()
+    no_w = kda.KdaGatedNorm(gate=FAKE.value, ld_gate=256, weight=None, eps=1e-5)
+    assert _fused(kda, hd, st, norm=no_w) == 1 and "weight" in kda.last_error()
+    # rows for 8-byte channel loads: pitches multiples of 4, 8-byte aligned pointers
+    assert _fused(kda, hd, st, ld_qkv=770) == 1 and "multiples of 4" in kda.last_error()
+    assert _fused(kda, hd, st, qkv=ctypes.c_void_p((1 << 20) + 4)) == 1
+    for T in (0, 17):
+        assert _fused(kda, hd, st, T=T) == 1 and "tokens_per_req" in kda.last_error()
+    assert _fused(kda, hd, st, N=0) == 0
+
+
+def test_spec_checkpoint_validation(kda):
+    hd = _heads(kda)
+    st = _state(kda, index_stride=4)
+    args = lambda T, acc=None: (FAKE, 768, FAKE, 256, FAKE, 2, 4, T, acc, ctypes.byref(hd),  # noqa: E731
+                                ctypes.byref(st), FAKE, 256, None, None)
+    assert kda.lib.kda_spec_verify_checkpoints(*args(5)) == 1 and "index_stride" in kda.last_error()
+    assert kda.lib.kda_spec_verify_checkpoints(*args(17)) == 1 and "tokens_per_req" in kda.last_error()
+    assert kda.lib.kda_spec_verify_checkpoints(*args(4, ctypes.c_void_p((1 << 20) + 2))) == 1
+    assert "num_accepted" in kda.last_error()
+
+
+def test_bounded_wait_selftest_needs_an_error_word(kda):
+    assert kda.lib.kda_selftest_bounded_wait(None, None) == 1
+    assert "err_flags" in kda.last_error()
