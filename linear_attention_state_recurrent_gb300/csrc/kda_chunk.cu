@@ -261,6 +261,45 @@ __device__ void solve_T(unsigned char *smem, int tid)
 }
 
 // ---------------------------------------------------------------------------
+// Phase C0 (flagged chunks only): the diagonal 16x16 blocks of A (before beta) and of Aqk,
+// pairwise in fp32 from the stash: one warp per (row r, column i <= r) pair of a block, 4
+// channels per lane and a warp reduction; e^{b_r - b_i} is evaluated once for both
+// products. Results: dgK / dgQ [64 rows][16] in the phase-C scratch.
+// ---------------------------------------------------------------------------
+__device__ void flagged_diag(unsigned char *smem, int warp, int lane)
+{
+    const float *stk = reinterpret_cast<const float *>(smem + SM_STK);
+    const float *stq = reinterpret_cast<const float *>(smem + SM_STQ);
+    const float *stb = reinterpret_cast<const float *>(smem + SM_STB);
+    float *dgK = reinterpret_cast<float *>(smem + SM_XTMP);
+    float *dgQ = dgK + 64 * 16;
+    const int c = 4 * lane;
+    for (int pidx = warp; pidx < 4 * 136; pidx += NT / 32) {
+        const int s = pidx / 136, q = pidx - s * 136;   // block s, pair q = rl (rl + 1) / 2 + il
+        int rl = static_cast<int>((sqrtf(8.f * q + 1.f) - 1.f) * 0.5f);
+        if ((rl + 1) * (rl + 2) / 2 <= q) rl++;
+        if (rl * (rl + 1) / 2 > q) rl--;
+        const int il = q - rl * (rl + 1) / 2;
+        const int r = 16 * s + rl, i = 16 * s + il;
+        const float4 kr = *reinterpret_cast<const float4 *>(stk + r * KD + c);
+        const float4 qr = *reinterpret_cast<const float4 *>(stq + r * KD + c);
+        const float4 br = *reinterpret_cast<const float4 *>(stb + r * KD + c);
+        const float4 ki = *reinterpret_cast<const float4 *>(stk + i * KD + c);
+        const float4 bi = *reinterpret_cast<const float4 *>(stb + i * KD + c);
+        const float e0 = __expf(br.x - bi.x) * ki.x, e1 = __expf(br.y - bi.y) * ki.y;
+        const float e2 = __expf(br.z - bi.z) * ki.z, e3 = __expf(br.w - bi.w) * ki.w;
+        float a = kr.x * e0 + kr.y * e1 + kr.z * e2 + kr.w * e3;
+        float aq = qr.x * e0 + qr.y * e1 + qr.z * e2 + qr.w * e3;
+        a = warp_sum(a);
+        aq = warp_sum(aq);
+        if (lane == 0) {
+            dgK[r * 16 + il] = a;
+            dgQ[r * 16 + il] = aq;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Phase C1: one 16-column slice of one row of A (K rows, scaled by beta_r) or Aqk
 // (Q rows), from the off-diagonal and diagonal Gram results in TMEM. Thread roles:
 // TMEM lane quarter qd = warp & 3 (lanes 0..63 are the K rows, 64..127 the Q rows),
@@ -283,26 +322,14 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
     tc::tmem_ld16(tlane + TM_XDIAG + i0, dg);
     tc::tmem_ld_wait();
     if (flagged && k4 == s) {
-        // pairwise in fp32 from the stash for the diagonal block; results go through a
-        // per-row shared-memory scratch so that dg[] keeps static indices (registers)
-        const float *stk = reinterpret_cast<const float *>(smem + SM_STK);
-        const float *stq = reinterpret_cast<const float *>(smem + SM_STQ);
-        const float *stb = reinterpret_cast<const float *>(smem + SM_STB);
-        float *scratch = reinterpret_cast<float *>(smem + SM_XTMP) + ((qpart ? 64 : 0) + r) * 16;
-        const float *xr = (qpart ? stq : stk) + r * KD;
-        const float *br = stb + r * KD;
-        for (int u = 0; u < 16; u++) {
-            const int i = i0 + u;
-            float acc = 0.f;
-            if (i <= r) {
-                const float *ki = stk + i * KD;
-                const float *bi = stb + i * KD;
-                for (int c = 0; c < KD; c++) acc += xr[c] * ki[c] * __expf(br[c] - bi[c]);
-            }
-            scratch[u] = acc;
-        }
+        // the diagonal block, computed pairwise by flagged_diag (entries i > r are not
+        // written there and are masked below)
+        const float4 *src = reinterpret_cast<const float4 *>(smem + SM_XTMP) + ((qpart ? 64 : 0) + r) * 4;
 #pragma unroll
-        for (int u = 0; u < 16; u++) dg[u] = scratch[u];
+        for (int u = 0; u < 4; u++) {
+            const float4 v = src[u];
+            dg[4 * u] = v.x; dg[4 * u + 1] = v.y; dg[4 * u + 2] = v.z; dg[4 * u + 3] = v.w;
+        }
     }
     const float beta = qpart ? 1.f : reinterpret_cast<const float *>(smem + SM_BETA)[r];
     float a[16];
@@ -405,8 +432,20 @@ struct DecodeIn {
 
 // Loads tile `tile`'s inputs into registers and starts its state slice on its way into this
 // thread's staging slots (cp.async; each thread stages exactly what it will hold).
-__device__ __forceinline__ void decode_load(const Args &args, uint32_t tile, int gt, uint32_t stage,
-                                            DecodeIn &in)
+// The row and the state slot of a tile (two index loads; issued a tile ahead of the data
+// loads that need them, so no thread waits on them).
+struct DecodeIdx {
+    int64_t slot, row;
+};
+
+__device__ __forceinline__ DecodeIdx decode_index(const Args &args, uint32_t tile)
+{
+    const uint32_t e = tile / (static_cast<uint32_t>(args.p.H) * (VD / 32));
+    return DecodeIdx{load_slot(args.p, e), static_cast<int64_t>(args.cu[e])};
+}
+
+__device__ __forceinline__ void decode_load(const Args &args, uint32_t tile, DecodeIdx ix, int gt,
+                                            uint32_t stage, DecodeIn &in)
 {
     constexpr int VS = VD / 32;
     const Params &p = args.p;
@@ -414,8 +453,8 @@ __device__ __forceinline__ void decode_load(const Args &args, uint32_t tile, int
     const uint32_t e = tile / per_e, rem = tile - e * per_e;
     in.h = static_cast<int>(rem / VS);
     in.j0 = static_cast<int>(rem % VS) * 32 + (gt & 7) * 4;
-    in.row = args.cu[e];
-    in.slot = load_slot(p, e);
+    in.row = ix.row;
+    in.slot = ix.slot;
     const int rg = gt >> 3;
     if (in.slot >= 0 && in.slot < p.num_slots) {
         const float *src = p.pool + in.slot * p.slot_stride + static_cast<int64_t>(in.h) * KD * VD + in.j0;
@@ -437,34 +476,52 @@ __device__ __forceinline__ void decode_load(const Args &args, uint32_t tile, int
 __device__ __noinline__ void decode_worker(const Args &args, unsigned char *smem)
 {
     constexpr int RPT = KD / 16;
+    constexpr int NS = 3;   // tiles in flight per group: the current one and the next two
     const Params &p = args.p;
     const int tid = threadIdx.x, g = tid >> 7, gt = tid & 127, lane = tid & 31, gw = gt >> 5;
     const int cg = gt & 7, rg = gt >> 3;
     // per group: s_a [KD], s_k [2][KD] (by tile parity: it is read after the group's second
-    // barrier), s_q [KD], s_part [4][3], s_red [4][2][32]; then the staging slots
-    // [RPT][128] float4 of every group
+    // barrier), s_q [KD], s_part [4][3], s_red [4][2][32]; then NS staging buffers of
+    // [RPT][128] float4 per group (208 KiB in all, inside the chain kernel's allocation)
     float *fs = reinterpret_cast<float *>(smem) + g * 1024;
     float *s_a = fs, *s_k = fs + KD, *s_q = fs + 3 * KD, *s_part = fs + 4 * KD, *s_red = fs + 4 * KD + 16;
-    const float4 *stage_ptr = reinterpret_cast<const float4 *>(smem + 16384 + g * RPT * 128 * 16) + gt;
-    const uint32_t stage = tc::smem_addr(stage_ptr);
+    const float4 *stage0 = reinterpret_cast<const float4 *>(smem + 16384 + g * NS * RPT * 128 * 16) + gt;
     const uint32_t ntiles = static_cast<uint32_t>(args.num_decodes) * static_cast<uint32_t>(p.H) * (VD / 32);
     const uint32_t step = (gridDim.x - static_cast<uint32_t>(args.n_chunk)) * 4u;
     uint32_t tile = (blockIdx.x - static_cast<uint32_t>(args.n_chunk)) * 4u + static_cast<uint32_t>(g);
     if (tile >= ntiles) return;
-    DecodeIn cur, nxt;
-    decode_load(args, tile, gt, stage, cur);
-    int kb = 0;
+    // tiles tile, tile + step, tile + 2 step live in c0, c1, c2 and in stages si, si+1, si+2
+    DecodeIn c0, c1, c2;
+    decode_load(args, tile, decode_index(args, tile), gt, tc::smem_addr(stage0), c0);
+    c1 = c0;
+    c2 = c0;
+    if (tile + step < ntiles)
+        decode_load(args, tile + step, decode_index(args, tile + step), gt, tc::smem_addr(stage0 + RPT * 128), c1);
+    else
+        cp_async_commit();
+    // indices of the tile two steps ahead (its data loads are issued next iteration)
+    DecodeIdx ix2 = tile + 2 * step < ntiles ? decode_index(args, tile + 2 * step) : DecodeIdx{0, 0};
+    int kb = 0, si = 0;
     for (; tile < ntiles; tile += step) {
-        const bool more = tile + step < ntiles;
+        // the stage being refilled is the previous tile's: every thread of the group read
+        // its slots there before that tile's first group barrier
+        const int s2 = si == 0 ? 2 : si - 1;
+        const DecodeIdx ix3 = tile + 3 * step < ntiles ? decode_index(args, tile + 3 * step) : DecodeIdx{0, 0};
+        if (tile + 2 * step < ntiles)
+            decode_load(args, tile + 2 * step, ix2, gt, tc::smem_addr(stage0 + s2 * RPT * 128), c2);
+        else
+            cp_async_commit();
+        ix2 = ix3;
+        const DecodeIn &cur = c0;
+        const float4 *stage_ptr = stage0 + si * RPT * 128;
         if (cur.slot >= p.num_slots) {                // out of range: flag, zero outputs
-            if (more) decode_load(args, tile + step, gt, stage, nxt);
             if (gt == 0 && p.err) atomicOr(p.err, kErrSlotRange);
             if (rg == 0)
                 *reinterpret_cast<uint2 *>(p.out + cur.row * p.ld_out + static_cast<int64_t>(cur.h) * VD + cur.j0) =
                     make_uint2(0u, 0u);
         } else {
             float4 S[RPT];
-            cp_async_wait_all();
+            cp_async_wait_group<NS - 1>();   // this tile's copies (the two newer may fly)
 #pragma unroll
             for (int i = 0; i < RPT; i++) S[i] = cur.slot >= 0 ? stage_ptr[i * 128] : make_float4(0.f, 0.f, 0.f, 0.f);
             // ---- [A] gate + stash ----
@@ -478,9 +535,6 @@ __device__ __noinline__ void decode_worker(const Args &args, unsigned char *smem
                 if (lane == 0) { s_part[gw * 3] = qq; s_part[gw * 3 + 1] = kk; s_part[gw * 3 + 2] = qk; }
             }
             group_bar(g);
-            // the group's reads of its staging slots are ordered before this barrier: the
-            // next tile's copies may start
-            if (more) decode_load(args, tile + step, gt, stage, nxt);
             // ---- [B] decay + partial reductions ----
             float qq = 0.f, kk = 0.f, qk = 0.f;
 #pragma unroll
@@ -539,7 +593,9 @@ __device__ __noinline__ void decode_worker(const Args &args, unsigned char *smem
             }
             kb ^= 1;
         }
-        if (more) cur = nxt;
+        c0 = c1;
+        c1 = c2;
+        si = si == 2 ? 0 : si + 1;
     }
     cp_async_wait_all();
 }
@@ -880,19 +936,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 
         // ================= Phase C: A, Aqk, T (the P product is in flight) =================
         // The V tile (read in D3) overlays the diagonal B operand (consumed by now) or, on
-        // the pairwise path, the stash read by the row assembly.
+        // the pairwise path, the stash (dead once flagged_diag has run).
         const uint16_t *vsrc = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD;
-        if (!flagged) {
-            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
-            cp_async_commit();
+        if (flagged) {   // the pairwise diagonal blocks; after them the stash is dead
+            flagged_diag(smem, warp, lane);
+            __syncthreads();
         }
+        stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
+        cp_async_commit();
         assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
-        if (flagged) {
-            stage_rows(sbase + SM_VST, vsrc, p.ld_qkv, n, tid);
-            cp_async_commit();
-        }
         solve_T(smem, tid);
         {
             // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)

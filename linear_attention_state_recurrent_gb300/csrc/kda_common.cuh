@@ -100,6 +100,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// waits until at most N of this thread's most recent cp.async groups are still pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // Slot of entry e: indices[e * index_stride] widened to 64 bits.
 __device__ __forceinline__ int64_t load_slot(const Params &p, int64_t e)
