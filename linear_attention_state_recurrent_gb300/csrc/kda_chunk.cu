@@ -79,9 +79,6 @@ constexpr uint32_t SM_AMAT = SM_OFFA;          // fp32 [64][68]
 constexpr uint32_t SM_XTMP = SM_OFFA + 17408;  // fp32 scratch (<= 15360 B)
 constexpr uint32_t SM_TMAT = SM_OFFB;          // fp32 [64][68]
 constexpr int AP = 68;                         // fp32 row pitch of AMAT / TMAT
-// phase D aliases
-constexpr uint32_t SM_OTILE = SM_OFFB;         // bf16 [64][OT_PITCH] output rows
-constexpr int OT_PITCH = 136;                  // bf16 row pitch (272 B: 16-byte aligned rows)
 // input staging (bf16 [64 rows][128], 16-byte chunks XOR-swizzled by row):
 // the next chunk's q, k, raw_g are copied during this chunk's chain step, this
 // chunk's V rows during its triangular solve
@@ -1024,29 +1021,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         }
         ok &= wait_mma(mbarc, phasec, warp, smem);
         phasec ^= 1;
-        // D7: O^T -> bf16 tile [r][j] in shared memory, then 16-byte row stores
+        // D7: O^T -> bf16 rows, straight from registers: lane j of the warp holds column j
+        // of 16 rows, so each store instruction writes 64 contiguous bytes of one row
         {
-            uint16_t *otile = reinterpret_cast<uint16_t *>(smem + SM_OTILE);
             float v[16];
             const int r0 = 16 * k4;
             tc::tmem_ld16(tlane + TM_P + 64 + r0, v);
             tc::tmem_ld_wait();
+            uint16_t *orow = p.out + (c0 + r0) * p.ld_out + static_cast<int64_t>(h) * VD + jv;
 #pragma unroll
-            for (int u = 0; u < 16; u++) otile[(r0 + u) * OT_PITCH + jv] = f32_to_bf16(v[u]);
+            for (int u = 0; u < 16; u++)
+                if (r0 + u < n) orow[u * p.ld_out] = f32_to_bf16(v[u]);
         }
         tc::fence_before_sync();
-        __syncthreads();
-        {
-            const uint16_t *otile = reinterpret_cast<const uint16_t *>(smem + SM_OTILE);
-#pragma unroll
-            for (int x = 0; x < 2; x++) {
-                const int id = tid + NT * x, r = id >> 4, c8 = (id & 15) * 8;
-                if (r < n) {
-                    const uint4 val = *reinterpret_cast<const uint4 *>(otile + r * OT_PITCH + c8);
-                    *reinterpret_cast<uint4 *>(p.out + (c0 + r) * p.ld_out + static_cast<int64_t>(h) * VD + c8) = val;
-                }
-            }
-        }
         if (__syncthreads_or(ok ? 0 : 1)) {
             ok = false;
             break;
