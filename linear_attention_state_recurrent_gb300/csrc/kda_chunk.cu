@@ -682,9 +682,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         const int n = static_cast<int>((row1 - c0) < C ? (row1 - c0) : C);
 
         // ================= Phase A: gate, norms, cumulative decay, operands =================
-        // staged inputs of this chunk (copied during the previous chain step)
+        // staged inputs of this chunk (copied during the previous chain step); the same
+        // barrier ends the previous chunk and carries its timeout verdict
         cp_async_wait_all();
-        __syncthreads();
+        if (__syncthreads_or(ok ? 0 : 1)) {
+            ok = false;
+            break;
+        }
+        tc::fence_after_sync();
         RowIn in;
         const bool valid = ra < n;
         load_row_inputs(sbase, ra, cb, in);
@@ -1034,10 +1039,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 if (r0 + u < n) orow[u * p.ld_out] = f32_to_bf16(v[u]);
         }
         tc::fence_before_sync();
-        if (__syncthreads_or(ok ? 0 : 1)) {
-            ok = false;
-            break;
-        }
     }
 
     // ---- final state -> pool ----
