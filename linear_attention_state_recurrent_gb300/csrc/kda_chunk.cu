@@ -926,15 +926,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             }
             tc::tmem_st_wait();
         }
+        // one barrier both orders every thread's S^T operand before the P issue and ends
+        // the Gram wait (P queues behind the Gram MMAs in the tensor pipe anyway)
         tc::fence_before_sync();
-        __syncthreads();
+        ok &= wait_mma(mbar, phase, warp, smem);
+        phase ^= 1;
         if (tid == 0) {
-            tc::fence_after_sync();
             tc::gemm_ta<128, 128>(tmem + TM_P, tmem + TM_A, sbase + SM_PB, SBO128_F16, false);
             tc::commit(mbarc);
         }
-        ok &= wait_mma(mbar, phase, warp, smem);
-        phase ^= 1;
 
         // ================= Phase C: A, Aqk, T (the P product is in flight) =================
         // The V tile (read in D3) overlays the diagonal B operand (consumed by now) or, on
@@ -974,11 +974,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             if (tid < nn) beta_raw = p.rb[(nx + tid) * p.ld_beta + h];
         }
         cp_async_commit();
+        // the V tile (the older group) has landed for this thread; the barrier inside the
+        // wait makes every thread's part of it visible
+        cp_async_wait_group<1>();
         ok &= wait_mma(mbarc, phasec, warp, smem);
         phasec ^= 1;
         // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 pairs in TMEM (rows r = 16 k4 .. +15)
-        asm volatile("cp.async.wait_group 1;" ::: "memory");   // the V tile (older group) has landed
-        __syncthreads();
         {
             const float *bet = reinterpret_cast<const float *>(smem + SM_BETA);
             const uint16_t *vt = reinterpret_cast<const uint16_t *>(smem + SM_VST);
