@@ -962,6 +962,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             }
             st_shared_u4(sbase + SM_TB + tc::core_offset(r, i0, 64, 2), pack8_f16(v));
         }
+        // TB and the Aqk rows of SB were written through the generic proxy; the U and O/S
+        // products read them through the async proxy (ordered by the barriers that precede
+        // their issue)
+        tc::fence_proxy_async();
 
         // ================= Phase D: the rest of the chain step =================
         // the next chunk's q, k, raw_g rows -> staging (the scratch of phase C is dead now)
