@@ -641,6 +641,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // this warp's lanes
     uint32_t phase = 0, phasec = 0;
     bool ok = true;
+    bool os_pending = false;   // the last product (O and S) of the previous chunk is in flight
 
     // thread roles
     const int jv = 32 * (warp & 3) + lane;  // TMEM lane: value column j in phase D
@@ -650,6 +651,20 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     const int ra = 8 * rga + ir;            // phase A: chunk row
     const int cb = 64 * (warp >> 3) + 16 * iq;  // phase A: first of 16 channels
     const int sA = rga >> 1, hfA = rga & 1; // phase A: row block, half of the block
+
+    // O^T of a finished chunk (rows cs .. cs + nrows - 1) -> bf16 rows, straight from
+    // registers: lane j of the warp holds column j of 16 rows, so each store instruction
+    // writes 64 contiguous bytes of one row
+    auto store_out = [&](int64_t cs, int nrows) {
+        float v[16];
+        const int r0 = 16 * k4;
+        tc::tmem_ld16(tlane + TM_P + 64 + r0, v);
+        tc::tmem_ld_wait();
+        uint16_t *orow = p.out + (cs + r0) * p.ld_out + static_cast<int64_t>(h) * VD + jv;
+#pragma unroll
+        for (int u = 0; u < 16; u++)
+            if (r0 + u < nrows) orow[u * p.ld_out] = f32_to_bf16(v[u]);
+    };
 
     // ---- S0 -> TMEM (S^T: lane j, columns c in this thread's 32-column slice) ----
     {
@@ -678,6 +693,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     uint16_t beta_raw = 0;   // raw_beta of row tid of the current chunk (threads < 64)
     if (tid < C && tid < row1 - row0) beta_raw = p.rb[(row0 + tid) * p.ld_beta + h];
 
+    int64_t last_c0 = row0;
+    int last_n = 0;
     for (int64_t c0 = row0; c0 < row1; c0 += C) {
         const int n = static_cast<int>((row1 - c0) < C ? (row1 - c0) : C);
 
@@ -733,7 +750,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 *reinterpret_cast<float4 *>(tot + rga * KD + cb + u) = make_float4(bv[u], bv[u + 1], bv[u + 2], bv[u + 3]);
         }
         if (tid < C) reinterpret_cast<float *>(smem + SM_BETA)[tid] = (tid < n) ? sigmoid_f(bf16_to_f32(beta_raw)) : 0.f;
-        __syncthreads();
+        if (os_pending) {
+            // this barrier also ends the previous chunk's last product (issued ~4k cycles
+            // ago, so the wait is short): its O rows are stored here, off the chain's
+            // critical path, and its Kd^T operand rows are free for this chunk's
+            ok &= wait_mma(mbarc, phasec, warp, smem);
+            phasec ^= 1;
+            os_pending = false;
+            store_out(c0 - C, C);   // every chunk but the last is full
+        } else {
+            __syncthreads();
+        }
 
         // per-(block, channel) constants: thread tid handles channel tid & 127, block tid >> 7
         int flag = 0;
@@ -1029,21 +1056,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             tc::gemm_ta<192, 64>(tmem + TM_P + 64, tmem + TM_A + 32, sbase + SM_SB, SBO_SB, true);
             tc::commit(mbarc);
         }
+        // D7 (the O rows) runs in the next chunk's phase A, or below for the last chunk
+        os_pending = true;
+        last_c0 = c0;
+        last_n = n;
+        tc::fence_before_sync();
+    }
+    // the last chunk's product; also waited for after a timeout elsewhere, so that no MMA
+    // is in flight when the tensor memory is released
+    if (os_pending) {
         ok &= wait_mma(mbarc, phasec, warp, smem);
         phasec ^= 1;
-        // D7: O^T -> bf16 rows, straight from registers: lane j of the warp holds column j
-        // of 16 rows, so each store instruction writes 64 contiguous bytes of one row
-        {
-            float v[16];
-            const int r0 = 16 * k4;
-            tc::tmem_ld16(tlane + TM_P + 64 + r0, v);
-            tc::tmem_ld_wait();
-            uint16_t *orow = p.out + (c0 + r0) * p.ld_out + static_cast<int64_t>(h) * VD + jv;
-#pragma unroll
-            for (int u = 0; u < 16; u++)
-                if (r0 + u < n) orow[u * p.ld_out] = f32_to_bf16(v[u]);
-        }
-        tc::fence_before_sync();
+        if (ok) store_out(last_c0, last_n);
     }
 
     // ---- final state -> pool ----
