@@ -10,11 +10,15 @@
 //   O   = (Q^ * Gamma) S0 + Aqk U
 //   S_C = Diag(e^{b_last}) S0 + (K^ * e^{b_last - b})^T U
 // (U = U~ - W S0 with W = T diag(beta)(K^ * Gamma) and U~ = T diag(beta) V, folded into
-// one product.) The state is kept transposed in tensor memory (lane = value column j,
-// column = key channel c), so every product has the 128-long V dimension as MMA M:
+// one product.) U only enters through Aqk U and Kd^T U, so T is applied to those two
+// instead, off the chain: with Y = V - K^G S,
+//   O   = (Q^ * Gamma) S0 + (Aqk T) diag(beta) Y,   S_C = ... + (Kd^T T) diag(beta) Y.
+// The state is kept transposed in tensor memory (lane = value column j, column = key
+// channel c), so the chain's products have the 128-long V dimension as MMA M:
 //   P    = S^T [K^G; Q^G]^T            M=128 N=128 K=128  fp16   -> (K^G S)^T | (Q^G S)^T
-//   U^T  = (beta Y)^T T^T,  Y = V - K^G S   M=128 N=64  K=64   fp16
-//   [O^T | S^T] += U^T [Aqk; Kd^T]^T   M=128 N=192 K=64   fp16   (S^T pre-scaled by e^{b_last})
+//   [O^T | S^T] += (beta Y)^T [Aqk T; Kd^T T]^T   M=128 N=192 K=64 fp16 (S^T pre-scaled by e^{b_last})
+// and [Aqk T; Kd^T T] = [Aqk; Kd^T] T is two M=128 N=64 K=64 fp16 products (rows 0..127
+// and 64..191) issued right after the triangular solve.
 // The decay-weighted Gram matrices are split into 16-row blocks. Off-diagonal blocks
 // use the start of the row block as reference point (both factors <= 1, fp16):
 //   X_off = [K^e; Q^e] [B_1; B_2; B_3]^T     M=128 N=96 K=128 fp16
@@ -53,8 +57,9 @@ constexpr uint32_t SM_OFFB = 32768;        // fp16 [96 x 128]  B_1 (16 rows), B_
 constexpr uint32_t SM_DIAGA = 57344;       // tf32 [128 x 128] K^L, Q^L
 constexpr uint32_t SM_DIAGB = 122880;      // tf32 [64 x 128]  K^R
 constexpr uint32_t SM_PB = 155648;         // fp16 [128 x 128] K^G rows 0..63, Q^G rows 64..127
-constexpr uint32_t SM_TB = 188416;         // fp16 [64 x 64]   T
-constexpr uint32_t SM_SB = 196608;         // fp16 [192 x 64]  Aqk rows 0..63, Kd^T rows 64..191
+constexpr uint32_t SM_TB = 188416;         // fp16 [64 x 64]   T^T (row m, K = k holds T[k][m])
+constexpr uint32_t SM_SB = 196608;         // fp16 [192 x 64]  Aqk rows 0..63, Kd^T rows 64..191,
+                                           // then Aqk T and Kd^T T in place
 // SB's 8-row core-matrix blocks sit SBO_SB = 1040 bytes apart (16 bytes of padding per
 // block): the transposed Kd^T stores of a warp's four 16-channel groups land 2 blocks
 // apart, which with a 1024-byte stride would put them in the same banks
@@ -97,7 +102,8 @@ constexpr uint32_t TM_S = 128;    // S^T (128 columns)
 constexpr uint32_t TM_XOFF = 256; // 96 columns
 constexpr uint32_t TM_XDIAG = 352;// 64 columns
 constexpr uint32_t TM_A = 416;    // A operands of the chain MMAs, fp16 packed in pairs:
-                                  // S^T (64 columns), then (beta Y)^T at +0 and U^T at +32
+                                  // S^T (64 columns), then (beta Y)^T at +0
+constexpr uint32_t TM_W = TM_XOFF;// [Aqk; Kd^T] T: rows 0..127 (64 columns), rows 64..191 (64)
 
 // stride byte offsets of the operand tiles
 constexpr uint32_t SBO128_F16 = 128 * 2 * 8;  // K = 128 fp16
@@ -357,6 +363,21 @@ __device__ __forceinline__ bool wait_mma(uint32_t mbar, uint32_t parity, int war
     volatile int *flag = reinterpret_cast<volatile int *>(smem + SM_WAITOK);
     if (warp == 0) {
         const bool ok = tc::mbar_wait(mbar, parity);
+        if ((threadIdx.x & 31) == 0) *flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    const bool ok = *flag != 0;
+    tc::fence_after_sync();
+    return ok;
+}
+
+// As wait_mma for two mbarriers (warp 0 polls both, then one CTA barrier).
+__device__ __forceinline__ bool wait_mma2(uint32_t mbar0, uint32_t parity0, uint32_t mbar1, uint32_t parity1,
+                                          int warp, unsigned char *smem)
+{
+    volatile int *flag = reinterpret_cast<volatile int *>(smem + SM_WAITOK);
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait(mbar0, parity0) && tc::mbar_wait(mbar1, parity1);
         if ((threadIdx.x & 31) == 0) *flag = ok ? 1 : 0;
     }
     __syncthreads();
@@ -978,21 +999,30 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         __syncthreads();
         solve_T(smem, tid);
         {
-            // T (fp32, lower, unit diagonal) -> TB fp16 rows r, K = i (8 per thread)
+            // T (fp32, lower, unit diagonal) -> T^T as fp16 rows m, K = k (8 per thread; the
+            // lanes of a warp take consecutive m, so the column reads are conflict-free)
             const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
-            const int r = tid >> 3, i0 = (tid & 7) * 8;
+            const int m = tid & 63, k0 = (tid >> 6) * 8;
             float v[8];
 #pragma unroll
             for (int u = 0; u < 8; u++) {
-                const int i = i0 + u;
-                v[u] = (i < r) ? Tm[r * AP + i] : (i == r ? 1.f : 0.f);
+                const int k = k0 + u;
+                v[u] = (k > m) ? Tm[k * AP + m] : (k == m ? 1.f : 0.f);
             }
-            st_shared_u4(sbase + SM_TB + tc::core_offset(r, i0, 64, 2), pack8_f16(v));
+            st_shared_u4(sbase + SM_TB + tc::core_offset(m, k0, 64, 2), pack8_f16(v));
         }
-        // TB and the Aqk rows of SB were written through the generic proxy; the U and O/S
-        // products read them through the async proxy (ordered by the barriers that precede
-        // their issue)
+        // T^T and the Aqk rows of SB were written through the generic proxy; the products
+        // read them through the async proxy
         tc::fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            // [Aqk; Kd^T] T -> TMEM (lane = row of SB); it runs while the inputs are staged
+            // and P is awaited
+            tc::fence_after_sync();
+            tc::gemm<0, 64, 64>(tmem + TM_W, sbase + SM_SB, SBO_SB, sbase + SM_TB, SBO64_F16, false);
+            tc::gemm<0, 64, 64>(tmem + TM_W + 64, sbase + SM_SB_KD, SBO_SB, sbase + SM_TB, SBO64_F16, false);
+            tc::commit(mbar);
+        }
 
         // ================= Phase D: the rest of the chain step =================
         // the next chunk's q, k, raw_g rows -> staging (the scratch of phase C is dead now)
@@ -1008,8 +1038,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         // the V tile (the older group) has landed for this thread; the barrier inside the
         // wait makes every thread's part of it visible
         cp_async_wait_group<1>();
-        ok &= wait_mma(mbarc, phasec, warp, smem);
+        ok &= wait_mma2(mbarc, phasec, mbar, phase, warp, smem);   // P and [Aqk; Kd^T] T
         phasec ^= 1;
+        phase ^= 1;
         // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 pairs in TMEM (rows r = 16 k4 .. +15)
         {
             const float *bet = reinterpret_cast<const float *>(smem + SM_BETA);
@@ -1029,31 +1060,29 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             tc::tmem_st8u(tlane + TM_A + (r0 >> 1), pk8);
             tc::tmem_st_wait();
         }
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            tc::gemm_ta<64, 64>(tmem + TM_P, tmem + TM_A, sbase + SM_TB, SBO64_F16, false);
-            tc::commit(mbarc);
-        }
-        ok &= wait_mma(mbarc, phasec, warp, smem);
-        phasec ^= 1;
-        // D5: U^T -> fp16 pairs in TMEM (A of the last product)
+        // D5: [Aqk T; Kd^T T] -> fp16 rows of SB, in place (the B operand of the last
+        // product); TMEM lane = row, 16 of the 64 K columns per warp
         {
+            const uint32_t sb = sbase + SM_SB;
+            const int row = 32 * (warp & 3) + lane;
             float v[16];
-            const int r0 = 16 * k4;
-            tc::tmem_ld16(tlane + TM_P + r0, v);
+            tc::tmem_ld16(tlane + TM_W + 16 * k4, v);
             tc::tmem_ld_wait();
-            uint32_t pk8[8];
-            pack_pairs<8>(v, pk8);
-            tc::tmem_st8u(tlane + TM_A + 32 + (r0 >> 1), pk8);
-            tc::tmem_st_wait();
+            st_shared_u4(sb + sb_offset(row, 16 * k4), pack8_f16(v));
+            st_shared_u4(sb + sb_offset(row, 16 * k4 + 8), pack8_f16(v + 8));
+            if ((warp & 3) >= 2) {   // lanes 64..127 of the second product: rows 128..191
+                tc::tmem_ld16(tlane + TM_W + 64 + 16 * k4, v);
+                tc::tmem_ld_wait();
+                st_shared_u4(sb + sb_offset(row + 64, 16 * k4), pack8_f16(v));
+                st_shared_u4(sb + sb_offset(row + 64, 16 * k4 + 8), pack8_f16(v + 8));
+            }
         }
+        tc::fence_proxy_async();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            tc::gemm_ta<192, 64>(tmem + TM_P + 64, tmem + TM_A + 32, sbase + SM_SB, SBO_SB, true);
+            tc::gemm_ta<192, 64>(tmem + TM_P + 64, tmem + TM_A, sbase + SM_SB, SBO_SB, true);
             tc::commit(mbarc);
         }
         // D7 (the O rows) runs in the next chunk's phase A, or below for the last chunk
