@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t mbar = sbase + SM_MBAR, mbarc = sbase + SM_MBARC;
     if (tid == 0) {
-        tc::mbar_init(mbar, 1);
+        tc::mbar_init(mbar, 2);    // two issuing threads commit to it
         tc::mbar_init(mbarc, 1);
     }
     if (tid < KD) reinterpret_cast<float *>(smem + SM_DTB)[tid] = p.dt_bias ? p.dt_bias[h * KD + tid] : 0.f;
@@ -944,9 +944,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         __syncthreads();
 
         // ================= Phase B: decay-weighted Gram blocks =================
+        // two issuing threads (in different warps), each committing its own products: one
+        // thread's tcgen05.mma issue takes longer than these small products take to run
         if (tid == 0) {
             tc::fence_after_sync();
             tc::gemm<0, 96, 128>(tmem + TM_XOFF, sbase + SM_OFFA, SBO128_F16, sbase + SM_OFFB, SBO128_F16, false);
+            tc::commit(mbar);
+        } else if (tid == 32) {
+            tc::fence_after_sync();
             if (!flagged)
                 tc::gemm<2, 64, 128>(tmem + TM_XDIAG, sbase + SM_DIAGA, SBO128_TF32, sbase + SM_DIAGB, SBO128_TF32, false);
             tc::commit(mbar);
@@ -1015,12 +1020,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         // read them through the async proxy
         tc::fence_proxy_async();
         __syncthreads();
-        if (tid == 0) {
-            // [Aqk; Kd^T] T -> TMEM (lane = row of SB); it runs while the inputs are staged
-            // and P is awaited
+        if (tid == 0 || tid == 32) {
+            // [Aqk; Kd^T] T -> TMEM (lane = row of SB), one half per issuing thread; it runs
+            // while the inputs are staged and P is awaited
             tc::fence_after_sync();
-            tc::gemm<0, 64, 64>(tmem + TM_W, sbase + SM_SB, SBO_SB, sbase + SM_TB, SBO64_F16, false);
-            tc::gemm<0, 64, 64>(tmem + TM_W + 64, sbase + SM_SB_KD, SBO_SB, sbase + SM_TB, SBO64_F16, false);
+            if (tid == 0)
+                tc::gemm<0, 64, 64>(tmem + TM_W, sbase + SM_SB, SBO_SB, sbase + SM_TB, SBO64_F16, false);
+            else
+                tc::gemm<0, 64, 64>(tmem + TM_W + 64, sbase + SM_SB_KD, SBO_SB, sbase + SM_TB, SBO64_F16, false);
             tc::commit(mbar);
         }
 
