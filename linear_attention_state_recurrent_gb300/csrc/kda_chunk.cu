@@ -116,14 +116,6 @@ __device__ __forceinline__ uint32_t sb_offset(int row, int k)
     return static_cast<uint32_t>((row >> 3) * SBO_SB + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
 }
 
-// fp32 -> bf16 bits, round to nearest even (the hardware conversion, one instruction)
-__device__ __forceinline__ uint16_t bf16_rn(float x)
-{
-    uint16_t r;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
-    return r;
-}
-
 // Packs 2*n fp32 values into n fp16 pairs (element 2i in the low half).
 template <int n>
 __device__ __forceinline__ void pack_pairs(const float *v, uint32_t (&o)[n])
@@ -692,7 +684,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         uint16_t *orow = p.out + (cs + r0) * p.ld_out + static_cast<int64_t>(h) * VD + jv;
 #pragma unroll
         for (int u = 0; u < 16; u++)
-            if (r0 + u < nrows) orow[u * p.ld_out] = bf16_rn(v[u]);
+            if (r0 + u < nrows) orow[u * p.ld_out] = f32_to_bf16(v[u]);
     };
 
     // ---- S0 -> TMEM (S^T: lane j, columns c in this thread's 32-column slice) ----

@@ -38,14 +38,12 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b)
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// fp32 -> bf16 bits, round to nearest even (inputs here are finite or +-inf).
+// fp32 -> bf16 bits, round to nearest even (the hardware conversion, one instruction)
 __device__ __forceinline__ uint16_t f32_to_bf16(float f)
 {
-    uint32_t u = __float_as_uint(f);
-    if ((u & 0x7f800000u) == 0x7f800000u)  // inf / nan: truncate, keep nan quiet
-        return static_cast<uint16_t>((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
-    u += 0x7fffu + ((u >> 16) & 1u);
-    return static_cast<uint16_t>(u >> 16);
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
 }
 
 // Two fp32 values to packed bf16 (lo in the low half), round to nearest even, one
