@@ -154,6 +154,10 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
 {
     asm volatile("st.shared.u16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
 }
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
 {
     float4 v;
@@ -192,9 +196,13 @@ __device__ __forceinline__ uint4 pack4_tf32(const float *v)
 
 // ---------------------------------------------------------------------------
 // Phase C: T = (I + A)^-1 for the strictly lower 64x64 A in AMAT (fp32, pitch AP),
-// by 16x16 diagonal-block inverses and two levels of block doubling (512 threads).
+// by 16x16 diagonal-block inverses and two levels of block doubling (512 threads). Each
+// level also writes its final entries of T, transposed and in fp16, to the T^T operand
+// tile (row m, K = k holds T[k][m]; at shared address tbt), and the six zero blocks of
+// T^T are written during the first level, so the tile is complete (and fenced for the
+// async proxy) when the solve returns. The fp32 T keeps only what later levels read.
 // ---------------------------------------------------------------------------
-__device__ void solve_T(unsigned char *smem, int tid)
+__device__ void solve_T(unsigned char *smem, int tid, uint32_t tbt)
 {
     float *A = reinterpret_cast<float *>(smem + SM_AMAT);
     float *T = reinterpret_cast<float *>(smem + SM_TMAT);
@@ -212,6 +220,15 @@ __device__ void solve_T(unsigned char *smem, int tid)
         }
 #pragma unroll
         for (int r = 0; r < 16; r++) T[(o + r) * AP + o + j] = t[r];
+        // column j of the block is row o + j of T^T, K = o .. o + 15
+        st_shared_u4(tbt + tc::core_offset(o + j, o, 64, 2), pack8_f16(t));
+        st_shared_u4(tbt + tc::core_offset(o + j, o + 8, 64, 2), pack8_f16(t + 8));
+    } else if (tid < 64 + 192) {
+        // T^T is zero where the K block precedes the row block: blocks (bm, bk) = (1, 0),
+        // (2, 0), (2, 1), (3, 0), (3, 1), (3, 2); 16 rows x two 16-byte chunks each
+        const int z = tid - 64, blk = z >> 5, rr = (z >> 1) & 15, hf = z & 1;
+        const int bm = blk < 1 ? 1 : (blk < 3 ? 2 : 3), bk = blk - bm * (bm - 1) / 2;
+        st_shared_u4(tbt + tc::core_offset(16 * bm + rr, 16 * bk + 8 * hf, 64, 2), make_uint4(0u, 0u, 0u, 0u));
     }
     __syncthreads();
     // level 2: within each 32-block p, X = A_10 T_00 then T_10 = -T_11 X (16x16)
@@ -230,6 +247,7 @@ __device__ void solve_T(unsigned char *smem, int tid)
         for (int m = 0; m < 16; m++)
             if (m <= r) y += T[(o + 16 + r) * AP + o + 16 + m] * X[(p * 16 + m) * 17 + j];
         T[(o + 16 + r) * AP + o + j] = -y;
+        st_shared_u16(tbt + tc::core_offset(o + j, o + 16 + r, 64, 2), f16_bits(-y));
     }
     __syncthreads();
     // level 3: X = A_ba T_a (32x32), T_ba = -T_b X; 2x2 output tiles on 256 threads
@@ -257,9 +275,12 @@ __device__ void solve_T(unsigned char *smem, int tid)
             y00 += t0 * x.x; y01 += t0 * x.y;
             y10 += t1 * x.x; y11 += t1 * x.y;
         }
-        *reinterpret_cast<float2 *>(T + (32 + r) * AP + j) = make_float2(-y00, -y01);
-        *reinterpret_cast<float2 *>(T + (33 + r) * AP + j) = make_float2(-y10, -y11);
+        // T_ba is final and read by no later level: only its fp16 transpose is stored, the
+        // rows 32 + r, 33 + r of columns j, j + 1 as K pairs of T^T rows j, j + 1
+        st_shared_u32(tbt + tc::core_offset(j, 32 + r, 64, 2), tc::pack_f16x2(-y00, -y10));
+        st_shared_u32(tbt + tc::core_offset(j + 1, 32 + r, 64, 2), tc::pack_f16x2(-y01, -y11));
     }
+    tc::fence_proxy_async();   // T^T is read by the products issued after the barrier
     __syncthreads();
 }
 
@@ -1002,24 +1023,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
-        solve_T(smem, tid);
-        {
-            // T (fp32, lower, unit diagonal) -> T^T as fp16 rows m, K = k (8 per thread; the
-            // lanes of a warp take consecutive m, so the column reads are conflict-free)
-            const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
-            const int m = tid & 63, k0 = (tid >> 6) * 8;
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int k = k0 + u;
-                v[u] = (k > m) ? Tm[k * AP + m] : (k == m ? 1.f : 0.f);
-            }
-            st_shared_u4(sbase + SM_TB + tc::core_offset(m, k0, 64, 2), pack8_f16(v));
-        }
-        // T^T and the Aqk rows of SB were written through the generic proxy; the products
-        // read them through the async proxy
-        tc::fence_proxy_async();
-        __syncthreads();
+        // T^T (fp16) is complete and fenced when the solve returns; the Aqk rows of SB were
+        // written before the solve's barriers and fenced at its end as well
+        solve_T(smem, tid, sbase + SM_TB);
         if (tid == 0 || tid == 32) {
             // [Aqk; Kd^T] T -> TMEM (lane = row of SB), one half per issuing thread; it runs
             // while the inputs are staged and P is awaited
