@@ -76,7 +76,9 @@ constexpr uint32_t SM_MBAR = SM_NRM + 1024;    // mbarrier of the Gram-block MMA
 constexpr uint32_t SM_MBARC = SM_MBAR + 8;     // mbarrier of the chain MMAs
 constexpr uint32_t SM_TMEMP = SM_MBARC + 8;
 constexpr uint32_t SM_WAITOK = SM_TMEMP + 4;
-constexpr uint32_t SMEM_BYTES = SM_WAITOK + 4;
+constexpr uint32_t SM_MBARW = SM_WAITOK + 4;   // mbarrier of the [Aqk; Kd^T] T products
+constexpr uint32_t SMEM_BYTES = SM_MBARW + 8;
+static_assert(SM_MBARW % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(SM_TAB + 4 * 7 * 128 * 4 <= SM_SB_KD, "constants table overlaps Kd^T");
 // phase C aliases
@@ -104,6 +106,7 @@ constexpr uint32_t TM_XDIAG = 352;// 64 columns
 constexpr uint32_t TM_A = 416;    // A operands of the chain MMAs, fp16 packed in pairs:
                                   // S^T (64 columns), then (beta Y)^T at +0
 constexpr uint32_t TM_W = TM_XOFF;// [Aqk; Kd^T] T: rows 0..127 (64 columns), rows 64..191 (64)
+constexpr uint32_t TM_XDIAG2 = TM_P;  // the diagonal product's channels 64..127 (P is issued after assembly)
 
 // stride byte offsets of the operand tiles
 constexpr uint32_t SBO128_F16 = 128 * 2 * 8;  // K = 128 fp16
@@ -344,7 +347,13 @@ __device__ void assemble_slice(unsigned char *smem, uint32_t tlane, int warp, in
     tc::tmem_ld16(tlane + TM_XOFF + (k4 < s0 ? off_b_base(s0) + i0 : 0), off0);
     tc::tmem_ld16(tlane + TM_XOFF + (k4 < s0 + 1 ? off_b_base(s0 + 1) + i0 : 0), off1);
     tc::tmem_ld16(tlane + TM_XDIAG + i0, dg);
-    tc::tmem_ld_wait();
+    {
+        float dg2[16];   // the diagonal product's second channel half
+        tc::tmem_ld16(tlane + TM_XDIAG2 + i0, dg2);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 16; u++) dg[u] += dg2[u];
+    }
     if (flagged && k4 == s) {
         // the diagonal block, computed pairwise by flagged_diag (entries i > r are not
         // written there and are masked below)
@@ -669,9 +678,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     const int64_t HK = static_cast<int64_t>(H) * KD;
 
     const uint32_t sbase = tc::smem_addr(smem);
-    const uint32_t mbar = sbase + SM_MBAR, mbarc = sbase + SM_MBARC;
+    const uint32_t mbar = sbase + SM_MBAR, mbarc = sbase + SM_MBARC, mbarw = sbase + SM_MBARW;
     if (tid == 0) {
-        tc::mbar_init(mbar, 2);    // two issuing threads commit to it
+        tc::mbar_init(mbar, 3);    // number of issuing threads that commit to each
+        tc::mbar_init(mbarw, 2);
         tc::mbar_init(mbarc, 1);
     }
     if (tid < KD) reinterpret_cast<float *>(smem + SM_DTB)[tid] = p.dt_bias ? p.dt_bias[h * KD + tid] : 0.f;
@@ -681,7 +691,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEMP);
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // this warp's lanes
-    uint32_t phase = 0, phasec = 0;
+    uint32_t phase = 0, phasec = 0, phasew = 0;
     bool ok = true;
     bool os_pending = false;   // the last product (O and S) of the previous chunk is in flight
 
@@ -965,20 +975,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         __syncthreads();
 
         // ================= Phase B: decay-weighted Gram blocks =================
-        // two issuing threads (in different warps), each committing its own products: one
-        // thread's tcgen05.mma issue takes longer than these small products take to run
+        // three issuing threads (in different warps), each committing its own products: one
+        // thread's tcgen05.mma issue takes longer than these small products take to run.
+        // The tf32 diagonal product is split by channels (0..63, 64..127) into two
+        // accumulators that the row assembly adds.
         if (tid == 0) {
             tc::fence_after_sync();
             tc::gemm<0, 96, 128>(tmem + TM_XOFF, sbase + SM_OFFA, SBO128_F16, sbase + SM_OFFB, SBO128_F16, false);
             tc::commit(mbar);
-        } else if (tid == 32) {
+        } else if (tid == 32 || tid == 64) {
             tc::fence_after_sync();
+            // channel c's 16-byte K chunk sits at (c / 4) * 128 bytes: channels 64.. at 2048
+            const uint32_t koff = tid == 32 ? 0u : 2048u;
             if (!flagged)
-                tc::gemm<2, 64, 128>(tmem + TM_XDIAG, sbase + SM_DIAGA, SBO128_TF32, sbase + SM_DIAGB, SBO128_TF32, false);
+                tc::gemm<2, 64, 64>(tmem + (tid == 32 ? TM_XDIAG : TM_XDIAG2), sbase + SM_DIAGA + koff, SBO128_TF32,
+                                    sbase + SM_DIAGB + koff, SBO128_TF32, false);
             tc::commit(mbar);
         }
         // D1 while the Gram MMAs run: S^T -> fp16 pairs in TMEM (A of P), and
-        // TMEM S^T <- S^T Diag(e^{b_last}); then issue P = S^T [K^G; Q^G]^T behind them.
+        // TMEM S^T <- S^T Diag(e^{b_last}).
         {
             const float *gc = reinterpret_cast<const float *>(smem + SM_GC);
             float v[2][16];
@@ -1000,17 +1015,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
             }
             tc::tmem_st_wait();
         }
-        // one barrier both orders every thread's S^T operand before the P issue and ends
-        // the Gram wait (P queues behind the Gram MMAs in the tensor pipe anyway)
+        // the barrier ends the Gram wait and orders every thread's S^T operand before the
+        // P issue (after the row assembly, which reads the second diagonal accumulator)
         tc::fence_before_sync();
         ok &= wait_mma(mbar, phase, warp, smem);
         phase ^= 1;
-        if (tid == 0) {
-            tc::gemm_ta<128, 128>(tmem + TM_P, tmem + TM_A, sbase + SM_PB, SBO128_F16, false);
-            tc::commit(mbarc);
-        }
 
-        // ================= Phase C: A, Aqk, T (the P product is in flight) =================
+        // ================= Phase C: A, Aqk, T (the P product is issued after assembly) =================
         // The V tile (read in D3) overlays the diagonal B operand (consumed by now) or, on
         // the pairwise path, the stash (dead once flagged_diag has run).
         const uint16_t *vsrc = p.qkv + c0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD;
@@ -1023,6 +1034,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         assemble_slice(smem, tlane, warp, lane, flagged);
         tc::fence_before_sync();
         __syncthreads();
+        if (tid == 64) {
+            // P = S^T [K^G; Q^G]^T (overwrites the second diagonal accumulator, read above);
+            // it runs during the solve
+            tc::fence_after_sync();
+            tc::gemm_ta<128, 128>(tmem + TM_P, tmem + TM_A, sbase + SM_PB, SBO128_F16, false);
+            tc::commit(mbarc);
+        }
         // T^T (fp16) is complete and fenced when the solve returns; the Aqk rows of SB were
         // written before the solve's barriers and fenced at its end as well
         solve_T(smem, tid, sbase + SM_TB);
@@ -1034,7 +1052,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
                 tc::gemm<0, 64, 64>(tmem + TM_W, sbase + SM_SB, SBO_SB, sbase + SM_TB, SBO64_F16, false);
             else
                 tc::gemm<0, 64, 64>(tmem + TM_W + 64, sbase + SM_SB_KD, SBO_SB, sbase + SM_TB, SBO64_F16, false);
-            tc::commit(mbar);
+            tc::commit(mbarw);
         }
 
         // ================= Phase D: the rest of the chain step =================
@@ -1051,9 +1069,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
         // the V tile (the older group) has landed for this thread; the barrier inside the
         // wait makes every thread's part of it visible
         cp_async_wait_group<1>();
-        ok &= wait_mma2(mbarc, phasec, mbar, phase, warp, smem);   // P and [Aqk; Kd^T] T
+        ok &= wait_mma2(mbarc, phasec, mbarw, phasew, warp, smem);   // P and [Aqk; Kd^T] T
         phasec ^= 1;
-        phase ^= 1;
+        phasew ^= 1;
         // D3: (beta Y)^T = beta (V - K^G S)^T -> fp16 pairs in TMEM (rows r = 16 k4 .. +15)
         {
             const float *bet = reinterpret_cast<const float *>(smem + SM_BETA);
