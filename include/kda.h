@@ -52,7 +52,9 @@
  *    traps. Two entries naming the same writable slot in one call is a caller
  *    error with an unspecified result.
  *  - Sizes: H >= 1, K and V in {32, 64, 128}. The pool must be 16-byte aligned and
- *    slot_stride a multiple of 4.
+ *    slot_stride a multiple of 4. One call is one launch: it covers at most
+ *    (2^31 - 1) / (4 H) entries (sequences or requests); a larger batch returns
+ *    KDA_ERR_UNSUPPORTED and is split by the caller.
  *  - Return value: KDA_OK, or an error code with a message in kda_last_error().
  *    All argument checks happen on the host before any launch; on error nothing
  *    is enqueued. A zero-sized call (N == 0 / no entries) returns KDA_OK and

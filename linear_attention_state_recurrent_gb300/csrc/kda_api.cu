@@ -1,6 +1,7 @@
 // extern "C" entry points of libkda (declared in include/kda.h): host-side
 // argument checks, then kernel launches on the caller's stream. Nothing here
 // allocates, synchronises or keeps state between calls.
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -113,6 +114,18 @@ int check_state(const kda_state *st, const kda_heads *hd)
     if (st->null_slot < -1 || st->null_slot >= st->num_slots)
         return fail(KDA_ERR_INVALID_ARGUMENT, "null_slot must be -1 or in [0, num_slots) (got %d)",
                     st->null_slot);
+    return KDA_OK;
+}
+
+// One launch covers a call: its grid has at most four CTAs per (entry, head) (the 32-column
+// V slices) and the grid's x dimension holds at most 2^31 - 1 blocks.
+int check_entry_count(int64_t entries, const kda_heads *hd)
+{
+    const int64_t per_entry = static_cast<int64_t>(hd->H) * 4;
+    if (entries > INT32_MAX / per_entry)
+        return fail(KDA_ERR_UNSUPPORTED,
+                    "%lld entries x %d heads exceed one launch (at most %lld entries at this H): split the call",
+                    (long long)entries, hd->H, (long long)(INT32_MAX / per_entry));
     return KDA_OK;
 }
 
@@ -231,6 +244,7 @@ int kda_packed_decode(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t 
     if ((s = check_rows(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, out, ld_out, heads))) return s;
     if ((s = check_state(state, heads))) return s;
     if (num_seqs < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs must be >= 0");
+    if ((s = check_entry_count(num_seqs, heads))) return s;
     if (num_seqs == 0) return ok();
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
@@ -252,6 +266,7 @@ int kda_spec_verify(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
     if (num_reqs < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "num_reqs must be >= 0");
     if (tokens_per_req < 1 || tokens_per_req > 64)
         return fail(KDA_ERR_INVALID_ARGUMENT, "tokens_per_req must be in 1..64 (got %d)", tokens_per_req);
+    if ((s = check_entry_count(num_reqs, heads))) return s;
     if (num_reqs == 0) return ok();
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
@@ -290,6 +305,7 @@ int kda_spec_verify_checkpoints(const uint16_t *mixed_qkv, int64_t ld_qkv, const
                     static_cast<long long>(state->index_stride), tokens_per_req);
     if (num_accepted && !aligned(num_accepted, 4))
         return fail(KDA_ERR_INVALID_ARGUMENT, "num_accepted must be 4-byte aligned");
+    if ((s = check_entry_count(num_reqs, heads))) return s;
     if (num_reqs == 0) return ok();
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
@@ -320,6 +336,7 @@ static int fused_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
         return fail(KDA_ERR_INVALID_ARGUMENT, "dt_bias must be 16-byte aligned");
     kda::TailParams tp;
     if ((s = make_tail(conv, norm, heads, &tp))) return s;
+    if ((s = check_entry_count(num_entries, heads))) return s;
     if (num_entries == 0) return ok();
     kda::Params p = make_params(mixed_qkv, ld_qkv, raw_g, ld_g, raw_beta, ld_beta, heads, state,
                                 out, ld_out, err_flags);
@@ -389,6 +406,7 @@ static int chunk_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
                     "%s: mixed_qkv, raw_g and out must be 16-byte aligned with ld_qkv, ld_g and ld_out "
                     "multiples of 8", name);
     const int64_t n = num_decodes + num_prefills;
+    if ((s = check_entry_count(n, heads))) return s;
     if (n == 0) return ok();
     if (!cu_seqlens) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
     if ((s = check_cu_host(cu_seqlens_host, n))) return s;

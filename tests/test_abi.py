@@ -215,3 +215,28 @@ def test_spec_checkpoint_validation(kda):
 def test_bounded_wait_selftest_needs_an_error_word(kda):
     assert kda.lib.kda_selftest_bounded_wait(None, None) == 1
     assert "err_flags" in kda.last_error()
+
+
+def test_oversized_batches_are_refused_before_launch(kda):
+    """One call is one launch: more entries than a grid can hold (4 CTAs per entry and head,
+    at most 2^31 - 1 blocks) is refused with KDA_ERR_UNSUPPORTED instead of being cut short."""
+    hd, st = _heads(kda), _state(kda)
+    limit = (2 ** 31 - 1) // (4 * hd.H)
+    too_many = limit + 1
+    assert _decode(kda, hd, st, N=too_many) == 2 and "split the call" in kda.last_error()
+    s = kda.lib.kda_spec_verify(FAKE, 768, FAKE, 256, FAKE, 2, too_many, 8, ctypes.byref(hd),
+                                ctypes.byref(st), FAKE, 256, None, None)
+    assert s == 2 and "split the call" in kda.last_error()
+    st8 = _state(kda, index_stride=8)
+    s = kda.lib.kda_spec_verify_checkpoints(FAKE, 768, FAKE, 256, FAKE, 2, too_many, 8, None,
+                                            ctypes.byref(hd), ctypes.byref(st8), FAKE, 256, None, None)
+    assert s == 2 and "split the call" in kda.last_error()
+    assert _fused(kda, hd, st, N=too_many) == 2 and "split the call" in kda.last_error()
+    for nd, npf in ((too_many, 0), (0, too_many), (limit, 1)):
+        s = kda.lib.kda_mixed_batch(FAKE, 768, FAKE, 256, FAKE, 2, FAKE, None, nd, npf,
+                                    ctypes.byref(hd), ctypes.byref(st), None, 0, FAKE, 256, None, None)
+        assert s == 2 and "split the call" in kda.last_error()
+    # at the limit the count itself is accepted (the call then fails on its NULL host cu_seqlens)
+    s = kda.lib.kda_chunk_prefill(FAKE, 768, FAKE, 256, FAKE, 2, FAKE, None, limit, 64,
+                                  ctypes.byref(hd), ctypes.byref(st), None, 0, FAKE, 256, None, None)
+    assert s == 1 and "split the call" not in kda.last_error()
