@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(const __grid_constant__ Ar
 
         // ================= Phase A: gate, norms, cumulative decay, operands =================
         // staged inputs of this chunk (copied during the previous chain step); the same
-        // barrier ends the previous chunk and carries its timeout verdict
+        // barrier ends the previous chunk and carries its timeout result
         cp_async_wait_all();
         if (__syncthreads_or(ok ? 0 : 1)) {
             ok = false;
