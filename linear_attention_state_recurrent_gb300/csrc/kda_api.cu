@@ -424,7 +424,7 @@ static int chunk_common(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_
                                 out, ld_out, err_flags);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(kda::launch_mixed(p, heads->K, heads->V, cu_seqlens, cu_seqlens_host,
-                                         num_decodes, num_prefills, st),
+                                         num_decodes, num_prefills, workspace, st),
                        "mixed batch launch");
 }
 

@@ -38,10 +38,10 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
 // The bounded-wait self-test (one CTA waits on an mbarrier nothing arrives at).
 cudaError_t launch_bounded_wait_selftest(uint32_t *err, cudaStream_t stream);
 
-// Mixed batch: decodes are entries [0, num_decodes) (length 1), prefills the next
-// num_prefills entries. At K = V = 128 one launch runs both (the decodes on worker CTAs
-// beside the prefill chains); otherwise the recurrent and chunk launches run in turn.
+// Mixed batch: decodes are entries [0, num_decodes) (length 1) and take the packed-decode
+// kernel; prefills are the next num_prefills entries and take the chunk path.
 cudaError_t launch_mixed(const Params &p, int K, int V, const int32_t *cu, const int32_t *cu_host,
-                         int64_t num_decodes, int64_t num_prefills, cudaStream_t stream);
+                         int64_t num_decodes, int64_t num_prefills, void *workspace,
+                         cudaStream_t stream);
 
 }  // namespace kda

@@ -102,6 +102,23 @@ __device__ __forceinline__ void gemm_ta(uint32_t d_tmem, uint32_t a_tmem, uint32
     }
 }
 
+// D[M=128, N] (+)= A[128, Kd] * B[N, Kd]^T in tf32 with A in tensor memory (one 32-bit
+// column per K element: one K step of 8 spans 8 columns) and B in shared memory.
+template <int N, int KD>
+__device__ __forceinline__ void gemm_ta_tf32(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr, uint32_t b_sbo,
+                                             bool accumulate)
+{
+    constexpr uint32_t ID = instr_desc(2, 128, N);
+#pragma unroll
+    for (int ks = 0; ks < KD / 8; ks++) {
+        const uint64_t db = smem_desc(b_saddr + ks * 256, 128, b_sbo);
+        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+        asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                     " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
+                     :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(ID), "r"(acc));
+    }
+}
+
 __device__ __forceinline__ void commit(uint32_t mbar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -139,6 +156,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
         if (it == 0) start = global_ns();
         else if ((it & 255u) == 0 && global_ns() - start > 2000000000ull) return false;
     }
+}
+
+// Arms an mbarrier for one arrival that also expects `bytes` of asynchronous copies.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(mbar), "r"(bytes) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// this CTA's shared memory; completion is counted on `mbar` in bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
 // TMEM allocation by one full warp; the base address is written to *dst (smem).
@@ -190,6 +221,13 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
                  :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
                     "r"(v[6]), "r"(v[7])
                  : "memory");
+}
+
+// 4 consecutive 32-bit columns of this thread's TMEM lane (warp-collective)
+__device__ __forceinline__ void tmem_st4u(uint32_t taddr, const uint32_t (&v)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
