@@ -29,27 +29,25 @@
 //                   [O^T | S^T] += Y^T [M1; M2]^T         M=128 N=192 K=64   fp16
 //                 with S^T pre-scaled by gamma, the records streamed in by bulk copies two
 //                 chunks ahead.
-// A chunk where some channel decays by more than 40 nats within half a 16-row block (or
-// 80 within a block) leaves the tensor-core Gram path: the prep CTA lists it and
-// exact_kernel recomputes its record in fp32 on the CUDA cores.
 //
 // The decay-weighted Gram matrices are split into 16-row blocks s = 0..3 with prefixes
-// P_s = b at the last row before block s. Off-diagonal blocks are computed in fp16 with
-// a reference point between the two rows, so both factors are <= 1 (a factor that
-// underflows only drops a term that is itself below 2^-24):
-//   block (1,0): reference P_1;  blocks (2|3, 0|1): reference P_2;  block (3,2): P_3,
-//   X_off = OFFA OFFB^T  with OFFA = [K^e; Q^e] rows (16..31 @P_1, 32..63 @P_2, and
-//   48..63 @P_3 on lanes 0..15) and OFFB = [rows 0..31 @P_2; rows 0..15 @P_1; rows
-//   32..47 @P_3]  (M=128 N=64 K=128, A in tensor memory).
-// Diagonal blocks use the block's eighth row as reference, whose factors reach e^{40},
-// in tf32:  X_diag = [K^L; Q^L] (K^R)^T  (M=128 N=64, K=128 in two channel halves, A in
-// tensor memory).
+// P_s = b at the last row before block s (P_0 = 0). Every row carries its own block's
+// reference, so the A operand is one tile for both products:
+//   A_op = [K^e; Q^e],  K^e_r = k^_r e^{b_r - P_s(r)} (<= 1)      (tf32, in tensor memory)
+// Diagonal blocks:      X_diag = A_op (K^R)^T,  K^R_i = k^_i e^{P_s(i) - b_i}   (>= 1)
+// Off-diagonal blocks:  X_off  = A_op [B_1; B_2; B_3]^T,  B_R = rows i < 16R at
+//                       k^_i e^{P_R - b_i} (<= 1), for the rows of block R.
+// K^R reaches e^{(decay over the block)}, which tf32 (fp32 range) holds while a block's
+// decay stays below 80 nats; a channel half in which some channel decays more within a
+// block computes its share of the diagonal blocks pairwise in fp32 instead.
 //
 // fp16 (11-bit significand, round to nearest) carries the same precision as tf32 with
 // round to nearest; bf16 operands would exceed the 2e-3 relative error bar.
 #include <algorithm>
 #include <numeric>
 #include <vector>
+
+#include <cuda_fp16.h>
 
 #include "kda_common.cuh"
 #include "kda_launch.h"
@@ -61,12 +59,11 @@ namespace chunk {
 constexpr int C = 64;
 constexpr int KD = 128;
 constexpr int VD = 128;
-constexpr int PT = 256;          // prep / exact threads
+constexpr int PT = 256;          // prep threads
 constexpr int CT = 256;          // chain threads
 constexpr int kMaxSeqs = 1024;   // sequences per launch (the host splits larger calls)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kHalfSpan2 = 40.f * kLog2e;    // largest half-block decay of the tf32 path (log2 units)
-constexpr float kBlockSpan2 = 80.f * kLog2e;   // largest block decay of the factored path
+constexpr float kBlockSpan2 = 80.f * kLog2e;   // largest in-block decay of the tf32 diagonal path (log2 units)
 
 // ---- one (chunk, head) record in the workspace ----
 constexpr uint32_t REC_KQG = 0;        // fp16 [128 rows][128] K-major, SBO 2048: K^G rows 0..63, Q^G 64..127
@@ -89,12 +86,13 @@ constexpr uint32_t SBO_SB = SBO64_F16 + 16;
 // ---- prep shared memory (bytes) ----
 constexpr uint32_t SM_G = 0;            // bf16 [64][128] raw_g, 16-byte chunks XOR-swizzled by row
 constexpr uint32_t SM_BH = 16384;       // fp32 [64][64]  b (log2 units) of the current channel half, swizzled
-constexpr uint32_t SM_OFFB = 32768;     // fp16 [64][128] off-diagonal B operand (SBO 2048)
-constexpr uint32_t SM_DIAGB = 49152;    // tf32 [64][64]  K^R of the current channel half (SBO 2048)
-constexpr uint32_t SM_SB = 65536;       // fp16 [192][64] Aqk rows 0..63, Kd^T rows 64..191 (SBO 1040)
+constexpr uint32_t SM_BOFF = 32768;     // tf32 [96][64]  [B_1; B_2; B_3] of the current half (SBO 2048)
+constexpr uint32_t SM_BDIAG = 57344;    // tf32 [64][64]  K^R of the current half (SBO 2048); on the
+                                        // pairwise path: fp16 [64][64] k^ then q^ (swizzled)
+constexpr uint32_t SM_SB = 73728;       // fp16 [192][64] Aqk rows 0..63, Kd^T rows 64..191 (SBO 1040)
 constexpr uint32_t SM_TAB = SM_SB + 24 * SBO_SB;   // fp32 [4 blocks][8][64] per-(block, channel) constants
-constexpr uint32_t SM_TOT = SM_TAB + 8192;         // fp32 [4][64] block sums of g
-constexpr uint32_t SM_NRM = SM_TOT + 1024;         // fp32 [2][128] half-row |k|^2, |q|^2
+constexpr uint32_t SM_TOT = SM_TAB + 8192;         // fp32 [8][64] sums of g over 8-row octets
+constexpr uint32_t SM_NRM = SM_TOT + 2048;         // fp32 [2][128] half-row |k|^2, |q|^2
 constexpr uint32_t SM_BETA = SM_NRM + 1024;        // fp32 [64]
 constexpr uint32_t SM_MBAR = SM_BETA + 256;        // mbarrier of the MMAs (two committing threads)
 constexpr uint32_t SM_TMEMP = SM_MBAR + 8;
@@ -102,35 +100,36 @@ constexpr uint32_t SM_WAITOK = SM_TMEMP + 4;
 constexpr uint32_t PREP_SMEM = SM_WAITOK + 4;
 static_assert(SM_MBAR % 8 == 0, "mbarrier alignment");
 static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two prep CTAs per SM");
-// solve-phase aliases over SM_G .. SM_DIAGB (dead once the Gram products are done)
+// solve-phase aliases over SM_G .. SM_BDIAG (dead once the Gram products are done)
 constexpr uint32_t SM_AMAT = 0;        // fp32 [64][68]
 constexpr uint32_t SM_TMAT = 17408;    // fp32 [64][68]
 constexpr uint32_t SM_XTMP = 34816;    // fp32 scratch (<= 4608 B)
 constexpr uint32_t SM_TT = 40960;      // fp16 [64][64] (T diag(beta))^T, K-major SBO 1024
+constexpr uint32_t SM_XD = 49152;      // fp32 [2][64][16] pairwise diagonal blocks (read before the solve)
 constexpr int AP = 68;                 // fp32 row pitch of AMAT / TMAT
-static_assert(SM_TT + 8192 <= SM_SB, "solve scratch overlaps SB");
+static_assert(SM_XD + 8192 <= SM_SB, "solve scratch overlaps SB");
 
 // ---- prep tensor memory columns (256) ----
-constexpr uint32_t TM_XOFF = 0;     // 64 columns
-constexpr uint32_t TM_XDIAG = 64;   // 64 columns
-constexpr uint32_t TM_OFFA = 128;   // fp16 A operand of X_off, packed pairs (64 columns)
-constexpr uint32_t TM_DIAGA = 192;  // tf32 A operand of X_diag, current channel half (64 columns)
+constexpr uint32_t TM_XOFF = 0;     // X_off   96 columns
+constexpr uint32_t TM_XDIAG = 96;   // X_diag  64 columns
+constexpr uint32_t TM_A = 160;      // tf32 A operand [K^e; Q^e] of the current channel half (64 columns)
 constexpr uint32_t TM_W1 = 0;       // [Aqk; Kd^T rows 0..63] T diag(beta)   (after assembly)
 constexpr uint32_t TM_W2 = 64;      // Kd^T T diag(beta)
 
-// per-(block, channel) constants (log2 units for prefixes)
-enum Tab { kP0 = 0, kP1 = 1, kTL = 2, kTR = 3, kE = 4, kD4 = 5, kDa = 6 };
+// per-(block, channel) constants, [block][constant][channel of the half]
+enum Tab { kP1 = 1, kE = 2, kBD = 3, kD4 = 4, kD2 = 5, kD3 = 6 };   // kP1: the block's log2 decay
+
+__device__ __forceinline__ uint32_t off_b_base(int R) { return R == 1 ? 0 : (R == 2 ? 16 : 48); }
 
 struct Args {
     Params p;
     const int32_t *cu;         // device cu_seqlens (entries)
     int64_t entry_base;        // first entry of this launch
     int32_t num_seqs;
-    int32_t num_decodes;       // (unused by the prefill kernels)
+    int32_t pf_stride;         // prep: the unit whose inputs a CTA prefetches into L2 (bid + pf_stride)
     unsigned char *rec;        // records of this launch: (chunk, head) at (cb + j) * H + h
-    uint32_t *flag_count;      // chunks that left the tensor-core Gram path
-    uint32_t *flag_list;
     int32_t cb[kMaxSeqs + 1];  // chunk prefix over the launch's sequences
+    int32_t rs[kMaxSeqs + 1];  // row starts of the launch's sequences (the host copy of cu_seqlens)
     int32_t order[kMaxSeqs];   // chain order: longest sequence first
 };
 
@@ -174,9 +173,13 @@ __device__ __forceinline__ uint4 pack8_f16(const float *v)
     return make_uint4(tc::pack_f16x2(v[0], v[1]), tc::pack_f16x2(v[2], v[3]),
                       tc::pack_f16x2(v[4], v[5]), tc::pack_f16x2(v[6], v[7]));
 }
+// fp32 -> tf32 operand, rounded to nearest with ties away from zero: the tensor core reads
+// the top 19 bits, so adding half a unit of the kept significand (bit 12) to the pattern
+// rounds the magnitude, carrying into the exponent where the significand overflows.
+__device__ __forceinline__ uint32_t tf32_rna(float x) { return __float_as_uint(x) + 0x1000u; }
 __device__ __forceinline__ uint4 pack4_tf32(const float *v)
 {
-    return make_uint4(tc::to_tf32(v[0]), tc::to_tf32(v[1]), tc::to_tf32(v[2]), tc::to_tf32(v[3]));
+    return make_uint4(tf32_rna(v[0]), tf32_rna(v[1]), tf32_rna(v[2]), tf32_rna(v[3]));
 }
 __device__ __forceinline__ void unpack_bf16x8(uint4 u, float *f)
 {
@@ -193,7 +196,7 @@ __device__ __forceinline__ uint32_t st_off(int r, int ch) { return static_cast<u
 // byte offset of fp32 element (r, c) of the [64][64] b tile (16-byte chunks swizzled by row)
 __device__ __forceinline__ uint32_t bh_off(int r, int c)
 {
-    return static_cast<uint32_t>(r * 256 + ((((c >> 2) ^ (r & 15))) << 4) + (c & 3) * 4);
+    return static_cast<uint32_t>(r * 256 + ((((c >> 2) ^ (r & 7))) << 4) + (c & 3) * 4);
 }
 // byte offset of fp16 element (row, k) of SB (K = 64, padded block stride SBO_SB)
 __device__ __forceinline__ uint32_t sb_offset(int row, int k)
@@ -231,6 +234,66 @@ __device__ __forceinline__ bool cta_wait(uint32_t mbar, uint32_t parity, unsigne
     return ok;
 }
 
+// ---------------------------------------------------------------------------
+// packed fp32x2 arithmetic: one instruction for two values
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " sub.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+// d = a * b, d = a - b and d = a * s over 8 values
+__device__ __forceinline__ void mul8(float *d, const float *a, const float *b)
+{
+#pragma unroll
+    for (int o = 0; o < 8; o += 2) {
+        const float2 v = fmul2(make_float2(a[o], a[o + 1]), make_float2(b[o], b[o + 1]));
+        d[o] = v.x; d[o + 1] = v.y;
+    }
+}
+__device__ __forceinline__ void sub8(float *d, const float *a, const float *b)
+{
+#pragma unroll
+    for (int o = 0; o < 8; o += 2) {
+        const float2 v = fsub2(make_float2(a[o], a[o + 1]), make_float2(b[o], b[o + 1]));
+        d[o] = v.x; d[o + 1] = v.y;
+    }
+}
+__device__ __forceinline__ void scale8(float *d, const float *a, float sc)
+{
+#pragma unroll
+    for (int o = 0; o < 8; o += 2) {
+        const float2 v = fmul2(make_float2(a[o], a[o + 1]), make_float2(sc, sc));
+        d[o] = v.x; d[o + 1] = v.y;
+    }
+}
 // ---------------------------------------------------------------------------
 // T = (I + A)^-1 for the strictly lower 64x64 A in AMAT (fp32, pitch AP) by 16x16
 // diagonal-block inverses and two levels of block doubling (256 threads). Each level
@@ -272,60 +335,113 @@ __device__ void solve_T(unsigned char *smem, int tid, uint32_t tbt, const float 
         st_shared_u4(tbt + tc::core_offset(16 * bm + rr, 16 * bk + 8 * hf, 64, 2), make_uint4(0u, 0u, 0u, 0u));
     }
     __syncthreads();
-    // level 2: within each 32-block p, X = A_10 T_00 then T_10 = -T_11 X (16x16)
+    // level 2: within each 32-block p, X = A_10 T_00 then T_10 = -T_11 X (16x16); each
+    // thread owns two adjacent columns (packed fp32x2 arithmetic)
+    {
+        const int p = tid >> 7, r = (tid >> 3) & 15, j = (tid & 7) * 2, o = 32 * p;
+        float2 x = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int it = 0; it < 2; it++) {
-        const int id = tid + 256 * it, p = id >> 8, r = (id >> 4) & 15, j = id & 15, o = 32 * p;
-        float x = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m++) x += A[(o + 16 + r) * AP + o + m] * T[(o + m) * AP + o + j];
-        X[(p * 16 + r) * 17 + j] = x;
+        for (int m = 0; m < 16; m++) {
+            const float a = A[(o + 16 + r) * AP + o + m];
+            x = ffma2(make_float2(a, a), *reinterpret_cast<const float2 *>(T + (o + m) * AP + o + j), x);
+        }
+        *reinterpret_cast<float2 *>(X + (p * 16 + r) * 18 + j) = x;
     }
     __syncthreads();
+    {
+        const int p = tid >> 7, r = (tid >> 3) & 15, j = (tid & 7) * 2, o = 32 * p;
+        float2 y = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int it = 0; it < 2; it++) {
-        const int id = tid + 256 * it, p = id >> 8, r = (id >> 4) & 15, j = id & 15, o = 32 * p;
-        float y = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m++)
-            if (m <= r) y += T[(o + 16 + r) * AP + o + 16 + m] * X[(p * 16 + m) * 17 + j];
-        T[(o + 16 + r) * AP + o + j] = -y;
-        st_shared_u16(tbt + tc::core_offset(o + j, o + 16 + r, 64, 2), f16_bits(-y * beta[o + j]));
+        for (int m = 0; m < 16; m++) {
+            if (m <= r) {
+                const float t = T[(o + 16 + r) * AP + o + 16 + m];
+                y = ffma2(make_float2(t, t), *reinterpret_cast<const float2 *>(X + (p * 16 + m) * 18 + j), y);
+            }
+        }
+        *reinterpret_cast<float2 *>(T + (o + 16 + r) * AP + o + j) = make_float2(-y.x, -y.y);
+        st_shared_u16(tbt + tc::core_offset(o + j, o + 16 + r, 64, 2), f16_bits(-y.x * beta[o + j]));
+        st_shared_u16(tbt + tc::core_offset(o + j + 1, o + 16 + r, 64, 2), f16_bits(-y.y * beta[o + j + 1]));
     }
     __syncthreads();
-    // level 3: X = A_ba T_a (32x32), T_ba = -T_b X; 2x2 output tiles
+    // level 3: X = A_ba T_a (32x32), T_ba = -T_b X; 2x2 output tiles, rows in packed pairs
     {
         const int r = (tid >> 4) * 2, j = (tid & 15) * 2;
-        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+        float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
         for (int m = j; m < 32; m++) {           // T_a is lower triangular: m >= j
             const float a0 = A[(32 + r) * AP + m], a1 = A[(33 + r) * AP + m];
-            const float2 t = *reinterpret_cast<const float2 *>(T + m * AP + j);
-            const float t1 = (m >= j + 1) ? t.y : 0.f;
-            x00 += a0 * t.x; x01 += a0 * t1;
-            x10 += a1 * t.x; x11 += a1 * t1;
+            float2 t = *reinterpret_cast<const float2 *>(T + m * AP + j);
+            if (m < j + 1) t.y = 0.f;
+            x0 = ffma2(make_float2(a0, a0), t, x0);
+            x1 = ffma2(make_float2(a1, a1), t, x1);
         }
-        *reinterpret_cast<float2 *>(X + r * 36 + j) = make_float2(x00, x01);
-        *reinterpret_cast<float2 *>(X + (r + 1) * 36 + j) = make_float2(x10, x11);
+        *reinterpret_cast<float2 *>(X + r * 36 + j) = x0;
+        *reinterpret_cast<float2 *>(X + (r + 1) * 36 + j) = x1;
     }
     __syncthreads();
     {
         const int r = (tid >> 4) * 2, j = (tid & 15) * 2;
-        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+        float2 y0 = make_float2(0.f, 0.f), y1 = make_float2(0.f, 0.f);
         for (int m = 0; m <= r + 1; m++) {       // T_b is lower triangular: m <= row
             const float t0 = (m <= r) ? T[(32 + r) * AP + 32 + m] : 0.f;
             const float t1 = T[(33 + r) * AP + 32 + m];
             const float2 x = *reinterpret_cast<const float2 *>(X + m * 36 + j);
-            y00 += t0 * x.x; y01 += t0 * x.y;
-            y10 += t1 * x.x; y11 += t1 * x.y;
+            y0 = ffma2(make_float2(t0, t0), x, y0);
+            y1 = ffma2(make_float2(t1, t1), x, y1);
         }
         // T_ba is final and read by no later level: only its scaled fp16 transpose is
         // stored, rows 32 + r, 33 + r of columns j, j + 1 as K pairs of rows j, j + 1
         const float bj0 = beta[j], bj1 = beta[j + 1];
-        st_shared_u32(tbt + tc::core_offset(j, 32 + r, 64, 2), tc::pack_f16x2(-y00 * bj0, -y10 * bj0));
-        st_shared_u32(tbt + tc::core_offset(j + 1, 32 + r, 64, 2), tc::pack_f16x2(-y01 * bj1, -y11 * bj1));
+        st_shared_u32(tbt + tc::core_offset(j, 32 + r, 64, 2), tc::pack_f16x2(-y0.x * bj0, -y1.x * bj0));
+        st_shared_u32(tbt + tc::core_offset(j + 1, 32 + r, 64, 2), tc::pack_f16x2(-y0.y * bj1, -y1.y * bj1));
     }
     tc::fence_proxy_async();   // the transpose is read by the products issued after the barrier
     __syncthreads();
+}
+
+__device__ __forceinline__ void ex2_8(float *d)
+{
+#pragma unroll
+    for (int o = 0; o < 8; o++) d[o] = ex2(d[o]);
+}
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void unpack_f16x8(uint4 u, float *f)
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __half2 h2 = *reinterpret_cast<const __half2 *>(&w[i]);
+        const float2 v = __half22float2(h2);
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+// fp16 [64][64] stash of the pairwise path: 16-byte chunks XOR-swizzled by row
+__device__ __forceinline__ uint32_t stash_off(int r, int c) { return static_cast<uint32_t>(r * 128 + (((c >> 3) ^ (r & 7)) << 4)); }
+
+// The per-channel log-decay in log2 units, g * log2(e): -e^{A_log} softplus(x) log2(e)
+// = -e^{A_log} (max(x, 0) log2(e) + log2(1 + 2^{-|x| log2(e)})), or lower_bound log2(e)
+// sigmoid(e^{A_log} x) with a lower bound.
+__device__ __forceinline__ float gate_log2(float x, float expA, float expA_l2e, int has_lb, float lb_l2e)
+{
+    if (has_lb) return lb_l2e * __fdividef(1.f, 1.f + ex2(-expA_l2e * x));
+    return -expA_l2e * fmaxf(x, 0.f) - expA * lg2(1.f + ex2(-kLog2e * fabsf(x)));
 }
 
 // ---------------------------------------------------------------------------
@@ -333,8 +449,11 @@ __device__ void solve_T(unsigned char *smem, int tid, uint32_t tbt, const float 
 //
 // Thread roles: TMEM lane l = 32 (warp & 3) + lane and channel quarter sub = warp >> 2.
 // Lanes 0..63 are the K side (key row r = l), lanes 64..127 the Q side (query row
-// r = l - 64); in a channel half a thread covers channels 32 sub .. 32 sub + 31.
-// The gate pass uses channel c = tid & 63 of the half and row block tid >> 6.
+// r = l - 64); in a channel half a thread covers channels 32 sub .. 32 sub + 31. The
+// key-side work beyond the A operand (F = e^{P_{s+1} - b}, K^R, the B_R rows, Kd^T) is
+// split between the two threads of a row: the K thread takes the first 16 of the 32
+// channels, the Q thread the last 16. The gate pass uses channel c = tid & 63 of the
+// half and row block tid >> 6.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Args a)
 {
@@ -342,39 +461,67 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     const Params &p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
-    const int cgi = static_cast<int>(blockIdx.x / H), h = static_cast<int>(blockIdx.x % H);
-    int lo = 0, hi = a.num_seqs - 1;   // the sequence: the last s with cb[s] <= cgi
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.cb[mid] <= cgi) lo = mid; else hi = mid - 1;
-    }
-    const int64_t e = a.entry_base + lo;
-    const int64_t row0 = static_cast<int64_t>(a.cu[e]) + static_cast<int64_t>(cgi - a.cb[lo]) * C;
-    const int64_t rem = static_cast<int64_t>(a.cu[e + 1]) - row0;
-    const int n = static_cast<int>(rem < C ? rem : C);
-    unsigned char *rec = a.rec + static_cast<size_t>(blockIdx.x) * REC_BYTES;
     const int64_t HK = static_cast<int64_t>(H) * KD;
-
+    const int total = a.cb[a.num_seqs] * H;   // (chunk, head) units of this launch
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t mbar = sbase + SM_MBAR;
     float *tab = reinterpret_cast<float *>(smem + SM_TAB);
     float *tot = reinterpret_cast<float *>(smem + SM_TOT);
     float *nrm = reinterpret_cast<float *>(smem + SM_NRM);
     float *betas = reinterpret_cast<float *>(smem + SM_BETA);
-
-    // ---- stage raw_g, start the norm pass ----
-    stage_rows<PT>(sbase + SM_G, p.rg + row0 * p.ld_g + static_cast<int64_t>(h) * KD, p.ld_g, n, tid);
-    cp_async_commit();
-    if (tid == 0) tc::mbar_init(mbar, 2);   // two issuing threads commit to every MMA stage
-    if (warp == 0) tc::tmem_alloc<256>(sbase + SM_TMEMP);
     const int l = 32 * (warp & 3) + lane, sub = warp >> 2;
     const bool kside = l < 64;
     const int r = l & 63, s = r >> 4;
-    // own row: [half][16 bf16 pairs] = channels 64 hf + 32 sub .. + 31
+    const int side = kside ? 0 : 1;
+    if (tid == 0) tc::mbar_init(mbar, 2);   // two issuing threads commit to every MMA stage
+    if (warp == 0) tc::tmem_alloc<256>(sbase + SM_TMEMP);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEMP);
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    uint32_t phase = 0;
+    bool ok = true;
+    // the unit's head, first row and row count (the sequence: the last s with cb[s] <= chunk)
+    auto locate = [&](int bid, int &hh, int64_t &r0, int &nn) {
+        const int cgi = bid / H;
+        hh = bid - cgi * H;
+        int lo = 0, hi = a.num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.cb[mid] <= cgi) lo = mid; else hi = mid - 1;
+        }
+        r0 = static_cast<int64_t>(a.rs[lo]) + static_cast<int64_t>(cgi - a.cb[lo]) * C;
+        const int64_t rem = static_cast<int64_t>(a.rs[lo + 1]) - r0;
+        nn = static_cast<int>(rem < C ? rem : C);
+    };
+    {
+    const int bid = static_cast<int>(blockIdx.x);   // this CTA's unit; the unit pf_stride later starts on
+                                                     // a CTA slot about when this one ends
+    int h, n;
+    int64_t row0;
+    locate(bid, h, row0, n);
+    unsigned char *rec = a.rec + static_cast<size_t>(bid) * REC_BYTES;
+
+    // ---- stage raw_g, prefetch the next unit's rows into L2, start the norm pass ----
+    stage_rows<PT>(sbase + SM_G, p.rg + row0 * p.ld_g + static_cast<int64_t>(h) * KD, p.ld_g, n, tid);
+    cp_async_commit();
+    if (tid < 3 * C && bid + a.pf_stride < total) {
+        int h2, n2;
+        int64_t r2;
+        locate(bid + a.pf_stride, h2, r2, n2);
+        const int rr = tid & 63, part = tid >> 6;   // q, k, raw_g rows
+        if (rr < n2) {
+            const uint16_t *src = part < 2 ? p.qkv + (r2 + rr) * p.ld_qkv + part * HK + static_cast<int64_t>(h2) * KD
+                                           : p.rg + (r2 + rr) * p.ld_g + static_cast<int64_t>(h2) * KD;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" :: "l"(src) : "memory");
+        }
+    }
+    // own row: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31
     uint4 xr[2][4];
     {
         const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + (kside ? HK : 0) + static_cast<int64_t>(h) * KD + 32 * sub;
-        float ss = 0.f;
+        float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
         for (int hf = 0; hf < 2; hf++)
 #pragma unroll
@@ -384,289 +531,370 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
                 float f[8];
                 unpack_bf16x8(v, f);
 #pragma unroll
-                for (int o = 0; o < 8; o++) ss += f[o] * f[o];
+                for (int o = 0; o < 8; o += 2) ss = ffma2(make_float2(f[o], f[o + 1]), make_float2(f[o], f[o + 1]), ss);
             }
-        nrm[sub * 128 + l] = ss;
+        nrm[sub * 128 + l] = ss.x + ss.y;
     }
     if (tid < C) betas[tid] = tid < n ? sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h])) : 0.f;
     const float expA = __expf(__ldg(p.A_log + h));
+    const float expA_l2e = expA * kLog2e, lb_l2e = p.lb * kLog2e;
     cp_async_wait_all();
-    tc::fence_before_sync();
     __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEMP);
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     // rows past the chunk hold zeros; their norm factor is 0 so that eps = 0 gives no NaN
     auto norm_of = [&](int lane_idx, int row) -> float {
         const float f = (lane_idx < 64 ? 1.f : p.scale) * rsqrtf(nrm[lane_idx] + nrm[128 + lane_idx] + p.eps);
         return row < n ? f : 0.f;
     };
     const float rn = norm_of(l, r);
-    uint32_t phase = 0;
-    bool ok = true;
+    const float rk = kside ? rn : norm_of(r, r);   // the key row's norm factor (the Q thread's key share)
 
-    // ---- gate pass over one channel half: b (log2 units) into SM_BH, the constants
-    // table, gamma into the record; returns whether the chunk leaves the tf32 path ----
+    // ---- gate pass over one channel half: per (row, channel) e1 = e^{b - P_s} (the decay
+    // since the block's reference) into SM_BH, or on the pairwise path the in-block log2
+    // prefix itself; the per-(block, channel) constants; gamma into the record. Returns
+    // whether some channel of the half decays by more than the tf32 diagonal path holds
+    // within a block. Thread (cp, o8): channels 2 cp, 2 cp + 1 of the half (packed pairs),
+    // rows 8 o8 .. 8 o8 + 7. ----
     auto gate_half = [&](int hf) -> bool {
-        const int c = tid & 63, sg = tid >> 6, cg = 64 * hf + c;
-        const float dtb = p.dt_bias ? __ldg(p.dt_bias + h * KD + cg) : 0.f;
-        const uint16_t *gt = reinterpret_cast<const uint16_t *>(smem + SM_G);
-        float v[16];
-        float acc = 0.f;
+        const int cp = tid & 31, o8 = tid >> 5, sg = o8 >> 1;
+        const int cg = 64 * hf + 2 * cp;                 // first channel of the pair (in the head)
+        const float2 dtb = p.dt_bias ? make_float2(__ldg(p.dt_bias + h * KD + cg), __ldg(p.dt_bias + h * KD + cg + 1))
+                                     : make_float2(0.f, 0.f);
+        const unsigned char *gt = smem + SM_G + 8 * o8 * 256 + (cg & 7) * 2;
+        const int ch = cg >> 3;
+        const int nv = n - 8 * o8;               // rows of this octet inside the chunk
+        float2 v[8];
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            const int row = 16 * sg + j;
-            const float x = bf16_to_f32(gt[(st_off(row, cg >> 3) >> 1) + (cg & 7)]) + dtb;
-            const float g = row < n ? kLog2e * gate_log_decay_fast(x, expA, p.has_lb, p.lb) : 0.f;
-            acc += g;
-            v[j] = acc;
+        for (int j = 0; j < 8; j++) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(gt + j * 256 + ((ch ^ j) << 4));
+            v[j] = fadd2(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)), dtb);
         }
-        tot[sg * 64 + c] = acc;
+        if (p.has_lb) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float2 t = fmul2(v[j], make_float2(-expA_l2e, -expA_l2e));
+                v[j] = make_float2(lb_l2e * rcp_approx(1.f + ex2(t.x)), lb_l2e * rcp_approx(1.f + ex2(t.y)));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float lx = lg2(1.f + ex2(-kLog2e * fabsf(v[j].x)));
+                const float ly = lg2(1.f + ex2(-kLog2e * fabsf(v[j].y)));
+                const float2 m = make_float2(fmaxf(v[j].x, 0.f), fmaxf(v[j].y, 0.f));
+                v[j] = ffma2(m, make_float2(-expA_l2e, -expA_l2e), fmul2(make_float2(lx, ly), make_float2(-expA, -expA)));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            if (j >= nv) v[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 1; j < 8; j++) v[j] = fadd2(v[j], v[j - 1]);
+        *reinterpret_cast<float2 *>(tot + o8 * 64 + 2 * cp) = v[7];
+        // the second octet of a block starts from the first octet's sum; the block sum
+        // decides the path (a block decaying beyond kBlockSpan2 nats)
         __syncthreads();
-        float P0 = 0.f, P4 = 0.f;
+        float2 oct[8];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float t = tot[q * 64 + c];
-            if (q < sg) P0 += t;
-            P4 += t;
+        for (int q = 0; q < 8; q++) oct[q] = *reinterpret_cast<const float2 *>(tot + q * 64 + 2 * cp);
+        const float2 blk0 = fadd2(oct[0], oct[1]), blk1 = fadd2(oct[2], oct[3]);
+        const float2 blk2 = fadd2(oct[4], oct[5]), blk3 = fadd2(oct[6], oct[7]);
+        const float2 acc = sg == 0 ? blk0 : (sg == 1 ? blk1 : (sg == 2 ? blk2 : blk3));
+        const int fl = (-acc.x > kBlockSpan2 || -acc.y > kBlockSpan2) ? 1 : 0;
+        const bool flagged = __syncthreads_or(fl) != 0;
+        if (o8 & 1) {
+            const float2 first = sg == 0 ? oct[0] : (sg == 1 ? oct[2] : (sg == 2 ? oct[4] : oct[6]));
+#pragma unroll
+            for (int j = 0; j < 8; j++) v[j] = fadd2(v[j], first);
         }
-        const float P1 = P0 + acc;
-        float *bh = reinterpret_cast<float *>(smem + SM_BH);
+        {
+            float *bh = reinterpret_cast<float *>(smem + SM_BH + 8 * o8 * 256);
+            const int q4 = cp >> 1, e4 = (cp & 1) * 2;
 #pragma unroll
-        for (int j = 0; j < 16; j++) bh[bh_off(16 * sg + j, c) >> 2] = P0 + v[j];
-        const float m2 = P0 + v[7];
-        tab[tab_off(sg, kP0, c) >> 2] = P0;
-        tab[tab_off(sg, kP1, c) >> 2] = P1;
-        tab[tab_off(sg, kTL, c) >> 2] = ex2(P0 - m2);
-        tab[tab_off(sg, kTR, c) >> 2] = ex2(m2 - P1);
-        tab[tab_off(sg, kE, c) >> 2] = ex2(P0);
-        tab[tab_off(sg, kD4, c) >> 2] = ex2(P4 - P1);
-        tab[tab_off(sg, kDa, c) >> 2] = sg == 0 ? ex2(tot[64 + c]) : (sg == 3 ? ex2(tot[128 + c]) : 1.f);
-        if (sg == 3) reinterpret_cast<float *>(rec + REC_GAM)[cg] = ex2(P4);
-        const int fl = (v[0] - v[7] > kHalfSpan2) || (v[7] - v[15] > kHalfSpan2) || (-acc > kBlockSpan2);
-        return __syncthreads_or(fl) != 0;
+            for (int j = 0; j < 8; j++) {
+                const int rr = 8 * o8 + j;
+                const float2 val = flagged ? v[j] : make_float2(ex2(v[j].x), ex2(v[j].y));
+                *reinterpret_cast<float2 *>(bh + (j * 256 + ((q4 ^ (rr & 7)) << 4)) / 4 + e4) = val;
+            }
+        }
+        if ((o8 & 1) == 0) {   // the first octet of each block writes the block's constants
+            const float2 P0 = sg == 0 ? make_float2(0.f, 0.f)
+                            : (sg == 1 ? blk0 : (sg == 2 ? fadd2(blk0, blk1) : fadd2(fadd2(blk0, blk1), blk2)));
+            const float2 P4 = fadd2(fadd2(blk0, blk1), fadd2(blk2, blk3));
+            const float2 n1 = sg == 0 ? blk1 : (sg == 1 ? blk2 : (sg == 2 ? blk3 : make_float2(0.f, 0.f)));
+            const float2 n2 = sg == 0 ? blk2 : (sg == 1 ? blk3 : make_float2(0.f, 0.f));
+            float *tb = tab + sg * 8 * 64 + 2 * cp;
+            auto put2 = [&](int k, float2 x) { *reinterpret_cast<float2 *>(tb + k * 64) = x; };
+            put2(kE, make_float2(ex2(P0.x), ex2(P0.y)));
+            put2(kBD, make_float2(ex2(acc.x), ex2(acc.y)));                                   // e^{P_{s+1} - P_s}
+            const float2 d4 = fsub2(fsub2(P4, P0), acc);
+            put2(kD4, make_float2(ex2(d4.x), ex2(d4.y)));                                     // e^{P_4 - P_{s+1}}
+            put2(kD2, make_float2(ex2(n1.x), ex2(n1.y)));                                     // e^{P_{s+2} - P_{s+1}}
+            const float2 n12 = fadd2(n1, n2);
+            put2(kD3, make_float2(ex2(n12.x), ex2(n12.y)));                                   // e^{P_{s+3} - P_{s+1}}
+            put2(kP1, acc);                                                                   // the block's log2 decay
+            if (sg == 3) *reinterpret_cast<float2 *>(rec + REC_GAM + 4 * cg) = make_float2(ex2(P4.x), ex2(P4.y));
+        }
+        __syncthreads();
+        return flagged;
     };
 
-    // ---- operand generation over one channel half ----
-    auto gen_half = [&](int hf) {
-        const uint32_t bh = sbase + SM_BH, tb = sbase + SM_TAB;
-        const bool extra = r < 16;       // this lane also holds the off-diagonal row 48 + r
-        uint4 xe[4];
-        float rne = 0.f;
-        if (extra) {
-            const int re = 48 + r;
-            const uint16_t *src = p.qkv + (row0 + re) * p.ld_qkv + (kside ? HK : 0) + static_cast<int64_t>(h) * KD +
-                                  64 * hf + 32 * sub;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; q4++)
-                xe[q4] = re < n ? __ldg(reinterpret_cast<const uint4 *>(src + 8 * q4)) : make_uint4(0u, 0u, 0u, 0u);
-            rne = norm_of(l + 48, re);
+    // ---- operand generation over one channel half; pw: this half's diagonal blocks take
+    // the pairwise path (SM_BH then holds the in-block log2 prefix, k^ and q^ go to the
+    // stash instead of K^R) ----
+    const uint32_t bh_row = sbase + SM_BH + r * 256;
+    const int swz = r & 7;
+    const uint32_t tb_blk = sbase + SM_TAB + s * 8 * 256;
+    const int row_g = kside ? r : 64 + r;     // record row of K^G / Q^G
+    unsigned char *kqg_row = rec + REC_KQG + tc::core_offset(row_g, 0, 128, 2);
+    const uint32_t bdiag_row = sbase + SM_BDIAG + tc::core_offset(r, 0, 64, 4);
+    const uint32_t boff = sbase + SM_BOFF;
+    const uint32_t kd_base = sbase + SM_SB + 8 * SBO_SB + static_cast<uint32_t>((r >> 3) * 128 + (r & 7) * 2);
+    auto gen_half = [&](int hf, bool pw) {
+        auto ld8 = [&](uint32_t addr, float *dst) {   // 8 floats at addr, addr + 16
+            const float4 lo4 = ld_shared_f4(addr), hi4 = ld_shared_f4(addr + 16);
+            dst[0] = lo4.x; dst[1] = lo4.y; dst[2] = lo4.z; dst[3] = lo4.w;
+            dst[4] = hi4.x; dst[5] = hi4.y; dst[6] = hi4.z; dst[7] = hi4.w;
+        };
+        // the Q thread's key share: key row r, channels 32 sub + 16 .. + 31 of the half
+        uint4 kq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+        if (!kside && r < n) {
+            const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + HK + static_cast<int64_t>(h) * KD + 64 * hf + 32 * sub + 16;
+            kq[0] = __ldg(reinterpret_cast<const uint4 *>(src));
+            kq[1] = __ldg(reinterpret_cast<const uint4 *>(src + 8));
         }
-        const int row_g = kside ? r : 64 + r;     // record row of K^G / Q^G
 #pragma unroll
         for (int u = 0; u < 4; u++) {
-            const int cl = 32 * sub + 8 * u;      // channel within the half
-            const int c = 64 * hf + cl;           // channel within the head
-            float x[8], b2[8], t[8], e1[8], v8[8];
+            const int cl = 32 * sub + 8 * u;       // channel within the half
+            const int c = 64 * hf + cl;            // channel within the head
+            const uint32_t tbu = tb_blk + cl * 4;  // this block's constants of channels cl ..
+            float x[8], e1[8], t[8], xe[8], v8[8];
             unpack_bf16x8(xr[hf][u], x);
-#pragma unroll
-            for (int o = 0; o < 8; o++) x[o] *= rn;
+            scale8(x, x, rn);
             {
-                const float4 lo4 = ld_shared_f4(bh + bh_off(r, cl)), hi4 = ld_shared_f4(bh + bh_off(r, cl + 4));
-                b2[0] = lo4.x; b2[1] = lo4.y; b2[2] = lo4.z; b2[3] = lo4.w;
-                b2[4] = hi4.x; b2[5] = hi4.y; b2[6] = hi4.z; b2[7] = hi4.w;
+                const int q = cl >> 2;
+                const float4 lo4 = ld_shared_f4(bh_row + ((q ^ swz) << 4));
+                const float4 hi4 = ld_shared_f4(bh_row + (((q + 1) ^ swz) << 4));
+                e1[0] = lo4.x; e1[1] = lo4.y; e1[2] = lo4.z; e1[3] = lo4.w;
+                e1[4] = hi4.x; e1[5] = hi4.y; e1[6] = hi4.z; e1[7] = hi4.w;
             }
-            auto tab8 = [&](int blk, int k, float *dst) {
-                const float4 lo4 = ld_shared_f4(tb + tab_off(blk, k, cl)), hi4 = ld_shared_f4(tb + tab_off(blk, k, cl + 4));
-                dst[0] = lo4.x; dst[1] = lo4.y; dst[2] = lo4.z; dst[3] = lo4.w;
-                dst[4] = hi4.x; dst[5] = hi4.y; dst[6] = hi4.z; dst[7] = hi4.w;
-            };
-            tab8(s, kP0, t);
+            float lp[8];   // pairwise path: the in-block log2 prefix
+            if (pw) {
 #pragma unroll
-            for (int o = 0; o < 8; o++) e1[o] = ex2(b2[o] - t[o]);   // e^{b - P_s} <= 1
-            // K^L / Q^L (tf32) -> tensor memory, lane l, column of the channel in the half
-            tab8(s, kTL, t);
-            {
+                for (int o = 0; o < 8; o++) { lp[o] = e1[o]; e1[o] = ex2(lp[o]); }
+            }
+            mul8(xe, x, e1);
+            {   // the A operand (tf32) -> tensor memory, lane l, column of the channel in the half
                 uint32_t d8[8];
 #pragma unroll
-                for (int o = 0; o < 8; o++) d8[o] = tc::to_tf32(x[o] * e1[o] * t[o]);
-                tc::tmem_st8u(tlane + TM_DIAGA + cl, d8);
+                for (int o = 0; o < 8; o++) d8[o] = tf32_rna(xe[o]);
+                tc::tmem_st8u(tlane + TM_A + cl, d8);
             }
+            if (pw)      // the stash of the pairwise path: k^ / q^ in fp16
+                st_shared_u4(sbase + SM_BDIAG + side * 8192 + stash_off(r, cl), pack8_f16(x));
             // K^G / Q^G = x e^{b} -> the record
-            tab8(s, kE, t);
+            ld8(tbu + kE * 256, t);
+            mul8(v8, xe, t);
+            *reinterpret_cast<uint4 *>(kqg_row + (c >> 3) * 128) = pack8_f16(v8);
+            // key-side share
+            if (kside ? (u < 2) : (u >= 2)) {
+                float kk[8], kf[8];
+                if (kside) {
 #pragma unroll
-            for (int o = 0; o < 8; o++) v8[o] = x[o] * e1[o] * t[o];
-            *reinterpret_cast<uint4 *>(rec + REC_KQG + tc::core_offset(row_g, c, 128, 2)) = pack8_f16(v8);
-            // off-diagonal A operand (fp16 pairs -> tensor memory)
-            if (!extra) {
-                if (r >= 48) {   // rows 48..63 against rows 0..31: reference P_2 = P_3 - (block 2's decay)
-                    tab8(3, kDa, t);
-#pragma unroll
-                    for (int o = 0; o < 8; o++) v8[o] = x[o] * e1[o] * t[o];
+                    for (int o = 0; o < 8; o++) kk[o] = x[o];
                 } else {
-#pragma unroll
-                    for (int o = 0; o < 8; o++) v8[o] = x[o] * e1[o];
+                    unpack_bf16x8(kq[u - 2], kk);
+                    scale8(kk, kk, rk);
                 }
-            } else {             // row 48 + r against block 2: reference P_3
-                float xx[8], be[8];
-                unpack_bf16x8(xe[u], xx);
-                const float4 lo4 = ld_shared_f4(bh + bh_off(48 + r, cl)), hi4 = ld_shared_f4(bh + bh_off(48 + r, cl + 4));
-                be[0] = lo4.x; be[1] = lo4.y; be[2] = lo4.z; be[3] = lo4.w;
-                be[4] = hi4.x; be[5] = hi4.y; be[6] = hi4.z; be[7] = hi4.w;
-                tab8(3, kP0, t);
+                if (!pw) {
+                    // K^R = k e^{P_s - b} = k / e1 (tf32) -> SM_BDIAG row r; k F = K^R e^{P_{s+1} - P_s}
 #pragma unroll
-                for (int o = 0; o < 8; o++) v8[o] = xx[o] * rne * ex2(be[o] - t[o]);
-            }
-            {
-                uint32_t a4[4];
+                    for (int o = 0; o < 8; o++) v8[o] = kk[o] * rcp_approx(e1[o]);
+                    st_shared_u4(bdiag_row + (cl >> 2) * 128, pack4_tf32(v8));
+                    st_shared_u4(bdiag_row + ((cl >> 2) + 1) * 128, pack4_tf32(v8 + 4));
+                    ld8(tbu + kBD * 256, t);
+                    mul8(kf, v8, t);
+                } else {   // k F = k e^{P_{s+1} - b} = k 2^{(block decay) - prefix}
+                    ld8(tbu + kP1 * 256, t);
 #pragma unroll
-                for (int o = 0; o < 4; o++) a4[o] = tc::pack_f16x2(v8[2 * o], v8[2 * o + 1]);
-                tc::tmem_st4u(tlane + TM_OFFA + (c >> 1), a4);
-            }
-            if (kside) {
-                // F = e^{P_{s+1} - b} <= 1; k F is the key row against later references
-                tab8(s, kP1, t);
-                float kf[8];
-#pragma unroll
-                for (int o = 0; o < 8; o++) kf[o] = x[o] * ex2(t[o] - b2[o]);
-                // K^R (tf32) -> SM_DIAGB row r
-                tab8(s, kTR, t);
-#pragma unroll
-                for (int o = 0; o < 8; o++) v8[o] = kf[o] * t[o];
-                st_shared_u4(sbase + SM_DIAGB + tc::core_offset(r, cl, 64, 4), pack4_tf32(v8));
-                st_shared_u4(sbase + SM_DIAGB + tc::core_offset(r, cl + 4, 64, 4), pack4_tf32(v8 + 4));
-                // rows of the off-diagonal B operand
-                const uint32_t ob = sbase + SM_OFFB;
-                if (s == 0) {
-                    tab8(0, kDa, t);
-#pragma unroll
-                    for (int o = 0; o < 8; o++) v8[o] = kf[o] * t[o];
-                    st_shared_u4(ob + tc::core_offset(r, c, 128, 2), pack8_f16(v8));
-                    st_shared_u4(ob + tc::core_offset(32 + r, c, 128, 2), pack8_f16(kf));
-                } else if (s == 1) {
-                    st_shared_u4(ob + tc::core_offset(r, c, 128, 2), pack8_f16(kf));
-                } else if (s == 2) {
-                    st_shared_u4(ob + tc::core_offset(16 + r, c, 128, 2), pack8_f16(kf));
+                    for (int o = 0; o < 8; o++) kf[o] = kk[o] * ex2(t[o] - lp[o]);
+                }
+                // B_R rows (R = s + 1 .. 3): k e^{P_R - b} -> SM_BOFF row off_b_base(R) + r
+                if (s < 3) {
+                    const uint32_t a1 = boff + tc::core_offset(off_b_base(s + 1) + r, cl, 64, 4);
+                    st_shared_u4(a1, pack4_tf32(kf));
+                    st_shared_u4(a1 + 128, pack4_tf32(kf + 4));
+                }
+                if (s < 2) {
+                    ld8(tbu + kD2 * 256, t);
+                    mul8(v8, kf, t);
+                    const uint32_t a2 = boff + tc::core_offset(off_b_base(s + 2) + r, cl, 64, 4);
+                    st_shared_u4(a2, pack4_tf32(v8));
+                    st_shared_u4(a2 + 128, pack4_tf32(v8 + 4));
+                }
+                if (s < 1) {
+                    ld8(tbu + kD3 * 256, t);
+                    mul8(v8, kf, t);
+                    const uint32_t a3 = boff + tc::core_offset(48 + r, cl, 64, 4);
+                    st_shared_u4(a3, pack4_tf32(v8));
+                    st_shared_u4(a3 + 128, pack4_tf32(v8 + 4));
                 }
                 // Kd^T = (k F e^{b_last - P_{s+1}})^T -> SB rows 64 + c
-                tab8(s, kD4, t);
+                ld8(tbu + kD4 * 256, t);
+                mul8(v8, kf, t);
+                const uint32_t kd = kd_base + static_cast<uint32_t>(c >> 3) * SBO_SB;
 #pragma unroll
-                for (int o = 0; o < 8; o++)
-                    st_shared_u16(sbase + SM_SB + sb_offset(64 + c + o, r), f16_bits(kf[o] * t[o]));
+                for (int o = 0; o < 8; o++) st_shared_u16(kd + o * 16, f16_bits(v8[o]));
             }
+        }
+    };
+
+    // ---- the pairwise diagonal blocks of one channel half (flagged halves): pair
+    // pi = tid + 256 k of the 4 x 136 (row, column <= row) pairs of the diagonal blocks,
+    // summed into registers (key rows: A before beta; query rows: Aqk) ----
+    float pa[3] = {0.f, 0.f, 0.f}, pq[3] = {0.f, 0.f, 0.f};
+    auto pair_of = [](int pi, int &rr, int &il) {
+        const int sb = pi / 136, q = pi - sb * 136;
+        int rl = static_cast<int>((sqrtf(8.f * q + 1.f) - 1.f) * 0.5f);
+        if ((rl + 1) * (rl + 2) / 2 <= q) rl++;
+        if (rl * (rl + 1) / 2 > q) rl--;
+        il = q - rl * (rl + 1) / 2;
+        rr = 16 * sb + rl;
+    };
+    auto pairwise_half = [&]() {
+        const uint32_t ks = sbase + SM_BDIAG, qs = ks + 8192, bh = sbase + SM_BH;
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            const int pi = tid + 256 * k;
+            if (pi < 4 * 136) {
+                int rr, il;
+                pair_of(pi, rr, il);
+                const int ii = (rr & ~15) + il;
+                float sa = 0.f, sq = 0.f;
+                for (int cc = 0; cc < 64; cc += 8) {
+                    float kr[8], ki[8], qr[8], br[8], bi[8];
+                    unpack_f16x8(ld_shared_u4(ks + stash_off(rr, cc)), kr);
+                    unpack_f16x8(ld_shared_u4(ks + stash_off(ii, cc)), ki);
+                    unpack_f16x8(ld_shared_u4(qs + stash_off(rr, cc)), qr);
+                    const float4 a0 = ld_shared_f4(bh + bh_off(rr, cc)), a1 = ld_shared_f4(bh + bh_off(rr, cc + 4));
+                    const float4 c0 = ld_shared_f4(bh + bh_off(ii, cc)), c1 = ld_shared_f4(bh + bh_off(ii, cc + 4));
+                    br[0] = a0.x; br[1] = a0.y; br[2] = a0.z; br[3] = a0.w; br[4] = a1.x; br[5] = a1.y; br[6] = a1.z; br[7] = a1.w;
+                    bi[0] = c0.x; bi[1] = c0.y; bi[2] = c0.z; bi[3] = c0.w; bi[4] = c1.x; bi[5] = c1.y; bi[6] = c1.z; bi[7] = c1.w;
+#pragma unroll
+                    for (int o = 0; o < 8; o++) {
+                        const float w = ex2(br[o] - bi[o]) * ki[o];
+                        sa += kr[o] * w;
+                        sq += qr[o] * w;
+                    }
+                }
+                pa[k] += sa;
+                pq[k] += sq;
+            }
+        }
+    };
+    auto issue_gram = [&](bool pw, bool acc_diag, bool acc_off) {
+        if (tid == 0 || tid == 32) {
+            tc::fence_after_sync();
+            if (tid == 0)
+                tc::gemm_ta_tf32<96, 64>(tmem + TM_XOFF, tmem + TM_A, sbase + SM_BOFF, SBO64_TF32, acc_off);
+            else if (!pw)
+                tc::gemm_ta_tf32<64, 64>(tmem + TM_XDIAG, tmem + TM_A, sbase + SM_BDIAG, SBO64_TF32, acc_diag);
+            tc::commit(mbar);
         }
     };
 
     // ================= channel half 0 =================
-    bool flagged = gate_half(0);
-    if (!flagged) {
-        gen_half(0);
-        tc::tmem_st_wait();
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0 || tid == 32) {
-            tc::fence_after_sync();
-            if (tid == 32)
-                tc::gemm_ta_tf32<64, 64>(tmem + TM_XDIAG, tmem + TM_DIAGA, sbase + SM_DIAGB, SBO64_TF32, false);
-            tc::commit(mbar);
-        }
-        // ================= channel half 1 =================
-        flagged = gate_half(1);
-        // the half-0 diagonal product reads SM_DIAGB and TM_DIAGA, which half 1 rewrites
-        ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
-        phase ^= 1;
-    }
-    if (flagged || !ok) {
-        if (tid == 0) {
-            if (!ok) {
-                if (p.err) atomicOr(p.err, kErrTimeout);
-            } else {
-                const uint32_t slot = atomicAdd(a.flag_count, 1u);
-                a.flag_list[slot] = blockIdx.x;
-            }
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::tmem_dealloc<256>(tmem);
-        return;
-    }
-    gen_half(1);
+    const bool pw0 = gate_half(0);
+    gen_half(0, pw0);
     tc::tmem_st_wait();
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0 || tid == 32) {
-        tc::fence_after_sync();
-        if (tid == 0)
-            tc::gemm_ta<64, 128>(tmem + TM_XOFF, tmem + TM_OFFA, sbase + SM_OFFB, SBO128_F16, false);
-        else
-            tc::gemm_ta_tf32<64, 64>(tmem + TM_XDIAG, tmem + TM_DIAGA, sbase + SM_DIAGB, SBO64_TF32, true);
-        tc::commit(mbar);
-    }
+    issue_gram(pw0, false, false);
+    if (pw0) pairwise_half();
+    // ================= channel half 1 =================
+    const bool pw1 = gate_half(1);
+    // the half-0 products read the A operand and SM_BOFF / SM_BDIAG, which half 1 rewrites
     ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
     phase ^= 1;
+    gen_half(1, pw1);
+    tc::tmem_st_wait();
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    issue_gram(pw1, !pw0, true);
+    if (pw1) pairwise_half();
+    ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
+    phase ^= 1;
+    const bool mma_diag = !(pw0 && pw1), pw_diag = pw0 || pw1;
+    if (pw_diag) {   // the pairwise sums -> SM_XD [side][row][column in the block]
+        float *xd = reinterpret_cast<float *>(smem + SM_XD);
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            const int pi = tid + 256 * k;
+            if (pi < 4 * 136) {
+                int rr, il;
+                pair_of(pi, rr, il);
+                xd[rr * 16 + il] = pa[k];
+                xd[1024 + rr * 16 + il] = pq[k];
+            }
+        }
+        __syncthreads();
+    }
 
     // ================= row assembly: A (fp32, with beta) and Aqk (fp16 into SB) =================
+    // Thread (l, sub) writes column blocks k4 = 2 sub, 2 sub + 1 of row r: zero above the
+    // diagonal block, the diagonal block from X_diag (+ the pairwise sums), the blocks
+    // left of it from X_off at column off_b_base(s) + i. A warp covers row blocks s0 and
+    // s0 + 1; its TMEM loads are collective, so it loads every source some lane needs.
     if (ok) {
         const int qd = warp & 3;          // lane quadrant: 0/1 K rows 0..31/32..63, 2/3 Q rows
-        const bool hiq = (qd & 1) != 0;   // rows 32..63 (blocks 2, 3)
-        const float beta_r = kside ? betas[r] : 1.f;
-        float *amat = reinterpret_cast<float *>(smem + SM_AMAT);
-        auto put = [&](int row, int k4, const float *v) {   // 16 entries of row `row`, columns 16 k4 ..
-            if (kside) {
-                const float br = betas[row];
-                float *dst = amat + row * AP + 16 * k4;
-#pragma unroll
-                for (int u = 0; u < 16; u += 4)
-                    *reinterpret_cast<float4 *>(dst + u) = make_float4(v[u] * br, v[u + 1] * br, v[u + 2] * br, v[u + 3] * br);
-            } else {
-                st_shared_u4(sbase + SM_SB + sb_offset(row, 16 * k4), pack8_f16(v));
-                st_shared_u4(sbase + SM_SB + sb_offset(row, 16 * k4 + 8), pack8_f16(v + 8));
-            }
-        };
-        (void)beta_r;
+        const int s0 = 2 * (qd & 1);
+        const int rl = r & 15;
+        const int lim = kside ? rl : rl + 1;   // diagonal-block columns < lim are kept
+        const float br = kside ? betas[r] : 1.f;
+        float *arow = reinterpret_cast<float *>(smem + SM_AMAT) + r * AP;
+        const float *xdr = reinterpret_cast<const float *>(smem + SM_XD) + side * 1024 + r * 16;
 #pragma unroll
         for (int kk = 0; kk < 2; kk++) {
             const int k4 = 2 * sub + kk;
-            float v[16], w[16];
-            // warp-uniform sources of this segment
-            uint32_t src0 = 0xffffffffu, src1 = 0xffffffffu;
-            if (!hiq) {
-                if (k4 == 0) { src0 = TM_XDIAG + 0; src1 = TM_XOFF + 32; }
-                else if (k4 == 1) src0 = TM_XDIAG + 16;
-                else if (k4 == 2) src1 = TM_XOFF + 48;    // rows 48 + r, block (3, 2), lanes r < 16
-            } else {
-                if (k4 == 0) src0 = TM_XOFF + 0;
-                else if (k4 == 1) src0 = TM_XOFF + 16;
-                else if (k4 == 2) src0 = TM_XDIAG + 32;
-                else src0 = TM_XDIAG + 48;
-            }
-            if (src0 != 0xffffffffu) tc::tmem_ld16(tlane + src0, v);
-            if (src1 != 0xffffffffu) tc::tmem_ld16(tlane + src1, w);
+            float off0[16], off1[16], dg[16], v[16];
+            if (k4 < s0) tc::tmem_ld16(tlane + TM_XOFF + off_b_base(s0) + 16 * k4, off0);
+            if (k4 <= s0) tc::tmem_ld16(tlane + TM_XOFF + off_b_base(s0 + 1) + 16 * k4, off1);
+            if (mma_diag && (k4 == s0 || k4 == s0 + 1)) tc::tmem_ld16(tlane + TM_XDIAG + 16 * k4, dg);
             tc::tmem_ld_wait();
-            float o[16];
-            bool write_own = true;
-            if (k4 > s) {
+            if (k4 < s) {
+                if (s == s0) {
 #pragma unroll
-                for (int u = 0; u < 16; u++) o[u] = 0.f;
-            } else if (k4 == s) {     // diagonal block: strictly lower for A, lower for Aqk
+                    for (int u = 0; u < 16; u++) v[u] = off0[u];
+                } else {
 #pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    const int i = 16 * k4 + u;
-                    o[u] = (kside ? (i < r) : (i <= r)) ? v[u] : 0.f;
+                    for (int u = 0; u < 16; u++) v[u] = off1[u];
                 }
-            } else if (s == 1) {      // block (1, 0)
+            } else if (k4 == s) {
+                if (!mma_diag) {
 #pragma unroll
-                for (int u = 0; u < 16; u++) o[u] = w[u];
-            } else if (k4 < 2) {      // blocks (2|3, 0|1)
+                    for (int u = 0; u < 16; u++) dg[u] = 0.f;
+                }
+                if (pw_diag) {
 #pragma unroll
-                for (int u = 0; u < 16; u++) o[u] = v[u];
-            } else {                  // block (3, 2): written by lane r - 48
-                write_own = false;
+                    for (int u = 0; u < 16; u++) dg[u] += (u <= rl) ? xdr[u] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 16; u++) v[u] = u < lim ? dg[u] : 0.f;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; u++) v[u] = 0.f;
             }
-            if (write_own) put(r, k4, o);
-            if (!hiq && k4 == 2 && r < 16) put(48 + r, 2, w);
+            if (kside) {
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    const float2 a = fmul2(make_float2(v[u], v[u + 1]), make_float2(br, br));
+                    const float2 b = fmul2(make_float2(v[u + 2], v[u + 3]), make_float2(br, br));
+                    *reinterpret_cast<float4 *>(arow + 16 * k4 + u) = make_float4(a.x, a.y, b.x, b.y);
+                }
+            } else {
+                st_shared_u4(sbase + SM_SB + sb_offset(r, 16 * k4), pack8_f16(v));
+                st_shared_u4(sbase + SM_SB + sb_offset(r, 16 * k4 + 8), pack8_f16(v + 8));
+            }
         }
     }
     tc::fence_proxy_async();   // the Aqk rows of SB are read by the last products
@@ -709,153 +937,12 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc<256>(tmem);
-}
-
-// ---------------------------------------------------------------------------
-// exact_kernel: the record of every (chunk, head) that prep_kernel listed, in fp32 on the
-// CUDA cores with pairwise exponentials (no factoring, so no range limit on the decay).
-// One CTA of 256 threads per listed record, grid-stride over the list.
-// ---------------------------------------------------------------------------
-constexpr uint32_t EX_KH = 0;            // fp32 [64][128] k^ (then Kd)
-constexpr uint32_t EX_QH = 32768;        // fp32 [64][128] q^
-constexpr uint32_t EX_BB = 65536;        // fp32 [64][128] b (natural log units)
-constexpr uint32_t EX_AM = 98304;        // fp32 [64][68] A
-constexpr uint32_t EX_TM = EX_AM + 17408;   // fp32 [64][68] T
-constexpr uint32_t EX_AQ = EX_TM + 17408;   // fp32 [64][68] Aqk
-constexpr uint32_t EX_BETA = EX_AQ + 17408; // fp32 [64]
-constexpr uint32_t EX_NRM = EX_BETA + 256;  // fp32 [2][64]
-constexpr uint32_t EXACT_SMEM = EX_NRM + 512;
-
-__global__ void __launch_bounds__(PT, 1) exact_kernel(const __grid_constant__ Args a)
-{
-    extern __shared__ __align__(1024) unsigned char smem[];
-    const Params &p = a.p;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = p.H;
-    float *KH = reinterpret_cast<float *>(smem + EX_KH);
-    float *QH = reinterpret_cast<float *>(smem + EX_QH);
-    float *BB = reinterpret_cast<float *>(smem + EX_BB);
-    float *AM = reinterpret_cast<float *>(smem + EX_AM);
-    float *TM = reinterpret_cast<float *>(smem + EX_TM);
-    float *AQ = reinterpret_cast<float *>(smem + EX_AQ);
-    float *bet = reinterpret_cast<float *>(smem + EX_BETA);
-    float *nq = reinterpret_cast<float *>(smem + EX_NRM);
-    const uint32_t count = *reinterpret_cast<volatile uint32_t *>(a.flag_count);
-    for (uint32_t idx = blockIdx.x; idx < count; idx += gridDim.x) {
-        const uint32_t bid = a.flag_list[idx];
-        const int cgi = static_cast<int>(bid / H), h = static_cast<int>(bid % H);
-        int lo = 0, hi = a.num_seqs - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.cb[mid] <= cgi) lo = mid; else hi = mid - 1;
-        }
-        const int64_t e = a.entry_base + lo;
-        const int64_t row0 = static_cast<int64_t>(a.cu[e]) + static_cast<int64_t>(cgi - a.cb[lo]) * C;
-        const int64_t rem = static_cast<int64_t>(a.cu[e + 1]) - row0;
-        const int n = static_cast<int>(rem < C ? rem : C);
-        unsigned char *rec = a.rec + static_cast<size_t>(bid) * REC_BYTES;
-        const int64_t HK = static_cast<int64_t>(H) * KD;
-        __syncthreads();   // the previous record's reads of shared memory are done
-        // raw q, k
-        for (int i = tid; i < C * KD; i += PT) {
-            const int rr = i >> 7, c = i & 127;
-            const uint16_t *row = p.qkv + (row0 + rr) * p.ld_qkv + static_cast<int64_t>(h) * KD + c;
-            QH[i] = rr < n ? bf16_to_f32(row[0]) : 0.f;
-            KH[i] = rr < n ? bf16_to_f32(row[HK]) : 0.f;
-        }
-        if (tid < C) bet[tid] = tid < n ? sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h])) : 0.f;
-        __syncthreads();
-        // norms: warp w handles rows w, w + 8, ...
-        for (int rr = warp; rr < C; rr += PT / 32) {
-            float sq = 0.f, sk = 0.f;
-            for (int c = lane; c < KD; c += 32) {
-                sq += QH[rr * KD + c] * QH[rr * KD + c];
-                sk += KH[rr * KD + c] * KH[rr * KD + c];
-            }
-            sq = warp_sum(sq);
-            sk = warp_sum(sk);
-            if (lane == 0) {
-                nq[rr] = rr < n ? p.scale * rsqrtf(sq + p.eps) : 0.f;
-                nq[64 + rr] = rr < n ? rsqrtf(sk + p.eps) : 0.f;
-            }
-        }
-        __syncthreads();
-        for (int i = tid; i < C * KD; i += PT) {
-            QH[i] *= nq[i >> 7];
-            KH[i] *= nq[64 + (i >> 7)];
-        }
-        // gate and cumulative decay: thread c < 128 walks the rows
-        if (tid < KD) {
-            const float expA = expf(__ldg(p.A_log + h));
-            const float dtb = p.dt_bias ? __ldg(p.dt_bias + h * KD + tid) : 0.f;
-            float acc = 0.f;
-            for (int rr = 0; rr < C; rr++) {
-                if (rr < n)
-                    acc += gate_log_decay(bf16_to_f32(p.rg[(row0 + rr) * p.ld_g + static_cast<int64_t>(h) * KD + tid]) + dtb,
-                                          expA, p.has_lb, p.lb);
-                BB[rr * KD + tid] = acc;
-            }
-            reinterpret_cast<float *>(rec + REC_GAM)[tid] = expf(acc);
-        }
-        __syncthreads();
-        // A and Aqk pairwise: warp per pair (rr, i), i <= rr, 4 channels per lane
-        for (int pr = warp; pr < C * (C + 1) / 2; pr += PT / 32) {
-            int rr = static_cast<int>((sqrtf(8.f * pr + 1.f) - 1.f) * 0.5f);
-            if ((rr + 1) * (rr + 2) / 2 <= pr) rr++;
-            if (rr * (rr + 1) / 2 > pr) rr--;
-            const int i = pr - rr * (rr + 1) / 2;
-            float sa = 0.f, sq = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int c = 4 * lane + q;
-                const float ex = expf(BB[rr * KD + c] - BB[i * KD + c]) * KH[i * KD + c];
-                sa += KH[rr * KD + c] * ex;
-                sq += QH[rr * KD + c] * ex;
-            }
-            sa = warp_sum(sa);
-            sq = warp_sum(sq);
-            if (lane == 0) {
-                AM[rr * AP + i] = i < rr ? bet[rr] * sa : 0.f;
-                AQ[rr * AP + i] = sq;
-            }
-        }
-        __syncthreads();
-        // T = (I + A)^-1, column j by forward substitution
-        if (tid < C) {
-            const int j = tid;
-            for (int rr = 0; rr < C; rr++) {
-                float t = 0.f;
-                if (rr == j) t = 1.f;
-                else if (rr > j) {
-                    for (int m = j; m < rr; m++) t -= AM[rr * AP + m] * TM[m * AP + j];
-                }
-                TM[rr * AP + j] = t;
-            }
-        }
-        // K^G, Q^G (record) and Kd = k^ e^{b_last - b} (in place of k^)
-        for (int i = tid; i < C * KD; i += PT) {
-            const int rr = i >> 7, c = i & 127;
-            const float g = expf(BB[i]);
-            reinterpret_cast<uint16_t *>(rec + REC_KQG)[tc::core_offset(rr, c, 128, 2) >> 1] = f16_bits(KH[i] * g);
-            reinterpret_cast<uint16_t *>(rec + REC_KQG)[tc::core_offset(64 + rr, c, 128, 2) >> 1] = f16_bits(QH[i] * g);
-        }
-        __syncthreads();
-        for (int i = tid; i < C * KD; i += PT) KH[i] *= expf(BB[(C - 1) * KD + (i & 127)] - BB[i]);
-        __syncthreads();
-        // M1[i][m] = beta_m sum_r Aqk[i][r] T[r][m];  M2[c][m] = beta_m sum_r Kd[r][c] T[r][m]
-        for (int o = tid; o < 192 * C; o += PT) {
-            const int row = o >> 6, m = o & 63;
-            float acc = 0.f;
-            if (row < C) {
-                for (int rr = m; rr <= row; rr++) acc += AQ[row * AP + rr] * TM[rr * AP + m];
-            } else {
-                const int c = row - C;
-                for (int rr = m; rr < C; rr++) acc += KH[rr * KD + c] * TM[rr * AP + m];
-            }
-            reinterpret_cast<uint16_t *>(rec + REC_MM)[tc::core_offset(row, m, 64, 2) >> 1] = f16_bits(acc * bet[m]);
-        }
     }
+    if (!ok && tid == 0)   // a wait gave up: give the product it waited for (bounded) time to end
+        (void)tc::mbar_wait(mbar, phase ^ 1u);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc<256>(tmem);
 }
 
 // ---------------------------------------------------------------------------
@@ -878,6 +965,8 @@ constexpr uint32_t TC_PQ = 64;     // (Q^G S)^T -> O^T   64 columns
 constexpr uint32_t TC_S = 128;     // S^T           128 columns
 constexpr uint32_t TC_AS = 256;    // S^T as fp16 pairs (A of P)   64 columns
 constexpr uint32_t TC_AY = 320;    // Y^T as fp16 pairs (A of the O/S product)   32 columns
+constexpr uint32_t TC_PK2 = 384;   // the second K half of (K^G S)^T   64 columns
+constexpr uint32_t TC_PQ2 = 448;   // the second K half of (Q^G S)^T   64 columns
 
 __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Args a)
 {
@@ -888,7 +977,7 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
     const int rank = static_cast<int>(blockIdx.x / H), h = static_cast<int>(blockIdx.x % H);
     const int sq = a.order[rank];
     const int64_t e = a.entry_base + sq;
-    const int64_t row0 = a.cu[e], row1 = a.cu[e + 1];
+    const int64_t row0 = a.rs[sq], row1 = a.rs[sq + 1];
     const int64_t slot = load_slot(p, e);
     const int j = 32 * (warp & 3) + lane, sub = warp >> 2;
     if (slot >= p.num_slots) {      // flagged before the length check: empty sequences too
@@ -911,7 +1000,8 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t bar = sbase + CH_BAR;   // kq[0], kq[1], mm[0], mm[1], mma
     if (tid == 0) {
-        for (int i = 0; i < 5; i++) tc::mbar_init(bar + 8 * i, 1);
+        for (int i = 0; i < 4; i++) tc::mbar_init(bar + 8 * i, 1);
+        tc::mbar_init(bar + 32, 2);   // the chain products: two issuing threads commit
     }
     if (warp == 0) tc::tmem_alloc<512>(sbase + CH_TMEMP);
     tc::fence_before_sync();
@@ -982,43 +1072,59 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
         ok &= cta_wait(bar + 8 * b, par, smem + CH_WAITOK);
         kq_pending[b] = -1;
         if (!ok) break;
-        float ov[2][16];
-        if (c > 0) {   // O^T of the previous chunk, read before P overwrites it
+        // D1: S^T -> fp16 pairs (the A operand of P); O^T of the previous chunk, read
+        // before P overwrites it. All TMEM loads are issued before one wait.
+        float ov[2][16], ow[2][16], sv[4][16];
+        if (c > 0) {
             tc::tmem_ld16(tlane + TC_PQ + 32 * sub, ov[0]);
             tc::tmem_ld16(tlane + TC_PQ + 32 * sub + 16, ov[1]);
+            tc::tmem_ld16(tlane + TC_PQ2 + 32 * sub, ow[0]);
+            tc::tmem_ld16(tlane + TC_PQ2 + 32 * sub + 16, ow[1]);
         }
-        {
-            const float *gam = reinterpret_cast<const float *>(smem + CH_KQ + b * CH_KQ_STRIDE + REC_GAM);
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 16) {
-                float v[16];
-                const int cidx = 64 * sub + cc;
-                tc::tmem_ld16(tlane + TC_S + cidx, v);
-                tc::tmem_ld_wait();
-                uint32_t pk8[8];
+        for (int q = 0; q < 4; q++) tc::tmem_ld16(tlane + TC_S + 64 * sub + 16 * q, sv[q]);
+        tc::tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 8; i++) pk8[i] = tc::pack_f16x2(v[2 * i], v[2 * i + 1]);
-                tc::tmem_st8u(tlane + TC_AS + (cidx >> 1), pk8);
+        for (int q = 0; q < 4; q++) {
+            uint32_t pk8[8];
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + cidx + u);
-                    v[u] *= g4.x; v[u + 1] *= g4.y; v[u + 2] *= g4.z; v[u + 3] *= g4.w;
-                }
-                tc::tmem_st16(tlane + TC_S + cidx, v);
-            }
+            for (int i = 0; i < 8; i++) pk8[i] = tc::pack_f16x2(sv[q][2 * i], sv[q][2 * i + 1]);
+            tc::tmem_st8u(tlane + TC_AS + 32 * sub + 8 * q, pk8);
         }
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            tc::gemm_ta<128, 128>(tmem + TC_PK, tmem + TC_AS, sbase + CH_KQ + b * CH_KQ_STRIDE, SBO128_F16, false);
+        if (tid == 0 || tid == 32) {   // P = [(K^G S)^T | (Q^G S)^T], one half per issuing thread, each
+            tc::fence_after_sync();      // as two accumulators over the two channel halves
+            const uint32_t half = tid == 0 ? 0u : 64u;
+            tc::gemm_ta_split<64, 128>(tmem + TC_PK + half, tmem + TC_PK2 + half, tmem + TC_AS,
+                                       sbase + CH_KQ + b * CH_KQ_STRIDE + half * 2 * 128, SBO128_F16);
             tc::commit(bar + 32);
         }
-        if (c > 0) store_o(ov, prev0, nprev);
-        // ---- P done: the record's first part is free for chunk c + 2 ----
+        // while P runs: S^T <- S^T Diag(gamma) (P reads the fp16 copy only), the previous
+        // chunk's O rows, and this chunk's V values
+        {
+            const float *gam = reinterpret_cast<const float *>(smem + CH_KQ + b * CH_KQ_STRIDE + REC_GAM);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int cidx = 64 * sub + 16 * q;
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + cidx + u);
+                    sv[q][u] *= g4.x; sv[q][u + 1] *= g4.y; sv[q][u + 2] *= g4.z; sv[q][u + 3] *= g4.w;
+                }
+                tc::tmem_st16(tlane + TC_S + cidx, sv[q]);
+            }
+        }
+        if (c > 0) {
+#pragma unroll
+            for (int q = 0; q < 2; q++)
+#pragma unroll
+                for (int u = 0; u < 16; u++) ov[q][u] += ow[q][u];
+            store_o(ov, prev0, nprev);
+        }
         cp_async_wait_group<1>();   // this chunk's V tile (the newer group may fly)
-        ok &= cta_wait(bar + 32, phc, smem + CH_WAITOK);
+        ok &= cta_wait(bar + 32, phc, smem + CH_WAITOK);   // P done; the barrier publishes V
         phc ^= 1;
         if (!ok) break;
         if (c + 2 < nch) {
@@ -1028,21 +1134,28 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
         // ---- Y^T = (V - K^G S)^T -> fp16 pairs in TMEM ----
         {
             const uint16_t *vt = reinterpret_cast<const uint16_t *>(smem + CH_VT + b * 16384);
+            float pv[2][16], pw[2][16];
+            tc::tmem_ld16(tlane + TC_PK + 32 * sub, pv[0]);
+            tc::tmem_ld16(tlane + TC_PK + 32 * sub + 16, pv[1]);
+            tc::tmem_ld16(tlane + TC_PK2 + 32 * sub, pw[0]);
+            tc::tmem_ld16(tlane + TC_PK2 + 32 * sub + 16, pw[1]);
+            float vv[2][16];
 #pragma unroll
-            for (int q = 0; q < 2; q++) {
-                float v[16];
-                const int r0 = 32 * sub + 16 * q;
-                tc::tmem_ld16(tlane + TC_PK + r0, v);
-                tc::tmem_ld_wait();
+            for (int q = 0; q < 2; q++)
 #pragma unroll
                 for (int u = 0; u < 16; u++) {
-                    const int rr = r0 + u;
-                    v[u] = bf16_to_f32(vt[(st_off(rr, j >> 3) >> 1) + (j & 7)]) - v[u];
+                    const int rr = 32 * sub + 16 * q + u;
+                    vv[q][u] = bf16_to_f32(vt[(st_off(rr, j >> 3) >> 1) + (j & 7)]);
                 }
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
                 uint32_t pk8[8];
 #pragma unroll
-                for (int i = 0; i < 8; i++) pk8[i] = tc::pack_f16x2(v[2 * i], v[2 * i + 1]);
-                tc::tmem_st8u(tlane + TC_AY + (r0 >> 1), pk8);
+                for (int i = 0; i < 8; i++)
+                    pk8[i] = tc::pack_f16x2(vv[q][2 * i] - (pv[q][2 * i] + pw[q][2 * i]),
+                                            vv[q][2 * i + 1] - (pv[q][2 * i + 1] + pw[q][2 * i + 1]));
+                tc::tmem_st8u(tlane + TC_AY + 16 * sub + 8 * q, pk8);
             }
         }
         tc::tmem_st_wait();
@@ -1052,11 +1165,15 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
         if (c + 2 < nch) stage_v(c + 2);
         cp_async_commit();
         bool mm_ok = true;
-        if (tid == 0) {
+        if (tid == 0 || tid == 32) {   // [O^T | S^T] += Y^T [M1; M2]^T: O^T on one thread, S^T on the other
             mm_ok = tc::mbar_wait(bar + 16 + 8 * b, par);
             if (mm_ok) {
                 tc::fence_after_sync();
-                tc::gemm_ta<192, 64>(tmem + TC_PQ, tmem + TC_AY, sbase + CH_MM + b * REC_B_BYTES, SBO64_F16, true);
+                if (tid == 0)
+                    tc::gemm_ta<64, 64>(tmem + TC_PQ, tmem + TC_AY, sbase + CH_MM + b * REC_B_BYTES, SBO64_F16, true);
+                else
+                    tc::gemm_ta<128, 64>(tmem + TC_S, tmem + TC_AY, sbase + CH_MM + b * REC_B_BYTES + 8 * 1024,
+                                         SBO64_F16, true);
             }
             tc::commit(bar + 32);
         }
@@ -1072,10 +1189,16 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
         nprev = n;
     }
     if (ok) {
-        float ov[2][16];
+        float ov[2][16], ow[2][16];
         tc::tmem_ld16(tlane + TC_PQ + 32 * sub, ov[0]);
         tc::tmem_ld16(tlane + TC_PQ + 32 * sub + 16, ov[1]);
+        tc::tmem_ld16(tlane + TC_PQ2 + 32 * sub, ow[0]);
+        tc::tmem_ld16(tlane + TC_PQ2 + 32 * sub + 16, ow[1]);
         tc::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 2; q++)
+#pragma unroll
+            for (int u = 0; u < 16; u++) ov[q][u] += ow[q][u];
         store_o(ov, prev0, nprev);
         if (writable) {
 #pragma unroll
@@ -1133,9 +1256,7 @@ cudaError_t launch_bounded_wait_selftest(uint32_t *err, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-// Workspace of a K = V = 128 prefill: a flag counter (256 bytes), the list of chunks that
-// take the exact path (4 bytes per (chunk, head), rounded up to 256), then one record per
-// (chunk, head).
+// Workspace of a K = V = 128 prefill: one record per (chunk, head).
 static int64_t total_chunks(const int32_t *cu_host, int64_t num_seqs)
 {
     int64_t t = 0;
@@ -1143,19 +1264,15 @@ static int64_t total_chunks(const int32_t *cu_host, int64_t num_seqs)
     return t;
 }
 
-static size_t list_bytes(int64_t chunk_heads) { return (static_cast<size_t>(chunk_heads) * 4 + 255) / 256 * 256; }
-
 size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V, int)
 {
     if (K != chunk::KD || V != chunk::VD || num_seqs <= 0) return 0;
-    const int64_t ch = total_chunks(cu_host, num_seqs) * H;
-    if (ch == 0) return 0;
-    return 256 + list_bytes(ch) + static_cast<size_t>(ch) * chunk::REC_BYTES;
+    return static_cast<size_t>(total_chunks(cu_host, num_seqs)) * H * chunk::REC_BYTES;
 }
 
 // The prefill chains of entries [entry_base, entry_base + num_seqs): per launch of at most
-// kMaxSeqs sequences, the prep pass, the exact pass over the chunks prep listed, and the
-// chains (longest sequence first).
+// kMaxSeqs sequences, the prep pass over every (chunk, head), then the chains (longest
+// sequence first).
 static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const int32_t *cu_host,
                                      int64_t entry_base, int64_t num_seqs, void *workspace,
                                      cudaStream_t stream)
@@ -1165,18 +1282,12 @@ static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const i
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(PREP_SMEM))) != cudaSuccess) return err;
-    if ((err = cudaFuncSetAttribute(exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(EXACT_SMEM))) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(CHAIN_SMEM))) != cudaSuccess) return err;
     int dev = 0, sms = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-    const int64_t all_ch = total_chunks(cu_host + entry_base, num_seqs) * p.H;
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    uint32_t *counter = reinterpret_cast<uint32_t *>(ws);
-    uint32_t *list = reinterpret_cast<uint32_t *>(ws + 256);
-    unsigned char *recs = ws + 256 + list_bytes(all_ch);
+    unsigned char *recs = static_cast<unsigned char *>(workspace);
     int64_t ch_done = 0;   // chunks (not chunk-heads) of the sequences already launched
     std::vector<int32_t> ord;
     for (int64_t s0 = 0; s0 < num_seqs; s0 += kMaxSeqs) {
@@ -1186,14 +1297,13 @@ static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const i
         a.cu = cu;
         a.entry_base = entry_base + s0;
         a.num_seqs = static_cast<int32_t>(ns);
-        a.num_decodes = 0;
-        a.flag_count = counter;
-        a.flag_list = list;
+        a.pf_stride = 2 * sms;
         a.rec = recs + static_cast<size_t>(ch_done) * p.H * REC_BYTES;
         const int32_t *cuh = cu_host + entry_base + s0;
         a.cb[0] = 0;
         for (int64_t i = 0; i < ns; i++)
             a.cb[i + 1] = a.cb[i] + static_cast<int32_t>((static_cast<int64_t>(cuh[i + 1]) - cuh[i] + C - 1) / C);
+        for (int64_t i = 0; i <= ns; i++) a.rs[i] = cuh[i];
         ord.resize(static_cast<size_t>(ns));
         std::iota(ord.begin(), ord.end(), 0);
         std::stable_sort(ord.begin(), ord.end(), [cuh](int32_t x, int32_t y) {
@@ -1202,10 +1312,7 @@ static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const i
         for (int64_t i = 0; i < ns; i++) a.order[i] = ord[static_cast<size_t>(i)];
         const int64_t nch = a.cb[ns];
         if (nch > 0) {
-            if ((err = cudaMemsetAsync(counter, 0, sizeof(uint32_t), stream)) != cudaSuccess) return err;
             prep_kernel<<<static_cast<unsigned>(nch * p.H), PT, PREP_SMEM, stream>>>(a);
-            if ((err = cudaGetLastError()) != cudaSuccess) return err;
-            exact_kernel<<<static_cast<unsigned>(std::min<int64_t>(nch * p.H, sms)), PT, EXACT_SMEM, stream>>>(a);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
         // every sequence gets a chain CTA: empty ones check their slot and return

@@ -102,6 +102,30 @@ __device__ __forceinline__ void gemm_ta(uint32_t d_tmem, uint32_t a_tmem, uint32
     }
 }
 
+// Two independent accumulators over the two K halves of one product (A in tensor memory,
+// fp16 pairs; B in shared memory): D0 = A[:, :Kd/2] B[:, :Kd/2]^T and
+// D1 = A[:, Kd/2:] B[:, Kd/2:]^T, their K steps issued alternately so that the two
+// accumulation chains overlap in the tensor pipe. D = D0 + D1.
+template <int N, int KD>
+__device__ __forceinline__ void gemm_ta_split(uint32_t d0, uint32_t d1, uint32_t a_tmem, uint32_t b_saddr,
+                                              uint32_t b_sbo)
+{
+    constexpr uint32_t ID = instr_desc(0, 128, N);
+    constexpr int HS = KD / 32;   // K steps of 16 per half
+#pragma unroll
+    for (int ks = 0; ks < HS; ks++) {
+        const uint32_t acc = ks > 0 ? 1u : 0u;
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const int kk = hh * HS + ks;
+            const uint64_t db = smem_desc(b_saddr + kk * 256, 128, b_sbo);
+            asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+                         :: "r"(hh ? d1 : d0), "r"(a_tmem + kk * 8), "l"(db), "r"(ID), "r"(acc));
+        }
+    }
+}
+
 // D[M=128, N] (+)= A[128, Kd] * B[N, Kd]^T in tf32 with A in tensor memory (one 32-bit
 // column per K element: one K step of 8 spans 8 columns) and B in shared memory.
 template <int N, int KD>
