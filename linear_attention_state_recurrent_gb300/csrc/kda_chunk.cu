@@ -90,6 +90,8 @@ constexpr uint32_t SM_BOFF = 32768;     // tf32 [96][64]  [B_1; B_2; B_3] of the
 constexpr uint32_t SM_BDIAG = 57344;    // tf32 [64][64]  K^R of the current half (SBO 2048); on the
                                         // pairwise path: fp16 [64][64] k^ then q^ (swizzled)
 constexpr uint32_t SM_SB = 73728;       // fp16 [192][64] Aqk rows 0..63, Kd^T rows 64..191 (SBO 1040)
+constexpr uint32_t SM_QSTG = SM_BH;     // bf16 [64][128] q, staged like raw_g (read before the gate pass)
+constexpr uint32_t SM_KSTG = SM_BH + 16384;   // bf16 [64][128] k
 constexpr uint32_t SM_TAB = SM_SB + 24 * SBO_SB;   // fp32 [4 blocks][8][64] per-(block, channel) constants
 constexpr uint32_t SM_TOT = SM_TAB + 8192;         // fp32 [8][64] sums of g over 8-row octets
 constexpr uint32_t SM_NRM = SM_TOT + 2048;         // fp32 [2][128] half-row |k|^2, |q|^2
@@ -503,8 +505,11 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     locate(bid, h, row0, n);
     unsigned char *rec = a.rec + static_cast<size_t>(bid) * REC_BYTES;
 
-    // ---- stage raw_g, prefetch the next unit's rows into L2, start the norm pass ----
+    // ---- stage raw_g, q and k (q and k in the b / B-operand regions, free until the gate
+    // pass), prefetch the next unit's rows into L2, start the norm pass ----
     stage_rows<PT>(sbase + SM_G, p.rg + row0 * p.ld_g + static_cast<int64_t>(h) * KD, p.ld_g, n, tid);
+    stage_rows<PT>(sbase + SM_QSTG, p.qkv + row0 * p.ld_qkv + static_cast<int64_t>(h) * KD, p.ld_qkv, n, tid);
+    stage_rows<PT>(sbase + SM_KSTG, p.qkv + row0 * p.ld_qkv + HK + static_cast<int64_t>(h) * KD, p.ld_qkv, n, tid);
     cp_async_commit();
     if (tid < 3 * C && bid + a.pf_stride < total) {
         int h2, n2;
@@ -517,16 +522,22 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" :: "l"(src) : "memory");
         }
     }
-    // own row: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31
+    if (tid < C) betas[tid] = tid < n ? sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h])) : 0.f;
+    const float expA = __expf(__ldg(p.A_log + h));
+    const float expA_l2e = expA * kLog2e, lb_l2e = p.lb * kLog2e;
+    cp_async_wait_all();
+    __syncthreads();
+    // own row from the staged tile: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31 (rows
+    // past the chunk were zero-filled)
     uint4 xr[2][4];
     {
-        const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + (kside ? HK : 0) + static_cast<int64_t>(h) * KD + 32 * sub;
+        const uint32_t stg = sbase + (kside ? SM_KSTG : SM_QSTG);
         float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
         for (int hf = 0; hf < 2; hf++)
 #pragma unroll
             for (int q4 = 0; q4 < 4; q4++) {
-                const uint4 v = r < n ? __ldg(reinterpret_cast<const uint4 *>(src + 64 * hf + 8 * q4)) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 v = ld_shared_u4(stg + st_off(r, 8 * hf + 4 * sub + q4));
                 xr[hf][q4] = v;
                 float f[8];
                 unpack_bf16x8(v, f);
@@ -535,11 +546,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             }
         nrm[sub * 128 + l] = ss.x + ss.y;
     }
-    if (tid < C) betas[tid] = tid < n ? sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h])) : 0.f;
-    const float expA = __expf(__ldg(p.A_log + h));
-    const float expA_l2e = expA * kLog2e, lb_l2e = p.lb * kLog2e;
-    cp_async_wait_all();
-    __syncthreads();
+    __syncthreads();   // the half-row norms; the staged q and k are consumed
     // rows past the chunk hold zeros; their norm factor is 0 so that eps = 0 gives no NaN
     auto norm_of = [&](int lane_idx, int row) -> float {
         const float f = (lane_idx < 64 ? 1.f : p.scale) * rsqrtf(nrm[lane_idx] + nrm[128 + lane_idx] + p.eps);
