@@ -198,7 +198,9 @@ def decode_config(world):
                         "[128,8] block table (stride 8), lower_bound=-5.0",
             "l2": "inputs larger than L2: steps rotate over 4 disjoint 128-slot "
                   "sets (256 MiB read per step, 1 GiB between reuses)",
-            "parallelism": f"replicas x{world} (no collective)"}
+            "parallelism": "1 GPU" if world == 1 else
+                           f"heads split over {world} ranks (tensor-parallel layout, each rank its own pool of "
+                           "its heads, no collective on the data path)"}
 
 
 # sequences of the serving decode that one reference step runs (a bounded sample: the
@@ -245,7 +247,9 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_decode(w, sets, budget_s=10.0):
+def cpu_baseline_decode(w, sets, budget_s=10.0, budget_1t_s=5.0):
+    """The fp64 oracle on the host: all cores (OpenMP over (sequence, head)) on full
+    serving-decode calls, and one thread on a bounded sample of them."""
     from oracle import kda_oracle as ko
     cores = ko.max_threads()
     ko.run(w, slots=sets[0])
@@ -256,9 +260,24 @@ def cpu_baseline_decode(w, sets, budget_s=10.0):
         dt = time.perf_counter() - t0
         if dt >= budget_s:
             break
+    # single thread: 8 of the 128 sequences per call, rotating through all of them
+    bounds_all = w.seq_bounds()
+    per = 8
+    m, t1 = 0, time.perf_counter()
+    while True:
+        first = (per * m) % w.num_entries
+        idx = [(first + k) % w.num_entries for k in range(per)]
+        ko.run(w, bounds=[bounds_all[e] for e in idx], slots=sets[m % 4][idx], nthreads=1)
+        m += 1
+        dt1 = time.perf_counter() - t1
+        if dt1 >= budget_1t_s:
+            break
+    one = 2 * 4 * w.K * w.V * w.H * per * m / dt1 / 1e9
     return {"value": w.state_bytes_per_call() * n / dt / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{n} full serving-decode calls (128 seqs x 32 heads) in {dt:.1f} s, fp64, OpenMP over (seq, head)"}
+            "sample": f"{n} full serving-decode calls (128 seqs x 32 heads) in {dt:.1f} s, fp64, OpenMP over (seq, head)",
+            "single_thread": {"value": one, "unit": "GB/s", "cores": 1,
+                              "sample": f"{m} calls of {per} of the 128 sequences (x 32 heads) in {dt1:.1f} s, one thread"}}
 
 
 # ---------------------------------------------------------------------------
@@ -275,6 +294,9 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--workload", choices=["decode", "prefill", "spec", "spec_ckpt", "fused_decode", "fused_spec", "mixed"], default="decode",
                     help="decode (default) is the headline line; the others time one row alone")
+    ap.add_argument("--prefill-lengths", default=None,
+                    help="comma-separated sequence lengths for --workload prefill (H=32, K=V=128; "
+                         "default: the seed-1 lengths, 33,494 tokens), e.g. a smaller case for profiling")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -295,7 +317,14 @@ def main():
         return
 
     # ---- headline: serving decode ----
-    w = wl.serving_decode(-5.0)
+    # Under torchrun the heads are split across the ranks as tensor parallelism does: rank
+    # r holds heads shard_units(H, world, r) of every slot (its own pool) and runs the same
+    # call on them; nothing crosses ranks on the data path.
+    w_full = wl.serving_decode(-5.0)
+    w = w_full
+    if world > 1:
+        lo, hi = shard_units(w_full.H, world, rank)
+        w = wl.shard_heads(w_full, lo, hi)
     dw = wl.DeviceWorkload(w, dev)
     sets = wl.serving_decode_index_sets(w)
     idx_dev = [torch.from_numpy(s).to(dev) for s in sets]
@@ -329,8 +358,9 @@ def main():
     barrier(world)
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_step = ms_total / args.steps
-    state_bytes = w.state_bytes_per_call()
-    value = state_bytes * world * args.steps / (ms_total * 1e-3) / 1e9
+    state_bytes = w.state_bytes_per_call()          # this rank's heads
+    total_bytes = w_full.state_bytes_per_call()     # all ranks together
+    value = total_bytes * args.steps / (ms_total * 1e-3) / 1e9
     achieved = state_bytes / (ms_step * 1e-3) / 1e9
     sha = source_sha("kda_recurrent.cu", "kda_common.cuh")
     traffic = ncu_traffic("recurrent_kernel<128,128> serving_decode", sha)
@@ -370,7 +400,8 @@ def main():
         dt = time.perf_counter() - t0
         h2d = sum(t.numel() * t.element_size() for t in (h_qkv, h_g, h_b, h_idx[0]))
         d2h = h_out.numel() * h_out.element_size()
-        e2e = {"value": state_bytes * e2e_steps / dt / 1e9 * world, "unit": "GB/s",
+        dt = max_over_ranks(dt, world)
+        e2e = {"value": total_bytes * e2e_steps / dt / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
                "api": "kda.kda_packed_decode (pinned host -> device copies, call, device -> host copy, stream sync each step)"}
@@ -378,7 +409,7 @@ def main():
     # ---- other rows (rank 0 only) ----
     secondary = {}
     if rank == 0 and not args.no_secondary:
-        secondary = measure_secondary(torch, kda, wl, dev, stream, pk)
+        secondary = measure_secondary(torch, kda, wl, dev, stream, pk, local)
 
     del dw, states, call_args
     torch.cuda.empty_cache()
@@ -390,7 +421,8 @@ def main():
     if rank == 0:
         line = {"metric": "KDA decode state-bytes GB/s", "value": value, "unit": "GB/s",
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "strong" if world > 1 else "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": decode_config(world),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -406,7 +438,11 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
     """One non-headline row alone: chunked prefill, spec-verify or mixed batch, timed over
     --steps calls after --warmup calls (the same calls the secondary fields time)."""
     if args.workload == "prefill":
-        w = wl.chunked_prefill(None)
+        if args.prefill_lengths:
+            w = wl.varlen_case([int(x) for x in args.prefill_lengths.split(",")], 32, 128, 128, seed=1,
+                               name="prefill " + args.prefill_lengths)
+        else:
+            w = wl.chunked_prefill(None)
         metric, unit = "chunk-prefill tokens/s", "tokens/s"
     elif args.workload == "mixed":
         w = wl.mixed_batch()
@@ -458,9 +494,9 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "tokens": w.N, "H": w.H, "K": w.K, "V": w.V},
-            "clocks": clk.summary(), "gpu_launches": args.steps * (2 if args.workload == "mixed" else 1)}
+            "clocks": clk.summary(), "gpu_launches": args.steps * {"prefill": 2, "mixed": 3}.get(args.workload, 1)}
     if args.workload == "prefill":
-        flops = prefill_alg_flops(wl.PREFILL_LENGTHS_SEED1, w.H, w.K, w.V)
+        flops = prefill_alg_flops([b - a for a, b in w.seq_bounds()], w.H, w.K, w.V)
         line["tflops_algorithmic"] = flops / (ms * 1e-3) / 1e12
         line["frac_bf16_peak"] = line["tflops_algorithmic"] / pk["bf16_tflops"]
         line["frac_hbm_min_bytes"] = prefill_min_bytes(w) / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]
@@ -468,12 +504,13 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def spec_call_args(kda, w, dw, out, stream_handle):
+def spec_call_args(kda, w, dw, out, stream_handle, indices=None):
     """Pre-marshalled C-ABI arguments of one kda_spec_verify call (kda_spec_verify_checkpoints
     for a checkpoint workload, kda_fused_decode / kda_fused_spec_verify for a fused one),
-    kept alive with the structs they point to. Returns (function, args, keep-alive)."""
+    kept alive with the structs they point to. `indices` (a device int32 tensor) replaces
+    the workload's state-index view. Returns (function, args, keep-alive)."""
     hd = kda.make_heads(dw.A_log, dw.dt_bias, w.lower_bound, w.K, w.V, w.scale, w.eps)
-    st = kda.make_state(dw.pool_view(), dw.indices_view(), w.null_slot)
+    st = kda.make_state(dw.pool_view(), dw.indices_view() if indices is None else indices, w.null_slot)
     head = (ctypes.c_void_p(dw.mixed_qkv.data_ptr()), dw.mixed_qkv.stride(0),
             ctypes.c_void_p(dw.raw_g.data_ptr()), dw.raw_g.stride(0),
             ctypes.c_void_p(dw.raw_beta.data_ptr()), dw.raw_beta.stride(0),
@@ -494,19 +531,42 @@ def spec_call_args(kda, w, dw, out, stream_handle):
     return kda.lib.kda_spec_verify, head + tail, (hd, st)
 
 
-def time_spec_graph(torch, kda, w, dw, out, calls=20, replays=50):
+def spec_index_sets(w, count):
+    """`count` disjoint state-index arrays for a spec-verify workload: every real request
+    gets fresh slots from 1 .. num_slots - 1 in each set, padding requests keep the null
+    slot. Rotating through them between calls keeps a call's state out of L2."""
+    import numpy as np
+    idx = w.indices()
+    real = np.nonzero(idx != w.null_slot)[0]
+    avail = np.array([s for s in range(w.num_slots) if s != w.null_slot], dtype=np.int32)
+    rng = np.random.default_rng(777)
+    rng.shuffle(avail)
+    assert count * len(real) <= len(avail)
+    sets = []
+    for i in range(count):
+        a = np.full(w.num_entries, w.null_slot, dtype=np.int32)
+        a[real] = avail[i * len(real):(i + 1) * len(real)]
+        sets.append(a)
+    return sets
+
+
+def time_spec_graph(torch, kda, w, dw, out, calls=20, replays=50, index_sets=None):
     """Spec-verify calls are a few microseconds of GPU time, far below the host cost of a
-    Python call, so they are timed as replays of a CUDA graph of `calls` launches."""
+    Python call, so they are timed as replays of a CUDA graph of `calls` launches. With
+    `index_sets` (device int32 tensors) consecutive calls rotate through them."""
     cap = torch.cuda.Stream()
-    fn, args, keep = spec_call_args(kda, w, dw, out, cap.cuda_stream)
+    marsh = [spec_call_args(kda, w, dw, out, cap.cuda_stream, ix) for ix in (index_sets or [None])]
+    keep = marsh
     with torch.cuda.stream(cap):
         for _ in range(3):
-            if fn(*args):
-                raise RuntimeError(kda.last_error())
+            for fn, args, _k in marsh:
+                if fn(*args):
+                    raise RuntimeError(kda.last_error())
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):
-        for _ in range(calls):
+        for i in range(calls):
+            fn, args, _k = marsh[i % len(marsh)]
             fn(*args)
     stream = torch.cuda.current_stream()
     for _ in range(3):
@@ -536,63 +596,48 @@ def spec_state_bytes(w):
     return total
 
 
-def time_calls(torch, fn, stream, n, warmup=2):
+def spec_leg(torch, kda, w, dw, out, pk, desc, rotate_sets):
+    """A spec-verify-shaped leg: L2-cold (rotating disjoint slot sets across the graph's
+    calls, when the workload leaves room for them) and warm (the same slots every call)."""
+    sbytes = spec_state_bytes(w)
+    res = {"workload": desc}
+    if rotate_sets:
+        sets = [torch.from_numpy(a).to(dw.mixed_qkv.device) for a in spec_index_sets(w, rotate_sets)]
+        ms = time_spec_graph(torch, kda, w, dw, out, index_sets=sets)
+        dw.reset_pool()
+        res.update({"us_per_call": ms * 1e3, "state_gbs": sbytes / (ms * 1e-3) / 1e9,
+                    "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                    "timing": f"L2-cold: CUDA graph of 20 calls rotating over {rotate_sets} disjoint slot sets "
+                              f"({rotate_sets - 1} calls' state, {(rotate_sets - 1) * sbytes / 1e6:.0f} MB, "
+                              "between reuses of a slot), 50 replays"})
+    ms_w = time_spec_graph(torch, kda, w, dw, out)
+    warm = {"us_per_call": ms_w * 1e3, "state_gbs": sbytes / (ms_w * 1e-3) / 1e9,
+            "timing": "L2-warm: CUDA graph of 20 calls on the same slots, 50 replays"}
+    if rotate_sets:
+        res["warm"] = warm
+    else:
+        res.update(warm)
+        res["frac_hbm"] = warm["state_gbs"] / pk["hbm_gbs"]
+    return res
+
+
+def time_calls_clocked(torch, fn, stream, n, warmup, local):
+    """Mean ms per call of `n` calls after `warmup`, CUDA events on `stream`, SM clocks
+    sampled during the timed region."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(n):
-        fn()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    return ev0.elapsed_time(ev1) / n
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(n):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / n, clk.summary()
 
 
-def measure_secondary(torch, kda, wl, dev, stream, pk):
-    res = {}
-    # spec verify: 16 requests x 8 tokens
-    w = wl.spec_verify()
-    dw = wl.DeviceWorkload(w, dev)
-    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
-    ms = time_spec_graph(torch, kda, w, dw, out)
-    sbytes = spec_state_bytes(w)
-    res["spec_verify"] = {"workload": "16 requests x 8 tokens, H=32, K=V=128, 2 padding requests on the null slot",
-                          "us_per_call": ms * 1e3, "state_gbs": sbytes / (ms * 1e-3) / 1e9,
-                          "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                          "timing": "CUDA graph of 20 calls, 50 replays"}
-    del dw
-    # spec verify with per-token checkpoints: 16 requests x 8 tokens, 8 writes per request
-    w = wl.spec_checkpoints()
-    dw = wl.DeviceWorkload(w, dev)
-    ms = time_spec_graph(torch, kda, w, dw, out)
-    sbytes = spec_state_bytes(w)
-    res["spec_verify_checkpoints"] = {
-        "workload": "16 requests x 8 tokens, H=32, K=V=128, state stored after every token "
-                    "(block-table row of 8 slots), 2 padding requests on the null slot",
-        "us_per_call": ms * 1e3, "state_gbs": sbytes / (ms * 1e-3) / 1e9,
-        "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-        "timing": "CUDA graph of 20 calls, 50 replays"}
-    del dw
-    # fused layer tail (conv W=4 -> recurrence -> gated RMSNorm): serving decode, spec 16x8
-    for key, base, desc in (
-            ("fused_decode", wl.serving_decode(-5.0),
-             "128 seqs, H=32, K=V=128, conv width 4, gated RMSNorm, index stride 8"),
-            ("fused_spec_verify", wl.spec_verify(),
-             "16 requests x 8 tokens, H=32, K=V=128, conv width 4, gated RMSNorm, 2 padding")):
-        w = wl.with_layer_tail(base, seed=99)
-        dw = wl.DeviceWorkload(w, dev)
-        fo = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
-        ms = time_spec_graph(torch, kda, w, dw, fo)
-        sbytes = spec_state_bytes(w)
-        res[key] = {"workload": desc, "us_per_call": ms * 1e3,
-                    "state_gbs": sbytes / (ms * 1e-3) / 1e9,
-                    "frac_hbm": sbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                    "bytes": "KDA state and conv state, read + written (null slot read only)",
-                    "timing": "CUDA graph of 20 calls, 50 replays"}
-        del dw, fo
-    # chunked prefill: seed-1 lengths, 33,494 tokens
-    w = wl.chunked_prefill(None)
+def prefill_leg(torch, kda, wl, w, dev, stream, pk, lower_bound, local, calls=20):
     dw = wl.DeviceWorkload(w, dev)
     out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
     cu_h = torch.from_numpy(w.cu_seqlens)
@@ -600,35 +645,89 @@ def measure_secondary(torch, kda, wl, dev, stream, pk):
     ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
 
     def pf():
-        kda.kda_chunk_prefill(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, None,
+        kda.kda_chunk_prefill(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, lower_bound,
                               dw.pool_view(), dw.indices_view(), dw.cu, cu_seqlens_host=cu_h,
                               scale=w.scale, out=out, workspace=ws)
-    ms = time_calls(torch, pf, stream, 5, 2)
+    ms, clocks = time_calls_clocked(torch, pf, stream, calls, 3, local)
     flops = prefill_alg_flops(wl.PREFILL_LENGTHS_SEED1, w.H, w.K, w.V)
     mb = prefill_min_bytes(w)
-    res["chunk_prefill"] = {"metric": "chunk-prefill tokens/s", "value": w.N / (ms * 1e-3),
-                            "unit": "tokens/s", "ms_per_call": ms,
-                            "workload": "8 seqs (seed-1 lengths, 33,494 tokens), H=32, K=V=128, chunk 64, lower_bound=None",
-                            "tflops_algorithmic": flops / (ms * 1e-3) / 1e12,
-                            "frac_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
-                            "hbm_gbs_min_bytes": mb / (ms * 1e-3) / 1e9,
-                            "frac_hbm": mb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                            "flop_count": "6cKV + c^2(3K+2V) + c^3/3 per (chunk of c rows, head)"}
-    del dw, ws
+    sha = source_sha("kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh")
+    traffic = ncu_traffic("prefill (prep_kernel + chain_kernel) chunked_prefill", sha)
+    achieved = mb / (ms * 1e-3) / 1e9
+    res = {"metric": "chunk-prefill tokens/s", "value": w.N / (ms * 1e-3), "unit": "tokens/s",
+           "ms_per_call": ms, "calls": calls,
+           "workload": "8 seqs (seed-1 lengths, 33,494 tokens), H=32, K=V=128, chunk 64, "
+                       f"lower_bound={lower_bound}",
+           "tflops_algorithmic": flops / (ms * 1e-3) / 1e12,
+           "frac_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+           "hbm_gbs_min_bytes": achieved, "frac_hbm": achieved / pk["hbm_gbs"],
+           "flop_count": "6cKV + c^2(3K+2V) + c^3/3 per (chunk of c rows, head)",
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                        "peak_source": f"{pk['source']} HBM copy bandwidth (of {pk['source']})",
+                        "algorithmic_bytes_per_call": mb,
+                        "kernels": "kda::chunk::prep_kernel (one CTA per (chunk, head)) then kda::chunk::chain_kernel",
+                        "tensor_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]},
+           "clocks": clocks}
+    del dw, ws, out
+    return res
+
+
+def measure_secondary(torch, kda, wl, dev, stream, pk, local=0):
+    res = {}
+    out = torch.empty(128, 32 * 128, dtype=torch.bfloat16, device=dev)
+    # spec verify: 16 requests x 8 tokens, L2-cold over 8 disjoint slot sets
+    w = wl.spec_verify()
+    dw = wl.DeviceWorkload(w, dev)
+    res["spec_verify"] = spec_leg(torch, kda, w, dw, out, pk,
+                                  "16 requests x 8 tokens, H=32, K=V=128, 2 padding requests on the null slot", 8)
+    del dw
+    # spec verify with per-token checkpoints: 16 requests x 8 tokens, 8 writes per request
+    # (264 MB of state per call: no call is served from L2)
+    w = wl.spec_checkpoints()
+    dw = wl.DeviceWorkload(w, dev)
+    res["spec_verify_checkpoints"] = spec_leg(
+        torch, kda, w, dw, out, pk,
+        "16 requests x 8 tokens, H=32, K=V=128, state stored after every token (block-table row of 8 slots), "
+        "2 padding requests on the null slot", 0)
+    del dw
+    # fused layer tail (conv W=4 -> recurrence -> gated RMSNorm): serving decode, spec 16x8
+    for key, base, desc, rot in (
+            ("fused_decode", wl.serving_decode(-5.0),
+             "128 seqs, H=32, K=V=128, conv width 4, gated RMSNorm, index stride 8", 0),
+            ("fused_spec_verify", wl.spec_verify(),
+             "16 requests x 8 tokens, H=32, K=V=128, conv width 4, gated RMSNorm, 2 padding", 8)):
+        w = wl.with_layer_tail(base, seed=99)
+        dw = wl.DeviceWorkload(w, dev)
+        fo = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+        r = spec_leg(torch, kda, w, dw, fo, pk, desc, rot)
+        r["bytes"] = "KDA state and conv state, read + written (null slot read only)"
+        res[key] = r
+        del dw, fo
+    # chunked prefill: seed-1 lengths, 33,494 tokens, both gate forms
+    w = wl.chunked_prefill(None)
+    res["chunk_prefill"] = prefill_leg(torch, kda, wl, w, dev, stream, pk, None, local)
+    res["chunk_prefill_lower_bound"] = prefill_leg(torch, kda, wl, wl.chunked_prefill(-5.0), dev, stream, pk,
+                                                   -5.0, local)
     # mixed batch
     w = wl.mixed_batch()
     dw = wl.DeviceWorkload(w, dev)
     out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
     cu_h = torch.from_numpy(w.cu_seqlens)
+    nb = kda.kda_chunk_prefill_workspace_bytes(cu_h[w.num_decodes:], w.H, w.K, w.V)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
 
     def mb_call():
         kda.kda_mixed_batch(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, None,
                             dw.pool_view(), dw.indices_view(), dw.cu, w.num_decodes,
-                            cu_seqlens_host=cu_h, scale=w.scale, out=out)
-    ms = time_calls(torch, mb_call, stream, 5, 2)
+                            cu_seqlens_host=cu_h, scale=w.scale, out=out, workspace=ws)
+    ms, clocks = time_calls_clocked(torch, mb_call, stream, 20, 3, local)
     res["mixed_batch"] = {"workload": "96 decodes + 4 x 4096 prefill tokens, H=32, K=V=128, index stride 4",
-                          "tokens_per_s": w.N / (ms * 1e-3), "ms_per_call": ms}
-    del dw
+                          "tokens_per_s": w.N / (ms * 1e-3), "ms_per_call": ms, "calls": 20,
+                          "algorithmic_bytes": 1095505920,
+                          "hbm_gbs": 1095505920 / (ms * 1e-3) / 1e9,
+                          "frac_hbm": 1095505920 / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "clocks": clocks}
+    del dw, ws
     return res
 
 

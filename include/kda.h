@@ -78,6 +78,10 @@ extern "C" {
 
 #define KDA_ERRFLAG_SLOT_RANGE 1u /* bit 0 of *err_flags: a state index was >= num_slots */
 #define KDA_ERRFLAG_TIMEOUT 2u    /* bit 1: a device-side wait gave up after ~2 s (results invalid) */
+#define KDA_ERRFLAG_RANGE 4u      /* bit 2: a value the chunked prefill carries in fp16 (a state entry,
+                                     V - K^G S or an intra-chunk operand) reached |x| >= 65504; the
+                                     affected outputs and states are invalid (kda_chunk_prefill and
+                                     kda_mixed_batch at K = V = 128) */
 
 /* Per-layer head parameters shared by every call. */
 typedef struct kda_heads {
@@ -259,9 +263,22 @@ size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t
  * launch; mixed_qkv, raw_g, raw_beta and out must hold cu_seqlens[num_seqs] rows.
  * chunk_size must be 64. mixed_qkv, raw_g and out must be 16-byte aligned with ld_qkv,
  * ld_g and ld_out multiples of 8 (the tensor-core path moves them in 16-byte vectors).
- * `workspace` (device, 256-byte aligned) must hold kda_chunk_prefill_workspace_bytes(...)
- * bytes; it may be NULL when that is 0 (this version's kernels need none).
- * Zero-length sequences are allowed: their slot is left untouched.
+ * `workspace` (device, 256-byte aligned, owned by the caller) must hold
+ * kda_chunk_prefill_workspace_bytes(...) bytes: at K = V = 128 one 57,856-byte record per
+ * (chunk of 64 rows, head), written by the call's first kernel (the intra-chunk pass over
+ * every chunk in parallel) and read by its second (the per-sequence state chain); its
+ * contents are scratch between calls. It may be NULL when the size is 0 (other head sizes).
+ * Calls that share a workspace must not overlap on the device. At K = V = 128 the call is
+ * two launches per 1024 sequences.
+ * Zero-length sequences are allowed: their slot is left untouched (a slot >= num_slots is
+ * still flagged).
+ * Precision and range (K = V = 128): the tensor-core products take fp16 / tf32 operands with
+ * fp32 accumulation; the state and V - K^G S enter them in fp16, so state entries and values
+ * must stay below 65504 in magnitude. Beyond that the call sets KDA_ERRFLAG_RANGE in
+ * *err_flags and its results are invalid (the fp32 pool itself holds any value).
+ * Bounded waits: a tensor-core wait that gives up (~2 s) sets KDA_ERRFLAG_TIMEOUT and leaves
+ * that sequence's outputs and state unwritten; with err_flags == NULL neither condition is
+ * reported, so pass an error word wherever results must be trusted.
  */
 int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
                       int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
@@ -276,10 +293,12 @@ int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t 
  * length-1 sequences). Sequences 0..num_decodes-1 must have length 1 and take the
  * recurrent decode path; sequences num_decodes..num_decodes+num_prefills-1 take
  * the chunked prefill path. One cu_seqlens (device + host copies) and one strided
- * index view cover all of them, decodes first. At K = V = 128 both run in one launch
- * (the decodes on worker CTAs beside the prefill chains); other head sizes take two
- * launches in turn. Workspace as for kda_chunk_prefill over the prefill sequences:
+ * index view cover all of them, decodes first. The decodes run the packed-decode kernel
+ * (the same code path as kda_packed_decode), then the prefills run kda_chunk_prefill's
+ * kernels, on `stream` in that order. Workspace as for kda_chunk_prefill over the prefill
+ * sequences:
  * kda_chunk_prefill_workspace_bytes(cu_seqlens_host + num_decodes, num_prefills, ...).
+ * The prefills' range limit and error bits are kda_chunk_prefill's.
  */
 int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
                     int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,

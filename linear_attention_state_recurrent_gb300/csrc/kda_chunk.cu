@@ -928,6 +928,10 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         tc::tmem_ld16(tlane + TM_W2 + 32 * sub + 16, v[1]);
         tc::tmem_ld_wait();
         unsigned char *mm = rec + REC_MM;
+        bool bad = false;   // [M1; M2] travel in fp16
+#pragma unroll
+        for (int u = 0; u < 16; u++) bad |= !(fabsf(v[0][u]) < 65504.f) || !(fabsf(v[1][u]) < 65504.f);
+        if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, kErrRange);
 #pragma unroll
         for (int q = 0; q < 4; q++)
             *reinterpret_cast<uint4 *>(mm + tc::core_offset(64 + l, 32 * sub + 8 * q, 64, 2)) = pack8_f16(&v[q >> 1][8 * (q & 1)]);
@@ -1060,15 +1064,23 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
     uint32_t phc = 0;
     int nprev = 0;
     int64_t prev0 = row0;
+    // a value that left the fp16 range on the way (the state, Y or an operand) reaches the
+    // outputs and the state as Inf or NaN: flag it (once per warp)
+    auto flag_nonfinite = [&](bool bad) {
+        if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, kErrRange);
+    };
     auto store_o = [&](const float (&ov)[2][16], int64_t cs, int nrows) {
         uint16_t *orow = p.out + cs * p.ld_out + static_cast<int64_t>(h) * VD + j;
+        bool bad = false;
 #pragma unroll
         for (int q = 0; q < 2; q++)
 #pragma unroll
             for (int u = 0; u < 16; u++) {
                 const int rr = 32 * sub + 16 * q + u;
+                bad |= !(fabsf(ov[q][u]) < INFINITY) && rr < nrows;
                 if (rr < nrows) orow[static_cast<int64_t>(rr) * p.ld_out] = f32_to_bf16(ov[q][u]);
             }
+        flag_nonfinite(bad);
     };
     for (int c = 0; c < nch; c++) {
         const int b = c & 1;
@@ -1208,6 +1220,7 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
             for (int u = 0; u < 16; u++) ov[q][u] += ow[q][u];
         store_o(ov, prev0, nprev);
         if (writable) {
+            bool bad = false;
 #pragma unroll
             for (int cc = 0; cc < 64; cc += 16) {
                 float v[16];
@@ -1215,8 +1228,12 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
                 tc::tmem_ld16(tlane + TC_S + cidx, v);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; u++) tile[static_cast<int64_t>(cidx + u) * VD + j] = v[u];
+                for (int u = 0; u < 16; u++) {
+                    bad |= !(fabsf(v[u]) < INFINITY);
+                    tile[static_cast<int64_t>(cidx + u) * VD + j] = v[u];
+                }
             }
+            flag_nonfinite(bad);
         }
     } else {
         // a wait gave up: record it, then let the copies this CTA started finish (bounded)

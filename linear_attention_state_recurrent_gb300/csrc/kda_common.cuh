@@ -32,6 +32,7 @@ struct TailParams {
 
 constexpr uint32_t kErrSlotRange = 1u;
 constexpr uint32_t kErrTimeout = 2u;   // a bounded wait on the tensor cores gave up
+constexpr uint32_t kErrRange = 4u;     // a value the chunked path carries in fp16 left its range
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b)
 {

@@ -170,7 +170,17 @@ def make_state(state_pool, state_indices, null_slot=-1):
 def _out(out, N, H, V, device):
     if out is None:
         out = torch.empty(N, H * V, dtype=torch.bfloat16, device=device)
+    elif out.dim() != 2 or out.shape[0] < N:
+        raise ValueError(f"out must have at least {N} rows")
     return out, _rows(out, "out")
+
+
+def _need_rows(N, **tensors):
+    """Every per-token input must hold at least N rows (the C ABI has no row counts, so a
+    short tensor would be read past its end on the device)."""
+    for name, t in tensors.items():
+        if t is not None and (t.dim() < 1 or t.shape[0] < N):
+            raise ValueError(f"{name} must have at least {N} rows (got {tuple(t.shape)})")
 
 
 def kda_gate(raw_g, raw_beta, A_log, dt_bias=None, lower_bound=None, *, K=None, g_out=None,
@@ -200,6 +210,7 @@ def kda_packed_decode(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, i
     st = make_state(initial_state, state_indices, null_slot)
     if state_indices.shape[0] < N:
         raise ValueError("state_indices has fewer entries than sequences")
+    _need_rows(N, raw_g=raw_g, raw_beta=raw_beta)
     out, ld_out = _out(out, N, H, V, mixed_qkv.device)
     _check(lib.kda_packed_decode(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
                                  _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
@@ -221,6 +232,7 @@ def kda_spec_verify(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, ini
     st = make_state(initial_state, state_indices, null_slot)
     if state_indices.shape[0] < R:
         raise ValueError("state_indices has fewer entries than requests")
+    _need_rows(N, raw_g=raw_g, raw_beta=raw_beta)
     out, ld_out = _out(out, N, H, V, mixed_qkv.device)
     _check(lib.kda_spec_verify(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
                                _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
@@ -253,6 +265,7 @@ def kda_spec_verify_checkpoints(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lowe
         raise ValueError("num_accepted must be a contiguous int32 tensor with a count per request")
     hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
     st = make_state(state_pool, block_table[:, 0], null_slot)
+    _need_rows(N, raw_g=raw_g, raw_beta=raw_beta)
     out, ld_out = _out(out, N, H, V, mixed_qkv.device)
     _check(lib.kda_spec_verify_checkpoints(
         _ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g), _rows(raw_g, "raw_g"),
@@ -295,6 +308,7 @@ def _fused(name, mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, initia
     st = make_state(initial_state, state_indices, null_slot)
     if state_indices.shape[0] < E:
         raise ValueError("state_indices has fewer entries than requests")
+    _need_rows(N, raw_g=raw_g, raw_beta=raw_beta)
     if conv is not None and conv[2].shape[0] < initial_state.shape[0]:
         raise ValueError("conv_state must have a slot for every state slot")
     cv = None if conv is None else make_conv(*conv)
@@ -340,11 +354,26 @@ def kda_selftest_bounded_wait(err_flags, stream=None):
 
 
 def _host_cu(cu_seqlens, cu_seqlens_host):
+    """The host copy of cu_seqlens (read from the device when not given; a given copy must
+    hold the same values as the device tensor, which the library sizes its launch from)."""
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
         raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor")
     if cu_seqlens_host is None:
         cu_seqlens_host = cu_seqlens.cpu()
-    return cu_seqlens_host.to(torch.int32).contiguous()
+    cu = cu_seqlens_host.to(torch.int32).contiguous()
+    if cu.numel() != cu_seqlens.numel():
+        raise ValueError("cu_seqlens_host and cu_seqlens must have the same length")
+    return cu
+
+
+def _check_varlen(cu_h, N, S, state_indices, **tensors):
+    """Sequence bounds inside the N rows, one state index per sequence, N rows everywhere."""
+    if S > 0 and (int(cu_h[0]) < 0 or int(cu_h[-1]) > N):
+        raise ValueError(f"cu_seqlens must start at >= 0 and end at <= {N} rows "
+                         f"(got {int(cu_h[0])} .. {int(cu_h[-1])})")
+    if state_indices.shape[0] < S:
+        raise ValueError(f"state_indices has fewer entries ({state_indices.shape[0]}) than sequences ({S})")
+    _need_rows(N, **tensors)
 
 
 def kda_chunk_prefill_workspace_bytes(cu_seqlens_host, H, K, V, chunk_size=64, num_seqs=None):
@@ -375,6 +404,7 @@ def kda_chunk_prefill(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, i
     S = cu_h.numel() - 1
     hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
     st = make_state(initial_state, state_indices, null_slot)
+    _check_varlen(cu_h, N, S, state_indices, raw_g=raw_g, raw_beta=raw_beta)
     out, ld_out = _out(out, N, H, V, mixed_qkv.device)
     nb = kda_chunk_prefill_workspace_bytes(cu_h, H, K, V, chunk_size)
     ws, ws_bytes = _workspace(nb, mixed_qkv.device, workspace)
@@ -400,6 +430,7 @@ def kda_mixed_batch(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, ini
     P = S - num_decodes
     hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
     st = make_state(initial_state, state_indices, null_slot)
+    _check_varlen(cu_h, N, S, state_indices, raw_g=raw_g, raw_beta=raw_beta)
     out, ld_out = _out(out, N, H, V, mixed_qkv.device)
     nb = kda_chunk_prefill_workspace_bytes(cu_h[num_decodes:], H, K, V, 64, num_seqs=P)
     ws, ws_bytes = _workspace(nb, mixed_qkv.device, workspace)

@@ -244,6 +244,28 @@ def serving_decode(lower_bound=-5.0, seed: int = 2) -> Workload:
     return w
 
 
+def shard_heads(w: Workload, lo: int, hi: int) -> Workload:
+    """The same call restricted to heads [lo, hi): what one tensor-parallel rank holds.
+    Heads are independent in the recurrence (each has its own state tile, gate and
+    normalisation), so the ranks' results together are the unsharded call's."""
+    H, K, V, N = w.H, w.K, w.V, w.N
+    hs = hi - lo
+    q = w.mixed_qkv[:, lo * K:hi * K]
+    k = w.mixed_qkv[:, H * K + lo * K:H * K + hi * K]
+    v = w.mixed_qkv[:, 2 * H * K + lo * V:2 * H * K + hi * V]
+    pool = w.pool[:, :H * K * V].reshape(w.num_slots, H, K * V)[:, lo:hi].reshape(w.num_slots, hs * K * V)
+    fields = dict(w.__dict__)
+    fields.update(name=f"{w.name}[heads {lo}:{hi}]", H=hs,
+                  mixed_qkv=np.ascontiguousarray(np.concatenate([q, k, v], axis=1)),
+                  raw_g=np.ascontiguousarray(w.raw_g[:, lo * K:hi * K]),
+                  raw_beta=np.ascontiguousarray(w.raw_beta[:, lo:hi]),
+                  A_log=np.ascontiguousarray(w.A_log[lo:hi]),
+                  dt_bias=None if w.dt_bias is None else np.ascontiguousarray(w.dt_bias[lo * K:hi * K]),
+                  pool=np.ascontiguousarray(pool))
+    assert not w.fused, "head sharding covers the plain calls"
+    return Workload(**fields)
+
+
 def serving_decode_index_sets(w: Workload, count: int = 4) -> list[np.ndarray]:
     """Disjoint sets of 128 slots (the first is the workload's own column 0), used by the
     bench to rotate which slots a step touches so that no step reads state from L2."""

@@ -27,9 +27,19 @@ def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
 
 
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    return np.exp2(np.floor(np.log2(np.maximum(np.abs(x), 1e-30))) - 7)
+
+
 def check(dw: DeviceWorkload, out: torch.Tensor, ref: ko.OracleResult, *, fp32_path: bool,
-          rows=None, label="", max_abs=MAX_ABS):
-    """Compares one call's GPU results with the oracle. Returns a dict of measured errors."""
+          rows=None, label="", max_abs=MAX_ABS, elementwise_abs=False):
+    """Compares one call's GPU results with the oracle. Returns a dict of measured errors.
+
+    elementwise_abs: the max-abs bar becomes per element max(MAX_ABS, half a bf16 ulp of
+    the larger of |exact| and |result| + 1e-4 |exact|): rounding the output once to bf16
+    costs up to half an ulp, which exceeds MAX_ABS only where |o| >= 4 (normalised
+    outputs)."""
     w = dw.w
     torch.cuda.synchronize()
     h_lo, h_hi = ref.heads
@@ -43,7 +53,12 @@ def check(dw: DeviceWorkload, out: torch.Tensor, ref: ko.OracleResult, *, fp32_p
     assert np.all(np.isfinite(exp)), f"{label}: oracle produced non-finite values"
     res = {"out_rel_l2": rel_l2(got, exp), "out_max_abs": float(np.abs(got - exp).max(initial=0.0))}
     assert res["out_rel_l2"] <= REL_L2, f"{label}: output rel L2 {res['out_rel_l2']:.3e}"
-    assert res["out_max_abs"] <= max_abs, f"{label}: output max abs {res['out_max_abs']:.3e}"
+    if elementwise_abs:
+        bound = np.maximum(MAX_ABS, 0.5 * bf16_ulp(np.maximum(np.abs(exp), np.abs(got))) + 1e-4 * np.abs(exp))
+        over = np.abs(got - exp) > bound
+        assert not over.any(), f"{label}: {over.sum()} outputs beyond max(1e-2, half a bf16 ulp)"
+    else:
+        assert res["out_max_abs"] <= max_abs, f"{label}: output max abs {res['out_max_abs']:.3e}"
     if fp32_path:
         ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exp), 1e-30))) - 7)
         slack = 1e-5 * max(np.abs(exp).max(initial=0.0), 1e-30)
@@ -127,12 +142,11 @@ def check_fused(dw: DeviceWorkload, out: torch.Tensor, ref, label=""):
     conv-state pool bit-exact: written slots hold the last W-1 inputs, every other byte
     (other slots, the spare tail of written slots) is unchanged.
 
-    The gated RMSNorm makes the outputs O(1) (RMS 1 before weight and gate), where one bf16
-    ulp reaches 1.6e-2 for |o| in [2, 4): the max-abs bound of 1e-2, stated for outputs of
-    magnitude <= 1, is applied relative to max(1, max |o|). The element-wise bound of one
-    bf16 ulp of the exact value holds unchanged."""
-    scale = max(1.0, float(np.abs(ref.out).max(initial=0.0)))
-    res = check(dw, out, ref, fp32_path=True, label=label, max_abs=MAX_ABS * scale)
+    The gated RMSNorm makes the outputs O(1) (RMS 1 before weight and gate); rounding them
+    once to bf16 costs up to half an ulp, which is above the 1e-2 max-abs bar where
+    |o| >= 4. The max-abs bar is therefore applied per element as max(1e-2, half a bf16 ulp
+    + fp32 slack); the bound of one bf16 ulp of the exact value holds unchanged."""
+    res = check(dw, out, ref, fp32_path=True, label=label, elementwise_abs=True)
     w = dw.w
     if w.conv_weight is None or w.conv_width < 2:
         return res

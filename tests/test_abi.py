@@ -240,3 +240,48 @@ def test_oversized_batches_are_refused_before_launch(kda):
     s = kda.lib.kda_chunk_prefill(FAKE, 768, FAKE, 256, FAKE, 2, FAKE, None, limit, 64,
                                   ctypes.byref(hd), ctypes.byref(st), None, 0, FAKE, 256, None, None)
     assert s == 1 and "split the call" not in kda.last_error()
+
+
+def _varlen_inputs(torch, N=10, H=2, K=128, V=128, S=2, slots=4):
+    qkv = torch.zeros(N, 2 * H * K + H * V, dtype=torch.bfloat16)
+    g = torch.zeros(N, H * K, dtype=torch.bfloat16)
+    b = torch.zeros(N, H, dtype=torch.bfloat16)
+    A_log = torch.zeros(H)
+    pool = torch.zeros(slots, H, K, V)
+    idx = torch.arange(S, dtype=torch.int32)
+    cu = torch.tensor([0, 4, N], dtype=torch.int32)
+    return qkv, g, b, A_log, pool, idx, cu
+
+
+def test_binding_refuses_short_varlen_inputs_without_gpu(kda):
+    """The C ABI has no row counts; the binding refuses inputs that would be read past
+    their end: too few state indices, sequence bounds beyond the rows, short per-token
+    tensors and a short caller-passed output."""
+    torch = pytest.importorskip("torch")
+    qkv, g, b, A_log, pool, idx, cu = _varlen_inputs(torch)
+    with pytest.raises(ValueError, match="state_indices"):
+        kda.kda_chunk_prefill(qkv, g, b, A_log, None, None, pool, idx[:1], cu)
+    with pytest.raises(ValueError, match="end at"):
+        kda.kda_chunk_prefill(qkv[:8], g[:8], b[:8], A_log, None, None, pool, idx, cu)
+    with pytest.raises(ValueError, match="start at"):
+        kda.kda_chunk_prefill(qkv, g, b, A_log, None, None, pool, idx,
+                              torch.tensor([-1, 4, 10], dtype=torch.int32))
+    with pytest.raises(ValueError, match="raw_g"):
+        kda.kda_chunk_prefill(qkv, g[:9], b, A_log, None, None, pool, idx, cu)
+    with pytest.raises(ValueError, match="raw_beta"):
+        kda.kda_mixed_batch(qkv, g, b[:9], A_log, None, None, pool, idx, cu, 0)
+    with pytest.raises(ValueError, match="out"):
+        kda.kda_chunk_prefill(qkv, g, b, A_log, None, None, pool, idx, cu,
+                              out=torch.zeros(9, 2 * 128, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="same length"):
+        kda.kda_chunk_prefill(qkv, g, b, A_log, None, None, pool, idx, cu,
+                              cu_seqlens_host=torch.tensor([0, 10], dtype=torch.int32))
+
+
+def test_binding_refuses_short_decode_inputs_without_gpu(kda):
+    torch = pytest.importorskip("torch")
+    qkv, g, b, A_log, pool, idx, _ = _varlen_inputs(torch, N=4, S=4)
+    with pytest.raises(ValueError, match="raw_g"):
+        kda.kda_packed_decode(qkv, g[:3], b, A_log, None, None, pool, idx)
+    with pytest.raises(ValueError, match="raw_beta"):
+        kda.kda_spec_verify(qkv, g, b[:3], A_log, None, None, pool, idx[:2], 2)

@@ -75,10 +75,10 @@ def test_length_one_prefill_equals_decode(kda):
 
 
 def test_chunked_prefill_config(kda):
-    """8 sequences of the seed-1 lengths (33,494 tokens), H=32, K=V=128; the oracle
-    samples heads 0..3 of every sequence."""
+    """8 sequences of the seed-1 lengths (33,494 tokens), H=32, K=V=128: every head of every
+    sequence against the oracle, element by element (outputs and final states)."""
     w = wl.chunked_prefill(None)
-    _run(kda, w, "chunked prefill 8 seqs", heads=(0, 4))
+    _run(kda, w, "chunked prefill 8 seqs", heads=(0, 32))
 
 
 def test_chunked_prefill_config_lower_bound(kda):
@@ -109,10 +109,10 @@ def test_split_prefill_resumes_from_slot(kda):
 
 
 def test_mixed_batch_config(kda):
-    """96 length-1 decodes + 4 prefills of 4096, index stride 4; the oracle samples
-    heads 0..3 and all decodes."""
+    """96 length-1 decodes + 4 prefills of 4096, index stride 4: every head of every
+    sequence against the oracle, element by element."""
     w = wl.mixed_batch()
-    _run(kda, w, "mixed batch", heads=(0, 4))
+    _run(kda, w, "mixed batch", heads=(0, 32))
 
 
 @pytest.mark.parametrize("lower_bound", [-5.0, None])
@@ -224,3 +224,32 @@ def test_mixed_batch_repeat_bit_identical(kda):
         if first is None:
             first = snap
         assert torch.equal(snap[0], first[0]) and torch.equal(snap[1], first[1])
+
+
+@pytest.mark.parametrize("K,V", [(128, 128), (64, 64)])
+def test_prefill_empty_sequence_out_of_range_slot(kda, K, V):
+    """An empty sequence whose slot is out of range sets the range bit on the chunked path
+    (K = V = 128) and on the token-recurrent one (other head sizes) alike, and touches
+    nothing."""
+    w = wl.varlen_case([0, 70, 0, 5], 2, K, V, seed=300 + K, num_slots=8)
+    w.index_buf = np.array([[9], [1], [2], [3]], np.int32)
+    ref = ko.run(w)
+    assert ref.err_flags == ko.ERR_SLOT_OUT_OF_RANGE
+    dw = hx.DeviceWorkload(w)
+    out = hx.run_gpu(dw, kda)
+    hx.check(dw, out, ref, fp32_path=(K != 128), label=f"empty out-of-range K={K}")
+
+
+def test_prefill_fp16_range_flag(kda):
+    """Values of ~1e5 exceed the fp16 range that the chunked path's V - K^G S operand has:
+    the call reports it in the error word (bit 2) instead of returning Inf silently."""
+    w = wl.varlen_case([70, 40], 2, 128, 128, seed=310)
+    HK = w.H * w.K
+    v = w.mixed_qkv[:, 2 * HK:].view(np.uint16)
+    big = wl.f32_to_bf16_bits(np.float32(1e5) * np.random.default_rng(5).standard_normal(v.shape).astype(np.float32))
+    w.mixed_qkv[:, 2 * HK:] = big
+    dw = hx.DeviceWorkload(w)
+    hx.run_gpu(dw, kda)
+    torch.cuda.synchronize()
+    err = int(dw.err.cpu().item())
+    assert err & 4, f"range bit not set (err = {err})"
