@@ -307,6 +307,38 @@ int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
                     const kda_state *state, void *workspace, size_t workspace_bytes,
                     uint16_t *out, int64_t ld_out, uint32_t *err_flags, void *stream);
 
+/*
+ * kda_chunk_prefill_no_alloc — kda_chunk_prefill for callers that cannot allocate device
+ * memory when they call: a host thread of a framework whose device memory belongs to a
+ * caching pool it must not bypass, an engine that fixes its footprint at load time, a
+ * plugin handed only its inputs and outputs. (This entry point is a property of this
+ * library's interface; the method's pages have no counterpart.)
+ * Arguments, results, error bits and precision are kda_chunk_prefill's, without the
+ * workspace: the intra-chunk records live in one fixed device array of
+ * KDA_NO_ALLOC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU that loads the
+ * library's code holds until the process exits. The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ * - Size limit: the call needs kda_chunk_prefill_workspace_bytes(...) bytes of scratch, one
+ *   57,856-byte record per (chunk of 64 rows, head) at K = V = 128 (e.g. 1,159 chunk-heads:
+ *   36 chunks at H = 32). A larger request is rejected, before any CUDA call, with
+ *   KDA_ERR_WORKSPACE and a message naming both sizes; split it or use kda_chunk_prefill.
+ *   Other head sizes need no scratch.
+ * - Set-up: the first call on a device that needs scratch looks up the array's device
+ *   address on the current device (cudaGetSymbolAddress; this may load the library's device
+ *   code) and keeps it. Make that first call on each device before any stream capture.
+ * - Sharing: every call on a device uses the same array, which keeps the last call's
+ *   records. Nothing in it has to start at zero (each call writes every record it reads),
+ *   but calls whose kernels can overlap on the GPU (other streams, other threads) race on
+ *   it: order them on one stream or serialise them.
+ */
+#define KDA_NO_ALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int kda_chunk_prefill_no_alloc(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *raw_g,
+                               int64_t ld_g, const uint16_t *raw_beta, int64_t ld_beta,
+                               const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                               int64_t num_seqs, int32_t chunk_size, const kda_heads *heads,
+                               const kda_state *state, uint16_t *out, int64_t ld_out,
+                               uint32_t *err_flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -453,3 +453,12 @@ int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
 }
 
 }  // extern "C"
+
+int kda::set_error(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}

@@ -35,6 +35,9 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
                                  int chunk_size, void *workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+// Sets the message kda_last_error returns (printf-style) and returns `status`.
+int set_error(int status, const char *fmt, ...);
+
 // The bounded-wait self-test (one CTA waits on an mbarrier nothing arrives at).
 cudaError_t launch_bounded_wait_selftest(uint32_t *err, cudaStream_t stream);
 

@@ -34,7 +34,9 @@ KDA_ERRFLAG_TIMEOUT = 2
 EXPORTED = ("kda_last_error", "kda_status_string", "kda_gate", "kda_packed_decode",
             "kda_spec_verify", "kda_spec_verify_checkpoints", "kda_fused_decode",
             "kda_fused_spec_verify", "kda_selftest_bounded_wait", "kda_chunk_prefill_workspace_bytes",
-            "kda_chunk_prefill", "kda_mixed_batch")
+            "kda_chunk_prefill", "kda_mixed_batch", "kda_chunk_prefill_no_alloc")
+
+KDA_NO_ALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # the fixed scratch of kda_chunk_prefill_no_alloc
 
 
 class KdaHeads(ctypes.Structure):
@@ -100,6 +102,9 @@ def _load():
     lib.kda_mixed_batch.restype = ctypes.c_int
     lib.kda_mixed_batch.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I64, HP, SP, P, SZ, P,
                                     I64, P, P]
+    lib.kda_chunk_prefill_no_alloc.restype = ctypes.c_int
+    lib.kda_chunk_prefill_no_alloc.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I32, HP, SP, P,
+                                               I64, P, P]
     return lib
 
 
@@ -414,6 +419,34 @@ def kda_chunk_prefill(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound, i
                                  int(chunk_size), ctypes.byref(hd), ctypes.byref(st), _ptr(ws),
                                  ws_bytes, _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
            "kda_chunk_prefill")
+    return out, initial_state
+
+
+def kda_chunk_prefill_no_alloc(mixed_qkv, raw_g, raw_beta, A_log, dt_bias, lower_bound,
+                               initial_state, state_indices, cu_seqlens, cu_seqlens_host, out, *,
+                               chunk_size=64, scale=None, l2_eps=1e-6, null_slot=-1,
+                               err_flags=None, stream=None):
+    """kda_chunk_prefill for callers that cannot allocate device memory: the library keeps
+    its records in a fixed 64 MiB device array (calls beyond it raise KdaError). `out` and
+    the host copy of cu_seqlens are required, so this wrapper allocates nothing on the
+    device either. The first call on a device should come before any stream capture; calls
+    that overlap on the GPU race on the shared array. Returns (out, initial_state)."""
+    _, H, K, V = initial_state.shape
+    N = mixed_qkv.shape[0]
+    if out is None or cu_seqlens_host is None:
+        raise ValueError("kda_chunk_prefill_no_alloc needs `out` and `cu_seqlens_host`")
+    cu_h = _host_cu(cu_seqlens, cu_seqlens_host)
+    S = cu_h.numel() - 1
+    hd = make_heads(A_log, dt_bias, lower_bound, K, V, scale, l2_eps)
+    st = make_state(initial_state, state_indices, null_slot)
+    _check_varlen(cu_h, N, S, state_indices, raw_g=raw_g, raw_beta=raw_beta)
+    out, ld_out = _out(out, N, H, V, mixed_qkv.device)
+    _check(lib.kda_chunk_prefill_no_alloc(_ptr(mixed_qkv), _rows(mixed_qkv, "mixed_qkv"), _ptr(raw_g),
+                                          _rows(raw_g, "raw_g"), _ptr(raw_beta), _rows(raw_beta, "raw_beta"),
+                                          _ptr(cu_seqlens), ctypes.c_void_p(cu_h.data_ptr()), S,
+                                          int(chunk_size), ctypes.byref(hd), ctypes.byref(st),
+                                          _ptr(out), ld_out, _ptr(err_flags), _stream(stream)),
+           "kda_chunk_prefill_no_alloc")
     return out, initial_state
 
 
