@@ -709,7 +709,13 @@ def measure_secondary(torch, kda, wl, dev, stream, pk, local=0):
     res["chunk_prefill"] = prefill_leg(torch, kda, wl, w, dev, stream, pk, None, local)
     res["chunk_prefill_lower_bound"] = prefill_leg(torch, kda, wl, wl.chunked_prefill(-5.0), dev, stream, pk,
                                                    -5.0, local)
-    # mixed batch
+    res["mixed_batch"] = mixed_leg(torch, kda, wl, dev, stream, pk, local)
+    return res
+
+
+def mixed_leg(torch, kda, wl, dev, stream, pk, local, calls=20):
+    """96 decodes + 4 x 4096 prefill tokens through kda_mixed_batch: `calls` calls after 3
+    warm-up calls, CUDA events, clocks sampled."""
     w = wl.mixed_batch()
     dw = wl.DeviceWorkload(w, dev)
     out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
@@ -721,14 +727,13 @@ def measure_secondary(torch, kda, wl, dev, stream, pk, local=0):
         kda.kda_mixed_batch(dw.mixed_qkv, dw.raw_g, dw.raw_beta, dw.A_log, dw.dt_bias, None,
                             dw.pool_view(), dw.indices_view(), dw.cu, w.num_decodes,
                             cu_seqlens_host=cu_h, scale=w.scale, out=out, workspace=ws)
-    ms, clocks = time_calls_clocked(torch, mb_call, stream, 20, 3, local)
-    res["mixed_batch"] = {"workload": "96 decodes + 4 x 4096 prefill tokens, H=32, K=V=128, index stride 4",
-                          "tokens_per_s": w.N / (ms * 1e-3), "ms_per_call": ms, "calls": 20,
-                          "algorithmic_bytes": 1095505920,
-                          "hbm_gbs": 1095505920 / (ms * 1e-3) / 1e9,
-                          "frac_hbm": 1095505920 / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "clocks": clocks}
+    ms, clocks = time_calls_clocked(torch, mb_call, stream, calls, 3, local)
     del dw, ws
-    return res
+    return {"workload": "96 decodes + 4 x 4096 prefill tokens, H=32, K=V=128, index stride 4",
+            "tokens_per_s": w.N / (ms * 1e-3), "ms_per_call": ms, "calls": calls,
+            "algorithmic_bytes": 1095505920,
+            "hbm_gbs": 1095505920 / (ms * 1e-3) / 1e9,
+            "frac_hbm": 1095505920 / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "clocks": clocks}
 
 
 if __name__ == "__main__":

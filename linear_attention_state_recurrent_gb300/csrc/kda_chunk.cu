@@ -47,6 +47,8 @@
 #include <numeric>
 #include <vector>
 
+#include <cuda.h>          // CUtensorMap and its enums (the encoder is fetched through the runtime)
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "kda_common.cuh"
@@ -84,20 +86,23 @@ constexpr uint32_t SBO64_TF32 = 64 * 4 * 8;    // K = 64 tf32
 constexpr uint32_t SBO_SB = SBO64_F16 + 16;
 
 // ---- prep shared memory (bytes) ----
-constexpr uint32_t SM_G = 0;            // bf16 [64][128] raw_g, 16-byte chunks XOR-swizzled by row
+constexpr uint32_t SM_G = 0;            // bf16 [2][64][64] raw_g as two TMA boxes (128B swizzle, see tma_off)
 constexpr uint32_t SM_BH = 16384;       // fp32 [64][64]  b (log2 units) of the current channel half, swizzled
 constexpr uint32_t SM_BOFF = 32768;     // tf32 [96][64]  [B_1; B_2; B_3] of the current half (SBO 2048)
 constexpr uint32_t SM_BDIAG = 57344;    // tf32 [64][64]  K^R of the current half (SBO 2048); on the
                                         // pairwise path: fp16 [64][64] k^ then q^ (swizzled)
 constexpr uint32_t SM_SB = 73728;       // fp16 [192][64] Aqk rows 0..63, Kd^T rows 64..191 (SBO 1040)
-constexpr uint32_t SM_QSTG = SM_BH;     // bf16 [64][128] q, staged like raw_g (read before the gate pass)
-constexpr uint32_t SM_KSTG = SM_BH + 16384;   // bf16 [64][128] k
+constexpr uint32_t SM_QSTG = SM_BOFF;   // bf16 [2][64][64] q, staged like raw_g (read before operand generation)
+constexpr uint32_t SM_KSTG = SM_BDIAG;  // bf16 [2][64][64] k
+static_assert(SM_QSTG + 16384 <= SM_BDIAG && SM_KSTG + 16384 <= SM_SB, "q/k staging regions");
+static_assert(SM_G % 1024 == 0 && SM_QSTG % 1024 == 0 && SM_KSTG % 1024 == 0, "128B-swizzled boxes");
 constexpr uint32_t SM_TAB = SM_SB + 24 * SBO_SB;   // fp32 [4 blocks][8][64] per-(block, channel) constants
 constexpr uint32_t SM_TOT = SM_TAB + 8192;         // fp32 [8][64] sums of g over 8-row octets
 constexpr uint32_t SM_NRM = SM_TOT + 2048;         // fp32 [2][128] half-row |k|^2, |q|^2
 constexpr uint32_t SM_BETA = SM_NRM + 1024;        // fp32 [64]
 constexpr uint32_t SM_MBAR = SM_BETA + 256;        // mbarrier of the MMAs (two committing threads)
-constexpr uint32_t SM_TMEMP = SM_MBAR + 8;
+constexpr uint32_t SM_LBAR = SM_MBAR + 8;          // mbarriers of the tensor copies: raw_g, then q and k
+constexpr uint32_t SM_TMEMP = SM_LBAR + 16;
 constexpr uint32_t SM_WAITOK = SM_TMEMP + 4;
 constexpr uint32_t PREP_SMEM = SM_WAITOK + 4;
 static_assert(SM_MBAR % 8 == 0, "mbarrier alignment");
@@ -124,6 +129,8 @@ enum Tab { kP1 = 1, kE = 2, kBD = 3, kD4 = 4, kD2 = 5, kD3 = 6 };   // kP1: the 
 __device__ __forceinline__ uint32_t off_b_base(int R) { return R == 1 ? 0 : (R == 2 ? 16 : 48); }
 
 struct Args {
+    CUtensorMap tm_qkv;        // mixed_qkv [rows][2HK + HV] bf16, boxes of 64 rows x 64 columns, 128B swizzle
+    CUtensorMap tm_g;          // raw_g [rows][HK], the same boxes
     Params p;
     const int32_t *cu;         // device cu_seqlens (entries)
     int64_t entry_base;        // first entry of this launch
@@ -206,6 +213,14 @@ __device__ __forceinline__ uint32_t sb_offset(int row, int k)
     return static_cast<uint32_t>((row >> 3) * SBO_SB + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
 }
 __device__ __forceinline__ uint32_t tab_off(int s, int k, int c) { return static_cast<uint32_t>(((s * 8 + k) * 64 + c) * 4); }
+
+// Byte offset of 16-byte chunk ch (0..15) of row r in a tile staged as two TMA boxes of
+// 64 rows x 128 bytes (channels 0..63, then 64..127) with the 128-byte swizzle: the chunk
+// index within a row's 128 bytes is XORed with r mod 8.
+__device__ __forceinline__ uint32_t tma_off(int r, int ch)
+{
+    return static_cast<uint32_t>((ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
 
 // Copies rows [0, 64) of one 128-wide bf16 column block (base + row*ld) into a staged tile
 // with NTH threads; rows at or past `nrows` are zero-filled (their source is not read).
@@ -475,7 +490,67 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     const bool kside = l < 64;
     const int r = l & 63, s = r >> 4;
     const int side = kside ? 0 : 1;
-    if (tid == 0) tc::mbar_init(mbar, 2);   // two issuing threads commit to every MMA stage
+    const uint32_t lbar = sbase + SM_LBAR;
+    if (tid == 0) {
+        tc::prefetch_tensormap(&a.tm_g);
+        tc::prefetch_tensormap(&a.tm_qkv);
+        tc::mbar_init(mbar, 2);   // two issuing threads commit to every MMA stage
+        tc::mbar_init(lbar, 1);
+        tc::mbar_init(lbar + 8, 1);
+    }
+    // the unit's head, first row and row count (the sequence: the last s with cb[s] <=
+    // chunk; a later unit's search starts from the known sequence of an earlier one,
+    // usually ending at once)
+    auto locate = [&](int bid, int &hh, int64_t &r0, int &nn, int &sq) {
+        const int cgi = bid / H;
+        hh = bid - cgi * H;
+        if (sq < 0) {
+            int lo = 0, hi = a.num_seqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (a.cb[mid] <= cgi) lo = mid; else hi = mid - 1;
+            }
+            sq = lo;
+        } else {
+            while (sq + 1 < a.num_seqs && a.cb[sq + 1] <= cgi) sq++;
+        }
+        r0 = static_cast<int64_t>(a.rs[sq]) + static_cast<int64_t>(cgi - a.cb[sq]) * C;
+        const int64_t rem = static_cast<int64_t>(a.rs[sq + 1]) - r0;
+        nn = static_cast<int>(rem < C ? rem : C);
+    };
+    const int bid = static_cast<int>(blockIdx.x);   // this CTA's unit; the unit pf_stride later starts on
+                                                     // a CTA slot about when this one ends
+    int h, n, sq = -1;
+    int64_t row0;
+    locate(bid, h, row0, n, sq);
+
+    // ---- raw_g, then q and k (into the B-operand regions, free until operand generation)
+    // by tensor copies from thread 0, issued before the tensor-memory allocation; thread 32
+    // prefetches a later unit's boxes into L2. The first gate pass runs while q and k are
+    // still in flight. Rows past the chunk hold the next sequence's rows (or zeros past the
+    // tensor) and are masked where read. ----
+    if (tid == 0) {
+        const int y = static_cast<int>(row0), xg = h * KD;
+        tc::mbar_expect_tx(lbar, 16384);
+        tc::tma_load_2d(sbase + SM_G, &a.tm_g, xg, y, lbar);
+        tc::tma_load_2d(sbase + SM_G + 8192, &a.tm_g, xg + 64, y, lbar);
+        tc::mbar_expect_tx(lbar + 8, 32768);
+        tc::tma_load_2d(sbase + SM_QSTG, &a.tm_qkv, xg, y, lbar + 8);
+        tc::tma_load_2d(sbase + SM_QSTG + 8192, &a.tm_qkv, xg + 64, y, lbar + 8);
+        tc::tma_load_2d(sbase + SM_KSTG, &a.tm_qkv, static_cast<int>(HK) + xg, y, lbar + 8);
+        tc::tma_load_2d(sbase + SM_KSTG + 8192, &a.tm_qkv, static_cast<int>(HK) + xg + 64, y, lbar + 8);
+    } else if (tid == 32 && bid + a.pf_stride < total) {
+        int h2, n2, sq2 = sq;
+        int64_t r2;
+        locate(bid + a.pf_stride, h2, r2, n2, sq2);
+        const int y2 = static_cast<int>(r2), x2 = h2 * KD;
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+            tc::tma_prefetch_2d(&a.tm_g, x2 + 64 * hf, y2);
+            tc::tma_prefetch_2d(&a.tm_qkv, x2 + 64 * hf, y2);
+            tc::tma_prefetch_2d(&a.tm_qkv, static_cast<int>(HK) + x2 + 64 * hf, y2);
+        }
+    }
     if (warp == 0) tc::tmem_alloc<256>(sbase + SM_TMEMP);
     tc::fence_before_sync();
     __syncthreads();
@@ -484,76 +559,16 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     uint32_t phase = 0;
     bool ok = true;
-    // the unit's head, first row and row count (the sequence: the last s with cb[s] <= chunk)
-    auto locate = [&](int bid, int &hh, int64_t &r0, int &nn) {
-        const int cgi = bid / H;
-        hh = bid - cgi * H;
-        int lo = 0, hi = a.num_seqs - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.cb[mid] <= cgi) lo = mid; else hi = mid - 1;
-        }
-        r0 = static_cast<int64_t>(a.rs[lo]) + static_cast<int64_t>(cgi - a.cb[lo]) * C;
-        const int64_t rem = static_cast<int64_t>(a.rs[lo + 1]) - r0;
-        nn = static_cast<int>(rem < C ? rem : C);
-    };
     {
-    const int bid = static_cast<int>(blockIdx.x);   // this CTA's unit; the unit pf_stride later starts on
-                                                     // a CTA slot about when this one ends
-    int h, n;
-    int64_t row0;
-    locate(bid, h, row0, n);
+    // this unit's beta (consumed after the first gate pass, so its latency is hidden)
+    const uint16_t braw = (tid < C && tid < n) ? p.rb[(row0 + tid) * p.ld_beta + h] : static_cast<uint16_t>(0);
     unsigned char *rec = a.rec + static_cast<size_t>(bid) * REC_BYTES;
 
-    // ---- stage raw_g, q and k (q and k in the b / B-operand regions, free until the gate
-    // pass), prefetch the next unit's rows into L2, start the norm pass ----
-    stage_rows<PT>(sbase + SM_G, p.rg + row0 * p.ld_g + static_cast<int64_t>(h) * KD, p.ld_g, n, tid);
-    stage_rows<PT>(sbase + SM_QSTG, p.qkv + row0 * p.ld_qkv + static_cast<int64_t>(h) * KD, p.ld_qkv, n, tid);
-    stage_rows<PT>(sbase + SM_KSTG, p.qkv + row0 * p.ld_qkv + HK + static_cast<int64_t>(h) * KD, p.ld_qkv, n, tid);
-    cp_async_commit();
-    if (tid < 3 * C && bid + a.pf_stride < total) {
-        int h2, n2;
-        int64_t r2;
-        locate(bid + a.pf_stride, h2, r2, n2);
-        const int rr = tid & 63, part = tid >> 6;   // q, k, raw_g rows
-        if (rr < n2) {
-            const uint16_t *src = part < 2 ? p.qkv + (r2 + rr) * p.ld_qkv + part * HK + static_cast<int64_t>(h2) * KD
-                                           : p.rg + (r2 + rr) * p.ld_g + static_cast<int64_t>(h2) * KD;
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" :: "l"(src) : "memory");
-        }
-    }
-    if (tid < C) betas[tid] = tid < n ? sigmoid_f(bf16_to_f32(p.rb[(row0 + tid) * p.ld_beta + h])) : 0.f;
     const float expA = __expf(__ldg(p.A_log + h));
     const float expA_l2e = expA * kLog2e, lb_l2e = p.lb * kLog2e;
-    cp_async_wait_all();
-    __syncthreads();
-    // own row from the staged tile: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31 (rows
-    // past the chunk were zero-filled)
-    uint4 xr[2][4];
-    {
-        const uint32_t stg = sbase + (kside ? SM_KSTG : SM_QSTG);
-        float2 ss = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int hf = 0; hf < 2; hf++)
-#pragma unroll
-            for (int q4 = 0; q4 < 4; q4++) {
-                const uint4 v = ld_shared_u4(stg + st_off(r, 8 * hf + 4 * sub + q4));
-                xr[hf][q4] = v;
-                float f[8];
-                unpack_bf16x8(v, f);
-#pragma unroll
-                for (int o = 0; o < 8; o += 2) ss = ffma2(make_float2(f[o], f[o + 1]), make_float2(f[o], f[o + 1]), ss);
-            }
-        nrm[sub * 128 + l] = ss.x + ss.y;
-    }
-    __syncthreads();   // the half-row norms; the staged q and k are consumed
-    // rows past the chunk hold zeros; their norm factor is 0 so that eps = 0 gives no NaN
-    auto norm_of = [&](int lane_idx, int row) -> float {
-        const float f = (lane_idx < 64 ? 1.f : p.scale) * rsqrtf(nrm[lane_idx] + nrm[128 + lane_idx] + p.eps);
-        return row < n ? f : 0.f;
-    };
-    const float rn = norm_of(l, r);
-    const float rk = kside ? rn : norm_of(r, r);   // the key row's norm factor (the Q thread's key share)
+    uint4 xr[2][4];   // own row of q or k: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31
+    float rn = 0.f, rk = 0.f;   // norm factors of the own row and of the key row r
+    ok &= cta_wait(lbar, 0, smem + SM_WAITOK);   // raw_g has landed
 
     // ---- gate pass over one channel half: per (row, channel) e1 = e^{b - P_s} (the decay
     // since the block's reference) into SM_BH, or on the pairwise path the in-block log2
@@ -566,13 +581,13 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         const int cg = 64 * hf + 2 * cp;                 // first channel of the pair (in the head)
         const float2 dtb = p.dt_bias ? make_float2(__ldg(p.dt_bias + h * KD + cg), __ldg(p.dt_bias + h * KD + cg + 1))
                                      : make_float2(0.f, 0.f);
-        const unsigned char *gt = smem + SM_G + 8 * o8 * 256 + (cg & 7) * 2;
         const int ch = cg >> 3;
+        const unsigned char *gt = smem + SM_G + (ch >> 3) * 8192 + 8 * o8 * 128 + (cg & 7) * 2;
         const int nv = n - 8 * o8;               // rows of this octet inside the chunk
         float2 v[8];
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-            const uint32_t w = *reinterpret_cast<const uint32_t *>(gt + j * 256 + ((ch ^ j) << 4));
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(gt + j * 128 + (((ch & 7) ^ j) << 4));
             v[j] = fadd2(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)), dtb);
         }
         if (p.has_lb) {
@@ -643,6 +658,34 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         __syncthreads();
         return flagged;
     };
+    const bool pw0 = gate_half(0);
+    if (tid < C) betas[tid] = tid < n ? sigmoid_f(bf16_to_f32(braw)) : 0.f;   // read in the assembly
+    ok &= cta_wait(lbar + 8, 0, smem + SM_WAITOK);   // q and k have landed
+    {   // own row from the staged tile (zero past the chunk) and its half-row sums of squares
+        const uint32_t stg = sbase + (kside ? SM_KSTG : SM_QSTG);
+        float2 ss = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++)
+#pragma unroll
+            for (int q4 = 0; q4 < 4; q4++) {
+                const uint4 v = r < n ? ld_shared_u4(stg + tma_off(r, 8 * hf + 4 * sub + q4)) : make_uint4(0u, 0u, 0u, 0u);
+                xr[hf][q4] = v;
+                float f[8];
+                unpack_bf16x8(v, f);
+#pragma unroll
+                for (int o = 0; o < 8; o += 2) ss = ffma2(make_float2(f[o], f[o + 1]), make_float2(f[o], f[o + 1]), ss);
+            }
+        nrm[sub * 128 + l] = ss.x + ss.y;
+    }
+    __syncthreads();   // the half-row norms; the staged q and k are consumed
+    {   // rows past the chunk hold zeros; their norm factor is 0 so that eps = 0 gives no NaN
+        auto norm_of = [&](int lane_idx, int row) -> float {
+            const float f = (lane_idx < 64 ? 1.f : p.scale) * rsqrtf(nrm[lane_idx] + nrm[128 + lane_idx] + p.eps);
+            return row < n ? f : 0.f;
+        };
+        rn = norm_of(l, r);
+        rk = kside ? rn : norm_of(r, r);
+    }
 
     // ---- operand generation over one channel half; pw: this half's diagonal blocks take
     // the pairwise path (SM_BH then holds the in-block log2 prefix, k^ and q^ go to the
@@ -808,8 +851,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         }
     };
 
-    // ================= channel half 0 =================
-    const bool pw0 = gate_half(0);
+    // ================= channel half 0 (its gate pass ran while q and k loaded) =================
     gen_half(0, pw0);
     tc::tmem_st_wait();
     tc::fence_proxy_async();
@@ -949,8 +991,11 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     tc::fence_before_sync();
     __syncthreads();
     }
-    if (!ok && tid == 0)   // a wait gave up: give the product it waited for (bounded) time to end
+    if (!ok && tid == 0) {   // a wait gave up: give the copies and the product it waited for (bounded) time to end
+        (void)tc::mbar_wait(lbar, 0);
+        (void)tc::mbar_wait(lbar + 8, 0);
         (void)tc::mbar_wait(mbar, phase ^ 1u);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc<256>(tmem);
@@ -1294,6 +1339,37 @@ size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, in
     return static_cast<size_t>(total_chunks(cu_host, num_seqs)) * H * chunk::REC_BYTES;
 }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link against the driver library)
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// A tensor map over a bf16 matrix of `rows` rows x `cols` columns with a row pitch of `ld`
+// elements, read in boxes of 64 rows x 64 columns (128 bytes) with the 128-byte swizzle.
+// Rows past the matrix read as zeros.
+static cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t cols, int64_t rows, int64_t ld)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorSymbolNotFound;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // The prefill chains of entries [entry_base, entry_base + num_seqs): per launch of at most
 // kMaxSeqs sequences, the prep pass over every (chunk, head), then the chains (longest
 // sequence first).
@@ -1314,9 +1390,18 @@ static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const i
     unsigned char *recs = static_cast<unsigned char *>(workspace);
     int64_t ch_done = 0;   // chunks (not chunk-heads) of the sequences already launched
     std::vector<int32_t> ord;
+    // tensor maps over the rows of this call (every row any of its chunks reads lies below
+    // the last sequence's end)
+    const int64_t rows = std::max<int64_t>(cu_host[entry_base + num_seqs], 1);
+    CUtensorMap tm_qkv, tm_g;
+    if ((err = encode_rows_map(&tm_qkv, p.qkv, 2 * static_cast<int64_t>(p.H) * KD + static_cast<int64_t>(p.H) * VD,
+                               rows, p.ld_qkv)) != cudaSuccess) return err;
+    if ((err = encode_rows_map(&tm_g, p.rg, static_cast<int64_t>(p.H) * KD, rows, p.ld_g)) != cudaSuccess) return err;
     for (int64_t s0 = 0; s0 < num_seqs; s0 += kMaxSeqs) {
         const int64_t ns = std::min<int64_t>(kMaxSeqs, num_seqs - s0);
         Args a;
+        a.tm_qkv = tm_qkv;
+        a.tm_g = tm_g;
         a.p = p;
         a.cu = cu;
         a.entry_base = entry_base + s0;

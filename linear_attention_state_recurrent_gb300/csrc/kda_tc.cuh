@@ -196,6 +196,29 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
+// 2-D tensor copy (TMA) of one box, described by a tensor map in kernel parameter space,
+// from global to this CTA's shared memory; completion is counted on `mbar` in bytes. x is
+// the inner (element) coordinate, y the outer (row) coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(mbar) : "memory");
+}
+
+// Brings a tensor map (kernel parameter space) into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
+}
+
+// Prefetch of one tensor-map box into L2.
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(tmap), "r"(x), "r"(y) : "memory");
+}
+
 // TMEM allocation by one full warp; the base address is written to *dst (smem).
 template <uint32_t NCOLS>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_saddr)
