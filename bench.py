@@ -651,7 +651,7 @@ def prefill_leg(torch, kda, wl, w, dev, stream, pk, lower_bound, local, calls=20
     ms, clocks = time_calls_clocked(torch, pf, stream, calls, 3, local)
     flops = prefill_alg_flops(wl.PREFILL_LENGTHS_SEED1, w.H, w.K, w.V)
     mb = prefill_min_bytes(w)
-    sha = source_sha("kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh")
+    sha = source_sha("kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_f32x2.cuh")
     traffic = ncu_traffic("prefill (prep_kernel + chain_kernel) chunked_prefill", sha)
     achieved = mb / (ms * 1e-3) / 1e9
     res = {"metric": "chunk-prefill tokens/s", "value": w.N / (ms * 1e-3), "unit": "tokens/s",

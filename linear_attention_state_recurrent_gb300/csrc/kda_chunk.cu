@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include "kda_common.cuh"
+#include "kda_f32x2.cuh"
 #include "kda_launch.h"
 #include "kda_tc.cuh"
 
@@ -251,41 +252,6 @@ __device__ __forceinline__ bool cta_wait(uint32_t mbar, uint32_t parity, unsigne
     return ok;
 }
 
-// ---------------------------------------------------------------------------
-// packed fp32x2 arithmetic: one instruction for two values
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " sub.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
-{
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
 // d = a * b, d = a - b and d = a * s over 8 values
 __device__ __forceinline__ void mul8(float *d, const float *a, const float *b)
 {

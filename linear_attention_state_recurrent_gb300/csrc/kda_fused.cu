@@ -10,6 +10,7 @@
 // the sequential part is the state update with one barrier per token; the gated norm and
 // the bf16 stores run once at the end over all T x V outputs.
 #include "kda_common.cuh"
+#include "kda_f32x2.cuh"
 #include "kda_launch.h"
 
 namespace kda {
@@ -55,8 +56,9 @@ template <int K, int V, int MAXT>
 struct HeadSmem {
     static constexpr int CG = V / 4, NRG = 128 / CG;
     float a[MAXT][K];                 // alpha = e^g
-    float k[MAXT][K];                 // conv'd k, raw
-    float q[MAXT][K];                 // conv'd q, raw
+    float k[MAXT][K];                 // conv'd k, raw; then k^ (normalised)
+    float q[MAXT][K];                 // conv'd q, raw; then alpha q^
+    float ka[MAXT][K];                // alpha k^
     float v[MAXT][V];                 // conv'd v
     float gw[MAXT][V];                // norm weight * sigmoid(gate)
     float o[MAXT][V];                 // o before the norm
@@ -270,6 +272,21 @@ head_kernel(Params p, TailParams tp, int T)
             sm.tok[t][3] = sigmoid_f(bf16_to_f32(p.rb[(row0 + t) * p.ld_beta + h]));
         }
     }
+    __syncthreads();
+    // ---- per-token row scalars of the state passes: k^ = k rk, alpha k^ and alpha q^ (the
+    //      decayed key and query against the state before the token's decay) ----
+    for (int idx = tid; idx < T * (K / 4); idx += 128) {
+        const int t = idx / (K / 4), c = 4 * (idx - t * (K / 4));
+        const float rq = sm.tok[t][0], rk = sm.tok[t][1];
+        const float4 al = *reinterpret_cast<const float4 *>(&sm.a[t][c]);
+        const float4 kr = *reinterpret_cast<const float4 *>(&sm.k[t][c]);
+        const float4 qr = *reinterpret_cast<const float4 *>(&sm.q[t][c]);
+        const float4 kh = make_float4(kr.x * rk, kr.y * rk, kr.z * rk, kr.w * rk);
+        *reinterpret_cast<float4 *>(&sm.k[t][c]) = kh;
+        *reinterpret_cast<float4 *>(&sm.ka[t][c]) = make_float4(kh.x * al.x, kh.y * al.y, kh.z * al.z, kh.w * al.w);
+        *reinterpret_cast<float4 *>(&sm.q[t][c]) =
+            make_float4(qr.x * rq * al.x, qr.y * rq * al.y, qr.z * rq * al.z, qr.w * rq * al.w);
+    }
     float4 S[RPT];
     if (has_state) {
         cp_async_wait_all();
@@ -283,25 +300,36 @@ head_kernel(Params p, TailParams tp, int T)
     // ---- the recurrence, token by token (one barrier per token) ----
     for (int t = 0; t < T; t++) {
         const int bb = MAXT == 1 ? 0 : (t & 1);
-        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = make_float4(0.f, 0.f, 0.f, 0.f);
+        // partial (alpha k^)^T S and (alpha q^)^T S over this thread's rows, packed pairs of
+        // columns, two accumulator sets (even and odd rows) to halve the dependency chains
+        float2 ak[2][2], aq[2][2];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; e2++)
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) { ak[e2][hh] = make_float2(0.f, 0.f); aq[e2][hh] = make_float2(0.f, 0.f); }
 #pragma unroll
         for (int i4 = 0; i4 < RPT; i4 += RB) {
-            float alv[4], krv[4], qrv[4];
-            load_rows<RB>(&sm.a[t][r0 + i4], alv);
-            load_rows<RB>(&sm.k[t][r0 + i4], krv);
-            load_rows<RB>(&sm.q[t][r0 + i4], qrv);
+            float kav[4], qav[4];
+            load_rows<RB>(&sm.ka[t][r0 + i4], kav);
+            load_rows<RB>(&sm.q[t][r0 + i4], qav);
 #pragma unroll
             for (int m = 0; m < RB; m++) {
-                float4 &Sv = S[i4 + m];
-                Sv.x *= alv[m]; Sv.y *= alv[m]; Sv.z *= alv[m]; Sv.w *= alv[m];
-                pk.x += krv[m] * Sv.x; pk.y += krv[m] * Sv.y; pk.z += krv[m] * Sv.z; pk.w += krv[m] * Sv.w;
-                pq.x += qrv[m] * Sv.x; pq.y += qrv[m] * Sv.y; pq.z += qrv[m] * Sv.z; pq.w += qrv[m] * Sv.w;
+                const float4 Sv = S[i4 + m];
+                const float2 kk = make_float2(kav[m], kav[m]), qq = make_float2(qav[m], qav[m]);
+                const int e2 = m & 1;
+                ak[e2][0] = ffma2(kk, make_float2(Sv.x, Sv.y), ak[e2][0]);
+                ak[e2][1] = ffma2(kk, make_float2(Sv.z, Sv.w), ak[e2][1]);
+                aq[e2][0] = ffma2(qq, make_float2(Sv.x, Sv.y), aq[e2][0]);
+                aq[e2][1] = ffma2(qq, make_float2(Sv.z, Sv.w), aq[e2][1]);
             }
         }
+        const float2 pk01 = fadd2(ak[0][0], ak[1][0]), pk23 = fadd2(ak[0][1], ak[1][1]);
+        const float2 pq01 = fadd2(aq[0][0], aq[1][0]), pq23 = fadd2(aq[0][1], aq[1][1]);
+        const float4 pk = make_float4(pk01.x, pk01.y, pk23.x, pk23.y), pq = make_float4(pq01.x, pq01.y, pq23.x, pq23.y);
         *reinterpret_cast<float4 *>(&sm.red[bb][rgp][0][j0]) = pk;
         *reinterpret_cast<float4 *>(&sm.red[bb][rgp][1][j0]) = pq;
         __syncthreads();
-        const float rq = sm.tok[t][0], rk = sm.tok[t][1], qkh = sm.tok[t][2], beta = sm.tok[t][3];
+        const float qkh = sm.tok[t][2], beta = sm.tok[t][3];
         float4 ks = make_float4(0.f, 0.f, 0.f, 0.f), qs = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int gI = 0; gI < NRG; gI++) {
@@ -311,23 +339,27 @@ head_kernel(Params p, TailParams tp, int T)
             qs.x += b.x; qs.y += b.y; qs.z += b.z; qs.w += b.w;
         }
         const float4 v4 = *reinterpret_cast<const float4 *>(&sm.v[t][j0]);
-        const float u0 = beta * (v4.x - ks.x * rk), u1 = beta * (v4.y - ks.y * rk);
-        const float u2 = beta * (v4.z - ks.z * rk), u3 = beta * (v4.w - ks.w * rk);
+        const float u0 = beta * (v4.x - ks.x), u1 = beta * (v4.y - ks.y);
+        const float u2 = beta * (v4.z - ks.z), u3 = beta * (v4.w - ks.w);
+        // S <- Diag(alpha) S + k^ u^T, packed pairs of columns
+        const float2 u01 = make_float2(u0, u1), u23 = make_float2(u2, u3);
 #pragma unroll
         for (int i4 = 0; i4 < RPT; i4 += RB) {
-            float khv[4];
+            float alv[4], khv[4];
+            load_rows<RB>(&sm.a[t][r0 + i4], alv);
             load_rows<RB>(&sm.k[t][r0 + i4], khv);
-#pragma unroll
-            for (int m = 0; m < RB; m++) khv[m] *= rk;
 #pragma unroll
             for (int m = 0; m < RB; m++) {
                 float4 &Sv = S[i4 + m];
-                Sv.x += khv[m] * u0; Sv.y += khv[m] * u1; Sv.z += khv[m] * u2; Sv.w += khv[m] * u3;
+                const float2 aa = make_float2(alv[m], alv[m]), kk = make_float2(khv[m], khv[m]);
+                const float2 lo = ffma2(aa, make_float2(Sv.x, Sv.y), fmul2(kk, u01));
+                const float2 hi = ffma2(aa, make_float2(Sv.z, Sv.w), fmul2(kk, u23));
+                Sv = make_float4(lo.x, lo.y, hi.x, hi.y);
             }
         }
         if (rgp == 0) {   // the first CG threads (lanes of warp 0) own the outputs
-            const float o0 = qs.x * rq + qkh * u0, o1 = qs.y * rq + qkh * u1;
-            const float o2 = qs.z * rq + qkh * u2, o3 = qs.w * rq + qkh * u3;
+            const float o0 = qs.x + qkh * u0, o1 = qs.y + qkh * u1;
+            const float o2 = qs.z + qkh * u2, o3 = qs.w + qkh * u3;
             *reinterpret_cast<float4 *>(&sm.o[t][j0]) = make_float4(o0, o1, o2, o3);
             if (norm) {
                 float ss = o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3;
