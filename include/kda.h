@@ -81,7 +81,7 @@ extern "C" {
 #define KDA_ERRFLAG_RANGE 4u      /* bit 2: a value the chunked prefill carries in fp16 (a state entry,
                                      V - K^G S or an intra-chunk operand) reached |x| >= 65504; the
                                      affected outputs and states are invalid (kda_chunk_prefill and
-                                     kda_mixed_batch at K = V = 128) */
+                                     kda_mixed_batch with K and V in {64, 128}) */
 
 /* Per-layer head parameters shared by every call. */
 typedef struct kda_heads {
@@ -264,15 +264,18 @@ size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t
  * chunk_size must be 64. mixed_qkv, raw_g and out must be 16-byte aligned with ld_qkv,
  * ld_g and ld_out multiples of 8 (the tensor-core path moves them in 16-byte vectors).
  * `workspace` (device, 256-byte aligned, owned by the caller) must hold
- * kda_chunk_prefill_workspace_bytes(...) bytes: at K = V = 128 one 57,856-byte record per
+ * kda_chunk_prefill_workspace_bytes(...) bytes: with K and V each 64 or 128 (the tensor-core
+ * path, which works on 128 x 128 tiles with the channels or columns past 64 held at zero)
+ * one 57,856-byte record per
  * (chunk of 64 rows, head), written by the call's first kernel (the intra-chunk pass over
  * every chunk in parallel) and read by its second (the per-sequence state chain); its
- * contents are scratch between calls. It may be NULL when the size is 0 (other head sizes).
- * Calls that share a workspace must not overlap on the device. At K = V = 128 the call is
+ * contents are scratch between calls. It may be NULL when the size is 0 (K or V of 32: the
+ * token-recurrent kernel).
+ * Calls that share a workspace must not overlap on the device. On the tensor-core path the call is
  * two launches per 1024 sequences.
  * Zero-length sequences are allowed: their slot is left untouched (a slot >= num_slots is
  * still flagged).
- * Precision and range (K = V = 128): the tensor-core products take fp16 / tf32 operands with
+ * Precision and range (tensor-core path): the products take fp16 / tf32 operands with
  * fp32 accumulation; the state and V - K^G S enter them in fp16, so state entries and values
  * must stay below 65504 in magnitude. Beyond that the call sets KDA_ERRFLAG_RANGE in
  * *err_flags and its results are invalid (the fp32 pool itself holds any value).
@@ -319,7 +322,7 @@ int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
  * library's code holds until the process exits. The call allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine).
  * - Size limit: the call needs kda_chunk_prefill_workspace_bytes(...) bytes of scratch, one
- *   57,856-byte record per (chunk of 64 rows, head) at K = V = 128 (e.g. 1,159 chunk-heads:
+ *   57,856-byte record per (chunk of 64 rows, head) with K and V in {64, 128} (e.g. 1,159 chunk-heads:
  *   36 chunks at H = 32). A larger request is rejected, before any CUDA call, with
  *   KDA_ERR_WORKSPACE and a message naming both sizes; split it or use kda_chunk_prefill.
  *   Other head sizes need no scratch.

@@ -61,7 +61,6 @@ namespace chunk {
 
 constexpr int C = 64;
 constexpr int KD = 128;
-constexpr int VD = 128;
 constexpr int PT = 256;          // prep threads
 constexpr int CT = 256;          // chain threads
 constexpr int kMaxSeqs = 1024;   // sequences per launch (the host splits larger calls)
@@ -224,14 +223,16 @@ __device__ __forceinline__ uint32_t tma_off(int r, int ch)
 }
 
 // Copies rows [0, 64) of one 128-wide bf16 column block (base + row*ld) into a staged tile
-// with NTH threads; rows at or past `nrows` are zero-filled (their source is not read).
+// with NTH threads; rows at or past `nrows` and 16-byte chunks at or past `nch16` (of 16)
+// are zero-filled (their source is not read).
 template <int NTH>
-__device__ __forceinline__ void stage_rows(uint32_t tile, const uint16_t *base, int64_t ld, int nrows, int tid)
+__device__ __forceinline__ void stage_rows(uint32_t tile, const uint16_t *base, int64_t ld, int nrows, int tid,
+                                           int nch16 = 16)
 {
 #pragma unroll
     for (int x = 0; x < 1024 / NTH; x++) {
         const int id = tid + NTH * x, r = id >> 4, ch = id & 15;
-        const bool ok = r < nrows;
+        const bool ok = r < nrows && ch < nch16;
         const uint16_t *src = base + (ok ? static_cast<int64_t>(r) * ld : 0) + 8 * ch;
         cp_async16(tile + st_off(r, ch), src, ok);
     }
@@ -438,13 +439,15 @@ __device__ __forceinline__ float gate_log2(float x, float expA, float expA_l2e, 
 // channels, the Q thread the last 16. The gate pass uses channel c = tid & 63 of the
 // half and row block tid >> 6.
 // ---------------------------------------------------------------------------
+template <int NH>   // channel halves that hold data: K = 64 NH
 __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Args a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
     const Params &p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
-    const int64_t HK = static_cast<int64_t>(H) * KD;
+    constexpr int kr = 64 * NH, nhalf = NH;
+    const int64_t HK = static_cast<int64_t>(H) * kr;
     const int total = a.cb[a.num_seqs] * H;   // (chunk, head) units of this launch
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t mbar = sbase + SM_MBAR;
@@ -496,22 +499,20 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     // still in flight. Rows past the chunk hold the next sequence's rows (or zeros past the
     // tensor) and are masked where read. ----
     if (tid == 0) {
-        const int y = static_cast<int>(row0), xg = h * KD;
-        tc::mbar_expect_tx(lbar, 16384);
-        tc::tma_load_2d(sbase + SM_G, &a.tm_g, xg, y, lbar);
-        tc::tma_load_2d(sbase + SM_G + 8192, &a.tm_g, xg + 64, y, lbar);
-        tc::mbar_expect_tx(lbar + 8, 32768);
-        tc::tma_load_2d(sbase + SM_QSTG, &a.tm_qkv, xg, y, lbar + 8);
-        tc::tma_load_2d(sbase + SM_QSTG + 8192, &a.tm_qkv, xg + 64, y, lbar + 8);
-        tc::tma_load_2d(sbase + SM_KSTG, &a.tm_qkv, static_cast<int>(HK) + xg, y, lbar + 8);
-        tc::tma_load_2d(sbase + SM_KSTG + 8192, &a.tm_qkv, static_cast<int>(HK) + xg + 64, y, lbar + 8);
+        const int y = static_cast<int>(row0), xg = h * kr;
+        tc::mbar_expect_tx(lbar, 8192u * nhalf);
+        for (int hf = 0; hf < nhalf; hf++) tc::tma_load_2d(sbase + SM_G + 8192 * hf, &a.tm_g, xg + 64 * hf, y, lbar);
+        tc::mbar_expect_tx(lbar + 8, 16384u * nhalf);
+        for (int hf = 0; hf < nhalf; hf++) {
+            tc::tma_load_2d(sbase + SM_QSTG + 8192 * hf, &a.tm_qkv, xg + 64 * hf, y, lbar + 8);
+            tc::tma_load_2d(sbase + SM_KSTG + 8192 * hf, &a.tm_qkv, static_cast<int>(HK) + xg + 64 * hf, y, lbar + 8);
+        }
     } else if (tid == 32 && bid + a.pf_stride < total) {
         int h2, n2, sq2 = sq;
         int64_t r2;
         locate(bid + a.pf_stride, h2, r2, n2, sq2);
-        const int y2 = static_cast<int>(r2), x2 = h2 * KD;
-#pragma unroll
-        for (int hf = 0; hf < 2; hf++) {
+        const int y2 = static_cast<int>(r2), x2 = h2 * kr;
+        for (int hf = 0; hf < nhalf; hf++) {
             tc::tma_prefetch_2d(&a.tm_g, x2 + 64 * hf, y2);
             tc::tma_prefetch_2d(&a.tm_qkv, x2 + 64 * hf, y2);
             tc::tma_prefetch_2d(&a.tm_qkv, static_cast<int>(HK) + x2 + 64 * hf, y2);
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     auto gate_half = [&](int hf) -> bool {
         const int cp = tid & 31, o8 = tid >> 5, sg = o8 >> 1;
         const int cg = 64 * hf + 2 * cp;                 // first channel of the pair (in the head)
-        const float2 dtb = p.dt_bias ? make_float2(__ldg(p.dt_bias + h * KD + cg), __ldg(p.dt_bias + h * KD + cg + 1))
+        const float2 dtb = p.dt_bias ? make_float2(__ldg(p.dt_bias + h * kr + cg), __ldg(p.dt_bias + h * kr + cg + 1))
                                      : make_float2(0.f, 0.f);
         const int ch = cg >> 3;
         const unsigned char *gt = smem + SM_G + (ch >> 3) * 8192 + 8 * o8 * 128 + (cg & 7) * 2;
@@ -634,7 +635,8 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         for (int hf = 0; hf < 2; hf++)
 #pragma unroll
             for (int q4 = 0; q4 < 4; q4++) {
-                const uint4 v = r < n ? ld_shared_u4(stg + tma_off(r, 8 * hf + 4 * sub + q4)) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 v = (r < n && hf < nhalf) ? ld_shared_u4(stg + tma_off(r, 8 * hf + 4 * sub + q4))
+                                                      : make_uint4(0u, 0u, 0u, 0u);
                 xr[hf][q4] = v;
                 float f[8];
                 unpack_bf16x8(v, f);
@@ -673,7 +675,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         // the Q thread's key share: key row r, channels 32 sub + 16 .. + 31 of the half
         uint4 kq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
         if (!kside && r < n) {
-            const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + HK + static_cast<int64_t>(h) * KD + 64 * hf + 32 * sub + 16;
+            const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + HK + static_cast<int64_t>(h) * kr + 64 * hf + 32 * sub + 16;
             kq[0] = __ldg(reinterpret_cast<const uint4 *>(src));
             kq[1] = __ldg(reinterpret_cast<const uint4 *>(src + 8));
         }
@@ -826,20 +828,31 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     issue_gram(pw0, false, false);
     if (pw0) pairwise_half();
     // ================= channel half 1 =================
-    const bool pw1 = gate_half(1);
-    // the half-0 products read the A operand and SM_BOFF / SM_BDIAG, which half 1 rewrites
+    bool pw1 = false;
+    if (nhalf == 2) {
+        pw1 = gate_half(1);
+        // the half-0 products read the A operand and SM_BOFF / SM_BDIAG, which half 1 rewrites
+        ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
+        phase ^= 1;
+        gen_half(1, pw1);
+        tc::tmem_st_wait();
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        issue_gram(pw1, !pw0, true);
+        if (pw1) pairwise_half();
+    } else {
+        // K = 64: channels 64 .. 127 hold no data. Their Kd^T rows are zero and their gamma is
+        // 1, so the chain's state columns past K stay zero; their [K^G; Q^G] columns are not
+        // written (the chain's products stop at K = 64).
+        for (int i = tid; i < 8 * SBO_SB / 16; i += PT)
+            st_shared_u4(sbase + SM_SB + 16 * SBO_SB + 16 * i, make_uint4(0u, 0u, 0u, 0u));
+        if (tid < 64) reinterpret_cast<float *>(rec + REC_GAM)[64 + tid] = 1.f;
+    }
     ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
     phase ^= 1;
-    gen_half(1, pw1);
-    tc::tmem_st_wait();
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    issue_gram(pw1, !pw0, true);
-    if (pw1) pairwise_half();
-    ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
-    phase ^= 1;
-    const bool mma_diag = !(pw0 && pw1), pw_diag = pw0 || pw1;
+    // X_diag holds a product unless every half present took the pairwise path
+    const bool mma_diag = nhalf == 2 ? !(pw0 && pw1) : !pw0, pw_diag = pw0 || pw1;
     if (pw_diag) {   // the pairwise sums -> SM_XD [side][row][column in the block]
         float *xd = reinterpret_cast<float *>(smem + SM_XD);
 #pragma unroll
@@ -990,6 +1003,7 @@ constexpr uint32_t TC_AY = 320;    // Y^T as fp16 pairs (A of the O/S product)  
 constexpr uint32_t TC_PK2 = 384;   // the second K half of (K^G S)^T   64 columns
 constexpr uint32_t TC_PQ2 = 448;   // the second K half of (Q^G S)^T   64 columns
 
+template <int NH, int NV>   // key channel and value column halves that hold data: K = 64 NH, V = 64 NV
 __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Args a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -1002,22 +1016,23 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
     const int64_t row0 = a.rs[sq], row1 = a.rs[sq + 1];
     const int64_t slot = load_slot(p, e);
     const int j = 32 * (warp & 3) + lane, sub = warp >> 2;
+    constexpr int kr = 64 * NH, vr = 64 * NV;   // state rows (channels) and columns that hold data
     if (slot >= p.num_slots) {      // flagged before the length check: empty sequences too
         if (tid == 0 && p.err) atomicOr(p.err, kErrSlotRange);
         for (int64_t t = row0 + (tid >> 6); t < row1; t += CT / 64) {
-            uint32_t *o = reinterpret_cast<uint32_t *>(p.out + t * p.ld_out + static_cast<int64_t>(h) * VD);
-            o[tid & 63] = 0u;
+            uint32_t *o = reinterpret_cast<uint32_t *>(p.out + t * p.ld_out + static_cast<int64_t>(h) * vr);
+            if ((tid & 63) < vr / 2) o[tid & 63] = 0u;
         }
         return;
     }
     if (row1 <= row0) return;
     const bool has_state = slot >= 0;
     const bool writable = has_state && slot != p.null_slot;
-    float *tile = has_state ? p.pool + slot * p.slot_stride + static_cast<int64_t>(h) * KD * VD : nullptr;
+    float *tile = has_state ? p.pool + slot * p.slot_stride + static_cast<int64_t>(h) * kr * vr : nullptr;
     const int nch = static_cast<int>((row1 - row0 + C - 1) / C);
     const unsigned char *rec0 = a.rec + (static_cast<size_t>(a.cb[sq]) * H + h) * REC_BYTES;
     const size_t rec_step = static_cast<size_t>(H) * REC_BYTES;
-    const int64_t HK = static_cast<int64_t>(H) * KD;
+    const int64_t HK = static_cast<int64_t>(H) * kr;
 
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t bar = sbase + CH_BAR;   // kq[0], kq[1], mm[0], mm[1], mma
@@ -1046,8 +1061,8 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
     auto stage_v = [&](int c) {
         const int64_t r0 = row0 + static_cast<int64_t>(c) * C;
         const int nn = static_cast<int>((row1 - r0) < C ? (row1 - r0) : C);
-        stage_rows<CT>(sbase + CH_VT + (c & 1) * 16384, p.qkv + r0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * VD,
-                       p.ld_qkv, nn, tid);
+        stage_rows<CT>(sbase + CH_VT + (c & 1) * 16384, p.qkv + r0 * p.ld_qkv + 2 * HK + static_cast<int64_t>(h) * vr,
+                       p.ld_qkv, nn, tid, vr / 8);
     };
     // chunk whose copy into buffer b is in flight and not yet waited for (-1: none)
     int kq_pending[2] = {-1, -1}, mm_pending[2] = {-1, -1};
@@ -1065,9 +1080,17 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
     for (int cc = 0; cc < 64; cc += 16) {
         float v[16];
         const int c = 64 * sub + cc;
+        const bool in = has_state && c < kr && j < vr;   // the group of 16 channels is in or out whole
 #pragma unroll
-        for (int u = 0; u < 16; u++) v[u] = has_state ? tile[static_cast<int64_t>(c + u) * VD + j] : 0.f;
+        for (int u = 0; u < 16; u++) v[u] = in ? tile[static_cast<int64_t>(c + u) * vr + j] : 0.f;
         tc::tmem_st16(tlane + TC_S + c, v);
+    }
+    if (kr < KD) {   // the second K half of P is not computed: its accumulators stay zero
+        float z[16];
+#pragma unroll
+        for (int u = 0; u < 16; u++) z[u] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 16) tc::tmem_st16(tlane + (sub ? TC_PQ2 : TC_PK2) + cc, z);
     }
     tc::tmem_st_wait();
 
@@ -1081,7 +1104,8 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
         if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, kErrRange);
     };
     auto store_o = [&](const float (&ov)[2][16], int64_t cs, int nrows) {
-        uint16_t *orow = p.out + cs * p.ld_out + static_cast<int64_t>(h) * VD + j;
+        uint16_t *orow = p.out + cs * p.ld_out + static_cast<int64_t>(h) * vr + j;
+        if (j >= vr) nrows = 0;   // columns past V hold no data
         bool bad = false;
 #pragma unroll
         for (int q = 0; q < 2; q++)
@@ -1127,8 +1151,8 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
         if (tid == 0 || tid == 32) {   // P = [(K^G S)^T | (Q^G S)^T], one half per issuing thread, each
             tc::fence_after_sync();      // as two accumulators over the two channel halves
             const uint32_t half = tid == 0 ? 0u : 64u;
-            tc::gemm_ta_split<64, 128>(tmem + TC_PK + half, tmem + TC_PK2 + half, tmem + TC_AS,
-                                       sbase + CH_KQ + b * CH_KQ_STRIDE + half * 2 * 128, SBO128_F16);
+            tc::gemm_ta_split<64, 128, NH>(tmem + TC_PK + half, tmem + TC_PK2 + half, tmem + TC_AS,
+                                           sbase + CH_KQ + b * CH_KQ_STRIDE + half * 2 * 128, SBO128_F16);
             tc::commit(bar + 32);
         }
         // while P runs: S^T <- S^T Diag(gamma) (P reads the fp16 copy only), the previous
@@ -1238,10 +1262,12 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
                 const int cidx = 64 * sub + cc;
                 tc::tmem_ld16(tlane + TC_S + cidx, v);
                 tc::tmem_ld_wait();
+                if (cidx < kr && j < vr) {   // K is a multiple of 16: the group is in or out whole
 #pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    bad |= !(fabsf(v[u]) < INFINITY);
-                    tile[static_cast<int64_t>(cidx + u) * VD + j] = v[u];
+                    for (int u = 0; u < 16; u++) {
+                        bad |= !(fabsf(v[u]) < INFINITY);
+                        tile[static_cast<int64_t>(cidx + u) * vr + j] = v[u];
+                    }
                 }
             }
             flag_nonfinite(bad);
@@ -1299,9 +1325,13 @@ static int64_t total_chunks(const int32_t *cu_host, int64_t num_seqs)
     return t;
 }
 
+// Head sizes the tensor-core path takes: K and V each 64 or 128 (both run on 128 x 128
+// tiles; at 64 the channels or columns past the data are held at zero).
+static bool chunk_dims(int K, int V) { return (K == 64 || K == 128) && (V == 64 || V == 128); }
+
 size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V, int)
 {
-    if (K != chunk::KD || V != chunk::VD || num_seqs <= 0) return 0;
+    if (!chunk_dims(K, V) || num_seqs <= 0) return 0;
     return static_cast<size_t>(total_chunks(cu_host, num_seqs)) * H * chunk::REC_BYTES;
 }
 
@@ -1339,16 +1369,20 @@ static cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t col
 // The prefill chains of entries [entry_base, entry_base + num_seqs): per launch of at most
 // kMaxSeqs sequences, the prep pass over every (chunk, head), then the chains (longest
 // sequence first).
-static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const int32_t *cu_host,
+static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_t *cu, const int32_t *cu_host,
                                      int64_t entry_base, int64_t num_seqs, void *workspace,
                                      cudaStream_t stream)
 {
     using namespace chunk;
     static_assert(sizeof(Args) < 32000, "kernel parameter space");
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the instances for this K and V (64: one half of the 128-wide tile holds data, 128: two)
+    void (*prep)(Args) = K == 64 ? prep_kernel<1> : prep_kernel<2>;
+    void (*chain)(Args) = K == 64 ? (V == 64 ? chain_kernel<1, 1> : chain_kernel<1, 2>)
+                                  : (V == 64 ? chain_kernel<2, 1> : chain_kernel<2, 2>);
+    if ((err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(PREP_SMEM))) != cudaSuccess) return err;
-    if ((err = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((err = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(CHAIN_SMEM))) != cudaSuccess) return err;
     int dev = 0, sms = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -1360,9 +1394,9 @@ static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const i
     // the last sequence's end)
     const int64_t rows = std::max<int64_t>(cu_host[entry_base + num_seqs], 1);
     CUtensorMap tm_qkv, tm_g;
-    if ((err = encode_rows_map(&tm_qkv, p.qkv, 2 * static_cast<int64_t>(p.H) * KD + static_cast<int64_t>(p.H) * VD,
+    if ((err = encode_rows_map(&tm_qkv, p.qkv, 2 * static_cast<int64_t>(p.H) * K + static_cast<int64_t>(p.H) * V,
                                rows, p.ld_qkv)) != cudaSuccess) return err;
-    if ((err = encode_rows_map(&tm_g, p.rg, static_cast<int64_t>(p.H) * KD, rows, p.ld_g)) != cudaSuccess) return err;
+    if ((err = encode_rows_map(&tm_g, p.rg, static_cast<int64_t>(p.H) * K, rows, p.ld_g)) != cudaSuccess) return err;
     for (int64_t s0 = 0; s0 < num_seqs; s0 += kMaxSeqs) {
         const int64_t ns = std::min<int64_t>(kMaxSeqs, num_seqs - s0);
         Args a;
@@ -1387,11 +1421,11 @@ static cudaError_t launch_chunk_path(const Params &p, const int32_t *cu, const i
         for (int64_t i = 0; i < ns; i++) a.order[i] = ord[static_cast<size_t>(i)];
         const int64_t nch = a.cb[ns];
         if (nch > 0) {
-            prep_kernel<<<static_cast<unsigned>(nch * p.H), PT, PREP_SMEM, stream>>>(a);
+            prep<<<static_cast<unsigned>(nch * p.H), PT, PREP_SMEM, stream>>>(a);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
         // every sequence gets a chain CTA: empty ones check their slot and return
-        chain_kernel<<<static_cast<unsigned>(ns * p.H), CT, CHAIN_SMEM, stream>>>(a);
+        chain<<<static_cast<unsigned>(ns * p.H), CT, CHAIN_SMEM, stream>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         ch_done += nch;
     }
@@ -1403,9 +1437,9 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
                                  int, void *workspace, size_t, cudaStream_t stream)
 {
     if (num_seqs <= 0) return cudaSuccess;
-    if (K != chunk::KD || V != chunk::VD)  // other head sizes take the token-recurrent kernel
+    if (!chunk_dims(K, V))  // other head sizes take the token-recurrent kernel
         return launch_recurrent(p, K, V, 2, 1, cu, entry_base, num_seqs, stream);
-    return launch_chunk_path(p, cu, cu_host, entry_base, num_seqs, workspace, stream);
+    return launch_chunk_path(p, K, V, cu, cu_host, entry_base, num_seqs, workspace, stream);
 }
 
 // Mixed batch: the decodes (entries [0, num_decodes), one row each) take the packed-decode

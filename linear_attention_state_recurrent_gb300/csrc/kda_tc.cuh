@@ -106,7 +106,8 @@ __device__ __forceinline__ void gemm_ta(uint32_t d_tmem, uint32_t a_tmem, uint32
 // fp16 pairs; B in shared memory): D0 = A[:, :Kd/2] B[:, :Kd/2]^T and
 // D1 = A[:, Kd/2:] B[:, Kd/2:]^T, their K steps issued alternately so that the two
 // accumulation chains overlap in the tensor pipe. D = D0 + D1.
-template <int N, int KD>
+// NH = 1: the first K half only (D1 untouched).
+template <int N, int KD, int NH = 2>
 __device__ __forceinline__ void gemm_ta_split(uint32_t d0, uint32_t d1, uint32_t a_tmem, uint32_t b_saddr,
                                               uint32_t b_sbo)
 {
@@ -116,7 +117,7 @@ __device__ __forceinline__ void gemm_ta_split(uint32_t d0, uint32_t d1, uint32_t
     for (int ks = 0; ks < HS; ks++) {
         const uint32_t acc = ks > 0 ? 1u : 0u;
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
+        for (int hh = 0; hh < NH; hh++) {
             const int kk = hh * HS + ks;
             const uint64_t db = smem_desc(b_saddr + kk * 256, 128, b_sbo);
             asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"

@@ -144,7 +144,14 @@ def test_workspace_query_is_host_only(kda):
     hd = _heads(kda)
     n = kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
                                                   ctypes.byref(hd), 64)
-    assert n >= 0
+    assert n == (2 + 4 + 1) * 2 * 57856   # one record per (chunk of 64 rows, head)
+    for K, V in ((64, 64), (64, 128), (128, 64)):
+        hk = _heads(kda, K=K, V=V)
+        assert kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
+                                                         ctypes.byref(hk), 64) == n
+    h32 = _heads(kda, K=32, V=64)   # the token-recurrent path needs none
+    assert kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
+                                                     ctypes.byref(h32), 64) == 0
     assert kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
                                                      ctypes.byref(hd), 16) == 0
     assert "chunk_size" in kda.last_error()

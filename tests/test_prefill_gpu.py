@@ -52,6 +52,31 @@ def test_prefill_dims(kda, K, V):
     _run(kda, w, f"prefill K={K} V={V}")
 
 
+@pytest.mark.parametrize("K,V", [(64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("lower_bound", [None, -5.0])
+def test_prefill_chunked_64_wide(kda, K, V, lower_bound):
+    """Heads with K or V of 64 take the tensor-core path on 128 x 128 tiles with the
+    channels / columns past the data held at zero: several chunks, ragged tails, an empty
+    sequence, length 1, a strided index view."""
+    lengths = [1, 63, 64, 65, 0, 200, 129]
+    w = wl.varlen_case(lengths, 4, K, V, seed=K + 7 * V + (0 if lower_bound is None else 1),
+                       lower_bound=lower_bound, index_stride=3)
+    _run(kda, w, f"prefill K={K} V={V} lb={lower_bound}")
+
+
+def test_prefill_chunked_64_strong_decay(kda):
+    """K = V = 64 with heads strong enough to take the pairwise diagonal path."""
+    w = wl.varlen_case([40, 150, 333], 4, 64, 64, seed=19)
+    w.A_log = np.array([3.0, -1.0, 4.0, 0.5], dtype=np.float32)
+    _run(kda, w, "prefill K=V=64 strong decay")
+
+
+def test_mixed_batch_64_wide(kda):
+    w = wl.varlen_case([1] * 6 + [77, 200], 4, 64, 64, seed=95, lower_bound=-5.0, index_stride=2,
+                       num_decodes=6, kind="mixed")
+    _run(kda, w, "mixed K=V=64")
+
+
 def test_prefill_empty_and_length_one(kda):
     w = wl.varlen_case([0, 1, 0, 1, 1], 2, 128, 128, seed=5)
     r = _run(kda, w, "empty/len1")
@@ -226,10 +251,10 @@ def test_mixed_batch_repeat_bit_identical(kda):
         assert torch.equal(snap[0], first[0]) and torch.equal(snap[1], first[1])
 
 
-@pytest.mark.parametrize("K,V", [(128, 128), (64, 64)])
+@pytest.mark.parametrize("K,V", [(128, 128), (64, 64), (32, 32)])
 def test_prefill_empty_sequence_out_of_range_slot(kda, K, V):
     """An empty sequence whose slot is out of range sets the range bit on the chunked path
-    (K = V = 128) and on the token-recurrent one (other head sizes) alike, and touches
+    (K, V in {64, 128}) and on the token-recurrent one (K or V of 32) alike, and touches
     nothing."""
     w = wl.varlen_case([0, 70, 0, 5], 2, K, V, seed=300 + K, num_slots=8)
     w.index_buf = np.array([[9], [1], [2], [3]], np.int32)
@@ -237,7 +262,7 @@ def test_prefill_empty_sequence_out_of_range_slot(kda, K, V):
     assert ref.err_flags == ko.ERR_SLOT_OUT_OF_RANGE
     dw = hx.DeviceWorkload(w)
     out = hx.run_gpu(dw, kda)
-    hx.check(dw, out, ref, fp32_path=(K != 128), label=f"empty out-of-range K={K}")
+    hx.check(dw, out, ref, fp32_path=(K == 32), label=f"empty out-of-range K={K}")
 
 
 def test_prefill_fp16_range_flag(kda):
