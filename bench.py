@@ -649,14 +649,15 @@ def prefill_leg(torch, kda, wl, w, dev, stream, pk, lower_bound, local, calls=20
                               dw.pool_view(), dw.indices_view(), dw.cu, cu_seqlens_host=cu_h,
                               scale=w.scale, out=out, workspace=ws)
     ms, clocks = time_calls_clocked(torch, pf, stream, calls, 3, local)
-    flops = prefill_alg_flops(wl.PREFILL_LENGTHS_SEED1, w.H, w.K, w.V)
+    flops = prefill_alg_flops([b - a for a, b in w.seq_bounds()], w.H, w.K, w.V)
     mb = prefill_min_bytes(w)
     sha = source_sha("kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_f32x2.cuh")
-    traffic = ncu_traffic("prefill (prep_kernel + chain_kernel) chunked_prefill", sha)
+    traffic = ncu_traffic("prefill (prep_kernel + chain_kernel) chunked_prefill", sha) \
+        if (w.K, w.V) == (128, 128) else None
     achieved = mb / (ms * 1e-3) / 1e9
     res = {"metric": "chunk-prefill tokens/s", "value": w.N / (ms * 1e-3), "unit": "tokens/s",
            "ms_per_call": ms, "calls": calls,
-           "workload": "8 seqs (seed-1 lengths, 33,494 tokens), H=32, K=V=128, chunk 64, "
+           "workload": f"8 seqs (seed-1 lengths, 33,494 tokens), H=32, K={w.K}, V={w.V}, chunk 64, "
                        f"lower_bound={lower_bound}",
            "tflops_algorithmic": flops / (ms * 1e-3) / 1e12,
            "frac_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
@@ -709,6 +710,9 @@ def measure_secondary(torch, kda, wl, dev, stream, pk, local=0):
     res["chunk_prefill"] = prefill_leg(torch, kda, wl, w, dev, stream, pk, None, local)
     res["chunk_prefill_lower_bound"] = prefill_leg(torch, kda, wl, wl.chunked_prefill(-5.0), dev, stream, pk,
                                                    -5.0, local)
+    # the same lengths with K = V = 64 heads (the tensor-core path on half-filled tiles)
+    w64 = wl.varlen_case(wl.PREFILL_LENGTHS_SEED1, 32, 64, 64, seed=1, num_slots=16, name="chunked_prefill_k64")
+    res["chunk_prefill_k64"] = prefill_leg(torch, kda, wl, w64, dev, stream, pk, None, local)
     res["mixed_batch"] = mixed_leg(torch, kda, wl, dev, stream, pk, local)
     return res
 
