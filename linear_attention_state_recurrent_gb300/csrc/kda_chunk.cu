@@ -1145,19 +1145,8 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
             for (int i = 0; i < 8; i++) pk8[i] = tc::pack_f16x2(sv[q][2 * i], sv[q][2 * i + 1]);
             tc::tmem_st8u(tlane + TC_AS + 32 * sub + 8 * q, pk8);
         }
-        tc::tmem_st_wait();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0 || tid == 32) {   // P = [(K^G S)^T | (Q^G S)^T], one half per issuing thread, each
-            tc::fence_after_sync();      // as two accumulators over the two channel halves
-            const uint32_t half = tid == 0 ? 0u : 64u;
-            tc::gemm_ta_split<64, 128, NH>(tmem + TC_PK + half, tmem + TC_PK2 + half, tmem + TC_AS,
-                                           sbase + CH_KQ + b * CH_KQ_STRIDE + half * 2 * 128, SBO128_F16);
-            tc::commit(bar + 32);
-        }
-        // while P runs: S^T <- S^T Diag(gamma) (P reads the fp16 copy only), the previous
-        // chunk's O rows, and this chunk's V values
-        {
+        {   // S^T <- S^T Diag(gamma), stored before P is issued (TMEM stores beside a running
+            // product slow it down; P reads the fp16 copy only)
             const float *gam = reinterpret_cast<const float *>(smem + CH_KQ + b * CH_KQ_STRIDE + REC_GAM);
 #pragma unroll
             for (int q = 0; q < 4; q++) {
@@ -1170,6 +1159,17 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
                 tc::tmem_st16(tlane + TC_S + cidx, sv[q]);
             }
         }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0 || tid == 32) {   // P = [(K^G S)^T | (Q^G S)^T], one half per issuing thread, each
+            tc::fence_after_sync();      // as two accumulators over the two channel halves
+            const uint32_t half = tid == 0 ? 0u : 64u;
+            tc::gemm_ta_split<64, 128, NH>(tmem + TC_PK + half, tmem + TC_PK2 + half, tmem + TC_AS,
+                                           sbase + CH_KQ + b * CH_KQ_STRIDE + half * 2 * 128, SBO128_F16);
+            tc::commit(bar + 32);
+        }
+        // while P runs: the previous chunk's O rows, and this chunk's V values
         if (c > 0) {
 #pragma unroll
             for (int q = 0; q < 2; q++)
