@@ -83,6 +83,14 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     const int cg = tid & 7;
     const int rg = tid >> 3;
 
+    // Programmatic dependent launch: this grid may be launched while the kernel before it
+    // in the stream finishes, if that kernel allows it; every read of global memory comes
+    // after the wait, which returns once that kernel has completed and its writes are
+    // visible. The next kernel in the stream may launch as soon as every CTA here has
+    // started (its own wait still orders it after this grid).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     const int64_t b = blockIdx.x;
     const int vs = static_cast<int>(b % VS);
     const int h = static_cast<int>((b / VS) % p.H);
@@ -473,11 +481,20 @@ static cudaError_t launch_rec_kv(const Params &p, int mode, int T, const int32_t
                                  int64_t entry_base, int64_t num_entries, cudaStream_t stream)
 {
     const int64_t grid = num_entries * p.H * (V / 32);
+    // launched with programmatic stream serialization (see the kernel's first lines)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (mode == kRowsDecode)
-        recurrent_kernel<K, V, true><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, mode, T, cu, entry_base);
-    else
-        recurrent_kernel<K, V, false><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, mode, T, cu, entry_base);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, recurrent_kernel<K, V, true>, p, mode, T, cu, entry_base);
+    return cudaLaunchKernelEx(&cfg, recurrent_kernel<K, V, false>, p, mode, T, cu, entry_base);
 }
 
 cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
