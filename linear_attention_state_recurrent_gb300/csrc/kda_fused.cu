@@ -12,6 +12,7 @@
 #include "kda_common.cuh"
 #include "kda_f32x2.cuh"
 #include "kda_launch.h"
+#include "kda_pdl.cuh"
 
 namespace kda {
 
@@ -84,6 +85,7 @@ head_kernel(Params p, TailParams tp, int T)
     HeadSmem<K, V, MAXT> &sm = *reinterpret_cast<HeadSmem<K, V, MAXT> *>(head_dsm);
     float4 *stage = reinterpret_cast<float4 *>(head_dsm + (sizeof(HeadSmem<K, V, MAXT>) + 15) / 16 * 16);
 
+    pdl_wait_then_release();   // launched by launch_pdl: no global read before this
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid % CG, rgp = tid / CG, r0 = rgp * RPT, j0 = 4 * cg;
     const int h = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.H));
@@ -399,8 +401,7 @@ cudaError_t launch_head_kv(const Params &p, const TailParams &tp, int T, int64_t
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const int64_t grid = num_entries * p.H;
-    head_kernel<K, V, MAXT><<<static_cast<unsigned>(grid), 128, smem, stream>>>(p, tp, T);
-    return cudaGetLastError();
+    return launch_pdl(head_kernel<K, V, MAXT>, dim3(static_cast<unsigned>(grid)), dim3(128), smem, stream, p, tp, T);
 }
 
 template <int K, int V>

@@ -9,6 +9,7 @@
 // entry's tokens, stored once. Gate, beta and the q/k L2 norms are fused in.
 #include "kda_common.cuh"
 #include "kda_launch.h"
+#include "kda_pdl.cuh"
 
 namespace kda {
 
@@ -83,13 +84,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     const int cg = tid & 7;
     const int rg = tid >> 3;
 
-    // Programmatic dependent launch: this grid may be launched while the kernel before it
-    // in the stream finishes, if that kernel allows it; every read of global memory comes
-    // after the wait, which returns once that kernel has completed and its writes are
-    // visible. The next kernel in the stream may launch as soon as every CTA here has
-    // started (its own wait still orders it after this grid).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_wait_then_release();   // launched by launch_pdl: no global read before this
 
     const int64_t b = blockIdx.x;
     const int vs = static_cast<int>(b % VS);
@@ -253,6 +248,7 @@ __global__ void __launch_bounds__(128, CKPT ? 6 : 7) spec_kernel(Params p, int T
     __shared__ float4 s_v[kSpecMaxT][VT / 4];      // this CTA's value columns of every token
     __shared__ int64_t s_col[CKPT ? kSpecMaxT : 1]; // checkpoint slot of every token
 
+    pdl_wait_then_release();   // launched by launch_pdl: no global read before this
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, cg = tid & 7, rg = tid >> 3;
     const int64_t b = blockIdx.x;
     const int vs = static_cast<int>(b % VS);
@@ -429,8 +425,8 @@ static cudaError_t launch_spec_kv(const Params &p, int T, int64_t num_reqs,
                                   const int32_t *num_accepted, cudaStream_t stream)
 {
     const int64_t grid = num_reqs * p.H * (V / 32);
-    spec_kernel<K, V, CKPT><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p, T, num_accepted);
-    return cudaGetLastError();
+    return launch_pdl(spec_kernel<K, V, CKPT>, dim3(static_cast<unsigned>(grid)), dim3(128), 0, stream, p, T,
+                      num_accepted);
 }
 
 template <bool CKPT>
@@ -481,20 +477,10 @@ static cudaError_t launch_rec_kv(const Params &p, int mode, int T, const int32_t
                                  int64_t entry_base, int64_t num_entries, cudaStream_t stream)
 {
     const int64_t grid = num_entries * p.H * (V / 32);
-    // launched with programmatic stream serialization (see the kernel's first lines)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 g(static_cast<unsigned>(grid)), blk(128);
     if (mode == kRowsDecode)
-        return cudaLaunchKernelEx(&cfg, recurrent_kernel<K, V, true>, p, mode, T, cu, entry_base);
-    return cudaLaunchKernelEx(&cfg, recurrent_kernel<K, V, false>, p, mode, T, cu, entry_base);
+        return launch_pdl(recurrent_kernel<K, V, true>, g, blk, 0, stream, p, mode, T, cu, entry_base);
+    return launch_pdl(recurrent_kernel<K, V, false>, g, blk, 0, stream, p, mode, T, cu, entry_base);
 }
 
 cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
