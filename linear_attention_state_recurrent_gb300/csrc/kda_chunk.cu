@@ -54,6 +54,7 @@
 #include "kda_common.cuh"
 #include "kda_f32x2.cuh"
 #include "kda_launch.h"
+#include "kda_pdl.cuh"
 #include "kda_tc.cuh"
 
 namespace kda {
@@ -492,6 +493,9 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     int h, n, sq = -1;
     int64_t row0;
     locate(bid, h, row0, n, sq);
+    // launched by launch_pdl: the barriers, the unit's location and the tensor-map
+    // prefetches above read kernel parameters only; every global read comes after this
+    pdl_wait_then_release();
 
     // ---- raw_g, then q and k (into the B-operand regions, free until operand generation)
     // by tensor copies from thread 0, issued before the tensor-memory allocation; thread 32
@@ -1008,6 +1012,7 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
 {
     extern __shared__ __align__(1024) unsigned char smem[];
     const Params &p = a.p;
+    pdl_wait_then_release();   // launched by launch_pdl: no global read before this
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
     const int rank = static_cast<int>(blockIdx.x / H), h = static_cast<int>(blockIdx.x % H);
@@ -1421,12 +1426,12 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
         for (int64_t i = 0; i < ns; i++) a.order[i] = ord[static_cast<size_t>(i)];
         const int64_t nch = a.cb[ns];
         if (nch > 0) {
-            prep<<<static_cast<unsigned>(nch * p.H), PT, PREP_SMEM, stream>>>(a);
-            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            if ((err = launch_pdl(prep, dim3(static_cast<unsigned>(nch * p.H)), dim3(PT), PREP_SMEM, stream, a)) !=
+                cudaSuccess) return err;
         }
         // every sequence gets a chain CTA: empty ones check their slot and return
-        chain<<<static_cast<unsigned>(ns * p.H), CT, CHAIN_SMEM, stream>>>(a);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if ((err = launch_pdl(chain, dim3(static_cast<unsigned>(ns * p.H)), dim3(CT), CHAIN_SMEM, stream, a)) !=
+            cudaSuccess) return err;
         ch_done += nch;
     }
     return cudaSuccess;
