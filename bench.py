@@ -362,7 +362,7 @@ def main():
     total_bytes = w_full.state_bytes_per_call()     # all ranks together
     value = total_bytes * args.steps / (ms_total * 1e-3) / 1e9
     achieved = state_bytes / (ms_step * 1e-3) / 1e9
-    sha = source_sha("kda_recurrent.cu", "kda_common.cuh")
+    sha = source_sha("kda_recurrent.cu", "kda_common.cuh", "kda_pdl.cuh")
     traffic = ncu_traffic("recurrent_kernel<128,128> serving_decode", sha)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
@@ -667,7 +667,7 @@ def prefill_leg(torch, kda, wl, w, dev, stream, pk, lower_bound, local, calls=20
     ms, clocks = time_calls_clocked(torch, pf, stream, calls, 3, local)
     flops = prefill_alg_flops([b - a for a, b in w.seq_bounds()], w.H, w.K, w.V)
     mb = prefill_min_bytes(w)
-    sha = source_sha("kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_f32x2.cuh")
+    sha = source_sha("kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_f32x2.cuh", "kda_pdl.cuh")
     traffic = ncu_traffic("prefill (prep_kernel + chain_kernel) chunked_prefill", sha) \
         if (w.K, w.V) == (128, 128) else None
     achieved = mb / (ms * 1e-3) / 1e9
