@@ -297,9 +297,16 @@ int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t 
  * recurrent decode path; sequences num_decodes..num_decodes+num_prefills-1 take
  * the chunked prefill path. One cu_seqlens (device + host copies) and one strided
  * index view cover all of them, decodes first. The decodes run the packed-decode kernel
- * (the same code path as kda_packed_decode), then the prefills run kda_chunk_prefill's
- * kernels, on `stream` in that order. Workspace as for kda_chunk_prefill over the prefill
- * sequences:
+ * (recurrent_kernel, rows located through cu_seqlens); the prefills run kda_chunk_prefill's
+ * kernels on `stream`. When both are present and K, V are in {64, 128}, the decodes run on
+ * a low-priority stream of the library that starts once the prefill's first kernel is done
+ * (so that they take the SMs the prefill chains leave free) and is joined back into
+ * `stream` within the call: everything enqueued on `stream` after the call sees all its
+ * results. The library creates that stream and two events once per device, on the first
+ * such call there (make it before any stream capture), keeps them until exit, and
+ * serialises the enqueue of concurrent mixed calls from different host threads.
+ * Otherwise the decodes run first on `stream`. Workspace as for kda_chunk_prefill over the
+ * prefill sequences:
  * kda_chunk_prefill_workspace_bytes(cu_seqlens_host + num_decodes, num_prefills, ...).
  * The prefills' range limit and error bits are kda_chunk_prefill's.
  */

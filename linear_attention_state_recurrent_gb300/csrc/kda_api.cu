@@ -1,6 +1,8 @@
 // extern "C" entry points of libkda (declared in include/kda.h): host-side
 // argument checks, then kernel launches on the caller's stream. Nothing here
-// allocates, synchronises or keeps state between calls.
+// allocates device memory or synchronises; the only state kept between calls is the
+// mixed batch's side stream and events (one set per device, kda_chunk.cu) and the
+// no-allocation prefill's scratch address (kda_noalloc.cu).
 #include <climits>
 #include <cmath>
 #include <cstdarg>

@@ -44,6 +44,7 @@
 // fp16 (11-bit significand, round to nearest) carries the same precision as tf32 with
 // round to nearest; bf16 operands would exceed the 2e-3 relative error bar.
 #include <algorithm>
+#include <mutex>
 #include <numeric>
 #include <vector>
 
@@ -1374,9 +1375,11 @@ static cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t col
 // The prefill chains of entries [entry_base, entry_base + num_seqs): per launch of at most
 // kMaxSeqs sequences, the prep pass over every (chunk, head), then the chains (longest
 // sequence first).
+// after_prep: if not null, recorded on `stream` once the first launch's prep kernel is
+// enqueued (before its chain kernel).
 static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_t *cu, const int32_t *cu_host,
                                      int64_t entry_base, int64_t num_seqs, void *workspace,
-                                     cudaStream_t stream)
+                                     cudaStream_t stream, cudaEvent_t after_prep = nullptr)
 {
     using namespace chunk;
     static_assert(sizeof(Args) < 32000, "kernel parameter space");
@@ -1429,6 +1432,7 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
             if ((err = launch_pdl(prep, dim3(static_cast<unsigned>(nch * p.H)), dim3(PT), PREP_SMEM, stream, a)) !=
                 cudaSuccess) return err;
         }
+        if (after_prep && s0 == 0 && (err = cudaEventRecord(after_prep, stream)) != cudaSuccess) return err;
         // every sequence gets a chain CTA: empty ones check their slot and return
         if ((err = launch_pdl(chain, dim3(static_cast<unsigned>(ns * p.H)), dim3(CT), CHAIN_SMEM, stream, a)) !=
             cudaSuccess) return err;
@@ -1449,9 +1453,55 @@ cudaError_t launch_chunk_prefill(const Params &p, int K, int V, const int32_t *c
 
 // Mixed batch: the decodes (entries [0, num_decodes), one row each) take the packed-decode
 // kernel, the prefills the chunk path.
+// The side stream a mixed batch hands its decodes to, and its two events: one set per
+// device, created on first use (lowest stream priority, no timing) and kept.
+namespace {
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t after_prep = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+SideStream g_side[kMaxSideDevices];
+std::mutex g_side_mutex;   // guards the creation and every hand-over ... join sequence
+}  // namespace
+
+static cudaError_t side_stream_locked(SideStream **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxSideDevices) return cudaErrorInvalidDevice;
+    SideStream &ss = g_side[dev];
+    if (!ss.s) {
+        int lo = 0, hi = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, lo)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.after_prep, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &ss;
+    return cudaSuccess;
+}
+
 cudaError_t launch_mixed(const Params &p, int K, int V, const int32_t *cu, const int32_t *cu_host,
                          int64_t num_decodes, int64_t num_prefills, void *workspace, cudaStream_t stream)
 {
+    if (num_decodes > 0 && num_prefills > 0 && chunk_dims(K, V)) {
+        // The decodes run beside the prefill chains: a chain CTA holds a whole SM and the
+        // chains of a batch rarely fill the GPU, so the (HBM-bound) decodes go to a
+        // low-priority side stream that starts once the prep kernel is done, takes the SMs
+        // the chains leave, and is joined back before the call returns.
+        std::lock_guard<std::mutex> lock(g_side_mutex);
+        SideStream *ss = nullptr;
+        cudaError_t e = side_stream_locked(&ss);
+        if (e != cudaSuccess) return e;
+        if ((e = launch_chunk_path(p, K, V, cu, cu_host, num_decodes, num_prefills, workspace, stream,
+                                   ss->after_prep)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(ss->s, ss->after_prep, 0)) != cudaSuccess) return e;
+        if ((e = launch_recurrent(p, K, V, 2, 1, cu, 0, num_decodes, ss->s)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
+        return cudaStreamWaitEvent(stream, ss->join, 0);
+    }
     if (num_decodes > 0) {
         cudaError_t e = launch_recurrent(p, K, V, 2, 1, cu, 0, num_decodes, stream);
         if (e != cudaSuccess) return e;
