@@ -230,3 +230,23 @@ def test_bounded_wait_gives_up_and_context_stays_usable(kda):
     assert int(err.item()) == kda.KDA_ERRFLAG_TIMEOUT
     assert time.perf_counter() - t0 >= 1.5
     _run_and_check(kda, wl.tiny_decode(), "decode after a timed-out wait")
+
+
+def test_back_to_back_dependent_decodes(kda):
+    """T decode calls in a row on the same slots, nothing launched between them: each one
+    reads the state the previous one wrote (the decode grid may launch while its
+    predecessor finishes, and must wait for it before its first read). Together they equal
+    spec-verify over the same T tokens."""
+    w = wl.spec_verify(seed=81, num_reqs=12, T=6, H=4, num_padding=0, lower_bound=-5.0)
+    dw = hx.DeviceWorkload(w)
+    R, T, H, K, V = w.num_entries, w.tokens_per_req, w.H, w.K, w.V
+    C = dw.mixed_qkv.shape[1]
+    out = torch.zeros(w.N, H * V, dtype=torch.bfloat16, device=dw.device)
+    qkv3, g3, b3 = dw.mixed_qkv.view(R, T, C), dw.raw_g.view(R, T, -1), dw.raw_beta.view(R, T, -1)
+    out3 = out.view(R, T, H * V)
+    for t in range(T):
+        kda.kda_packed_decode(qkv3[:, t], g3[:, t], b3[:, t], dw.A_log, dw.dt_bias, w.lower_bound,
+                              dw.pool_view(), dw.indices_view(), scale=w.scale, l2_eps=w.eps,
+                              null_slot=w.null_slot, out=out3[:, t], err_flags=dw.err)
+    ref = ko.run(w)
+    hx.check(dw, out, ref, fp32_path=True, label="back-to-back decodes")
