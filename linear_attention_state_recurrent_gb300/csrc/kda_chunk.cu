@@ -1232,8 +1232,8 @@ __global__ void __launch_bounds__(CT, 1) chain_kernel(const __grid_constant__ Ar
                 if (tid == 0)
                     tc::gemm_ta<64, 64>(tmem + TC_PQ, tmem + TC_AY, sbase + CH_MM + b * REC_B_BYTES, SBO64_F16, true);
                 else
-                    tc::gemm_ta<128, 64>(tmem + TC_S, tmem + TC_AY, sbase + CH_MM + b * REC_B_BYTES + 8 * 1024,
-                                         SBO64_F16, true);
+                    tc::gemm_ta<64 * NH, 64>(tmem + TC_S, tmem + TC_AY, sbase + CH_MM + b * REC_B_BYTES + 8 * 1024,
+                                             SBO64_F16, true);   // K = 64: the state columns past K stay zero
             }
             tc::commit(bar + 32);
         }
