@@ -124,6 +124,8 @@ constexpr uint32_t TM_XDIAG = 96;   // X_diag  64 columns
 constexpr uint32_t TM_A = 160;      // tf32 A operand [K^e; Q^e] of the current channel half (64 columns)
 constexpr uint32_t TM_W1 = 0;       // [Aqk; Kd^T rows 0..63] T diag(beta)   (after assembly)
 constexpr uint32_t TM_W2 = 64;      // Kd^T T diag(beta)
+constexpr uint32_t TM_L3X = 160;    // the solve's last level: X^T (32 columns)
+constexpr uint32_t TM_L3T = 192;    //                         X^T T_b^T (32 columns)
 
 // per-(block, channel) constants, [block][constant][channel of the half]
 enum Tab { kP1 = 1, kE = 2, kBD = 3, kD4 = 4, kD2 = 5, kD3 = 6 };   // kP1: the block's log2 decay
@@ -281,12 +283,13 @@ __device__ __forceinline__ void scale8(float *d, const float *a, float sc)
     }
 }
 // ---------------------------------------------------------------------------
-// T = (I + A)^-1 for the strictly lower 64x64 A in AMAT (fp32, pitch AP) by 16x16
-// diagonal-block inverses and two levels of block doubling (256 threads). Each level
-// writes its final entries of T diag(beta), transposed and in fp16, to the operand tile
-// at `tbt` (row m, K = k holds T[k][m] beta_m); the six zero blocks of the transpose are
-// written during the first level, so the tile is complete (and fenced for the async
-// proxy) when the solve returns. The fp32 T keeps only what later levels read.
+// T = (I + A)^-1 for the strictly lower 64x64 A in AMAT (fp32, pitch AP), first two
+// levels (256 threads): the 16x16 diagonal-block inverses, then the block doubling to the
+// two 32x32 diagonal blocks T_a, T_b. Each level writes its final entries of T diag(beta),
+// transposed and in fp16, to the operand tile at `tbt` (row m, K = k holds T[k][m]
+// beta_m); the six zero blocks of the transpose are written during the first level. The
+// fp32 T keeps only what later levels read. The last level (the block T_ba) runs on the
+// tensor cores in the prep kernel.
 // ---------------------------------------------------------------------------
 __device__ void solve_T(unsigned char *smem, int tid, uint32_t tbt, const float *beta)
 {
@@ -349,40 +352,8 @@ __device__ void solve_T(unsigned char *smem, int tid, uint32_t tbt, const float 
         st_shared_u16(tbt + tc::core_offset(o + j + 1, o + 16 + r, 64, 2), f16_bits(-y.y * beta[o + j + 1]));
     }
     __syncthreads();
-    // level 3: X = A_ba T_a (32x32), T_ba = -T_b X; 2x2 output tiles, rows in packed pairs
-    {
-        const int r = (tid >> 4) * 2, j = (tid & 15) * 2;
-        float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
-        for (int m = j; m < 32; m++) {           // T_a is lower triangular: m >= j
-            const float a0 = A[(32 + r) * AP + m], a1 = A[(33 + r) * AP + m];
-            float2 t = *reinterpret_cast<const float2 *>(T + m * AP + j);
-            if (m < j + 1) t.y = 0.f;
-            x0 = ffma2(make_float2(a0, a0), t, x0);
-            x1 = ffma2(make_float2(a1, a1), t, x1);
-        }
-        *reinterpret_cast<float2 *>(X + r * 36 + j) = x0;
-        *reinterpret_cast<float2 *>(X + (r + 1) * 36 + j) = x1;
-    }
-    __syncthreads();
-    {
-        const int r = (tid >> 4) * 2, j = (tid & 15) * 2;
-        float2 y0 = make_float2(0.f, 0.f), y1 = make_float2(0.f, 0.f);
-        for (int m = 0; m <= r + 1; m++) {       // T_b is lower triangular: m <= row
-            const float t0 = (m <= r) ? T[(32 + r) * AP + 32 + m] : 0.f;
-            const float t1 = T[(33 + r) * AP + 32 + m];
-            const float2 x = *reinterpret_cast<const float2 *>(X + m * 36 + j);
-            y0 = ffma2(make_float2(t0, t0), x, y0);
-            y1 = ffma2(make_float2(t1, t1), x, y1);
-        }
-        // T_ba is final and read by no later level: only its scaled fp16 transpose is
-        // stored, rows 32 + r, 33 + r of columns j, j + 1 as K pairs of rows j, j + 1
-        const float bj0 = beta[j], bj1 = beta[j + 1];
-        st_shared_u32(tbt + tc::core_offset(j, 32 + r, 64, 2), tc::pack_f16x2(-y0.x * bj0, -y1.x * bj0));
-        st_shared_u32(tbt + tc::core_offset(j + 1, 32 + r, 64, 2), tc::pack_f16x2(-y0.y * bj1, -y1.y * bj1));
-    }
-    tc::fence_proxy_async();   // the transpose is read by the products issued after the barrier
-    __syncthreads();
 }
+
 
 __device__ __forceinline__ void ex2_8(float *d)
 {
@@ -936,6 +907,91 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     // ================= T = (I + A)^-1, then [Aqk; Kd^T] T diag(beta) =================
     if (ok) {
         solve_T(smem, tid, sbase + SM_TT, betas);
+        // last level on the tensor cores (tf32): X^T = T_a^T A_ba^T (32 x 32), then
+        // T_ba^T = -(X^T T_b^T) with X^T read from tensor memory. Operand tiles (K-major,
+        // 32 K, SBO 1024): T_a^T at SM_BDIAG (the product is M = 128: its rows 32..127 read
+        // the rest of that region and land in lanes nothing reads), A_ba at SM_XTMP, T_b
+        // at SM_XD. The upper triangles of T_a and T_b are not stored in SM_TMAT: zeros.
+        const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
+        const int row = tid >> 3, k4 = (tid & 7) * 4;   // one 16-byte chunk of each tile per thread
+        const uint32_t off = tc::core_offset(row, k4, 32, 4);
+        {
+            const float *Am = reinterpret_cast<const float *>(smem + SM_AMAT);
+            float ta[4], ab[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int m = k4 + u;
+                ta[u] = m >= row ? Tm[m * AP + row] : 0.f;                  // T_a^T[row][m] = T_a[m][row]
+            }
+            const float4 a4 = *reinterpret_cast<const float4 *>(Am + (32 + row) * AP + k4);   // A_ba[row][k4..]
+            ab[0] = a4.x; ab[1] = a4.y; ab[2] = a4.z; ab[3] = a4.w;
+            st_shared_u4(sbase + SM_BDIAG + off, pack4_tf32(ta));
+            st_shared_u4(sbase + SM_XTMP + off, pack4_tf32(ab));
+        }
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0 || tid == 32) {
+            tc::fence_after_sync();
+            if (tid == 0) tc::gemm<2, 32, 32>(tmem + TM_L3X, sbase + SM_BDIAG, 1024, sbase + SM_XTMP, 1024, false);
+            tc::commit(mbar);
+        }
+        {   // T_b, the second product's B operand, while the first runs
+            float tb[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int m = k4 + u;
+                tb[u] = m <= row ? Tm[(32 + row) * AP + 32 + m] : 0.f;      // T_b[row][m]
+            }
+            st_shared_u4(sbase + SM_XD + off, pack4_tf32(tb));
+            tc::fence_proxy_async();
+        }
+        ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
+        phase ^= 1;
+    }
+    if (ok) {
+        if (warp == 0) {   // X^T (lanes 0..31) rounded to tf32 in place: the next product's A operand
+            float x0[16], x1[16];
+            tc::tmem_ld16(tlane + TM_L3X, x0);
+            tc::tmem_ld16(tlane + TM_L3X + 16, x1);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                x0[u] = __uint_as_float(tf32_rna(x0[u]));
+                x1[u] = __uint_as_float(tf32_rna(x1[u]));
+            }
+            tc::tmem_st16(tlane + TM_L3X, x0);
+            tc::tmem_st16(tlane + TM_L3X + 16, x1);
+            tc::tmem_st_wait();
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0 || tid == 32) {
+            tc::fence_after_sync();
+            if (tid == 0) tc::gemm_ta_tf32<32, 32>(tmem + TM_L3T, tmem + TM_L3X, sbase + SM_XD, 1024, false);
+            tc::commit(mbar);
+        }
+        ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
+        phase ^= 1;
+    }
+    if (ok) {
+        if (warp == 0) {   // T_ba = -(X^T T_b^T)^T -> rows j of the (T diag(beta))^T tile, K = 32..63
+            float y0[16], y1[16];
+            tc::tmem_ld16(tlane + TM_L3T, y0);
+            tc::tmem_ld16(tlane + TM_L3T + 16, y1);
+            tc::tmem_ld_wait();
+            const float nb = -betas[lane];
+#pragma unroll
+            for (int u = 0; u < 16; u++) { y0[u] *= nb; y1[u] *= nb; }
+            const uint32_t tt = sbase + SM_TT;
+            st_shared_u4(tt + tc::core_offset(lane, 32, 64, 2), pack8_f16(y0));
+            st_shared_u4(tt + tc::core_offset(lane, 40, 64, 2), pack8_f16(y0 + 8));
+            st_shared_u4(tt + tc::core_offset(lane, 48, 64, 2), pack8_f16(y1));
+            st_shared_u4(tt + tc::core_offset(lane, 56, 64, 2), pack8_f16(y1 + 8));
+        }
+        tc::fence_proxy_async();   // the transpose is read by the products issued after the barrier
+        tc::fence_before_sync();
+        __syncthreads();
         if (tid == 0 || tid == 32) {
             tc::fence_after_sync();
             if (tid == 0)
