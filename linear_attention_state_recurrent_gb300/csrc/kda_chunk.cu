@@ -913,7 +913,8 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         // the rest of that region and land in lanes nothing reads), A_ba at SM_XTMP, T_b
         // at SM_XD. The upper triangles of T_a and T_b are not stored in SM_TMAT: zeros.
         const float *Tm = reinterpret_cast<const float *>(smem + SM_TMAT);
-        const int row = tid >> 3, k4 = (tid & 7) * 4;   // one 16-byte chunk of each tile per thread
+        const int row = tid & 31, k4 = (tid >> 5) * 4;  // one 16-byte chunk of each tile per thread
+                                                         // (a warp: 32 rows of one K chunk)
         const uint32_t off = tc::core_offset(row, k4, 32, 4);
         {
             const float *Am = reinterpret_cast<const float *>(smem + SM_AMAT);
@@ -937,12 +938,11 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             tc::commit(mbar);
         }
         {   // T_b, the second product's B operand, while the first runs
-            float tb[4];
+            const float4 b4 = *reinterpret_cast<const float4 *>(Tm + (32 + row) * AP + 32 + k4);   // T_b[row][k4..]
+            float tb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const int m = k4 + u;
-                tb[u] = m <= row ? Tm[(32 + row) * AP + 32 + m] : 0.f;      // T_b[row][m]
-            }
+            for (int u = 0; u < 4; u++)
+                if (k4 + u > row) tb[u] = 0.f;   // above T_b's diagonal: not stored
             st_shared_u4(sbase + SM_XD + off, pack4_tf32(tb));
             tc::fence_proxy_async();
         }
