@@ -510,7 +510,7 @@ def run_row(args, torch, kda, wl, dev, stream, pk, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "tokens": w.N, "H": w.H, "K": w.K, "V": w.V},
-            "clocks": clk.summary(), "gpu_launches": args.steps * {"prefill": 2, "mixed": 3}.get(args.workload, 1)}
+            "clocks": clk.summary(), "gpu_launches": args.steps * {"prefill": 3, "mixed": 4}.get(args.workload, 1)}
     if args.workload == "prefill":
         flops = prefill_alg_flops([b - a for a, b in w.seq_bounds()], w.H, w.K, w.V)
         line["tflops_algorithmic"] = flops / (ms * 1e-3) / 1e12

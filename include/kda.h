@@ -266,13 +266,15 @@ size_t kda_chunk_prefill_workspace_bytes(const int32_t *cu_seqlens_host, int64_t
  * `workspace` (device, 256-byte aligned, owned by the caller) must hold
  * kda_chunk_prefill_workspace_bytes(...) bytes: with K and V each 64 or 128 (the tensor-core
  * path, which works on 128 x 128 tiles with the channels or columns past 64 held at zero)
- * one 57,856-byte record per
- * (chunk of 64 rows, head), written by the call's first kernel (the intra-chunk pass over
- * every chunk in parallel) and read by its second (the per-sequence state chain); its
- * contents are scratch between calls. It may be NULL when the size is 0 (K or V of 32: the
+ * one 57,856-byte record per (chunk of 64 rows, head), then one flag byte per record
+ * (rounded up to 16 bytes). The call's first kernel (the intra-chunk pass over every chunk
+ * in parallel) writes the records and flags; the second redoes the records whose flag
+ * is set: a channel half that decays by more than 80 nats within 16 rows, computed
+ * pairwise in fp32. The third (the per-sequence state chain) reads them. The contents are
+ * scratch between calls. It may be NULL when the size is 0 (K or V of 32: the
  * token-recurrent kernel).
  * Calls that share a workspace must not overlap on the device. On the tensor-core path the call is
- * two launches per 1024 sequences.
+ * three launches per 1024 sequences.
  * Zero-length sequences are allowed: their slot is left untouched (a slot >= num_slots is
  * still flagged).
  * Precision and range (tensor-core path): the products take fp16 / tf32 operands with
@@ -329,8 +331,8 @@ int kda_mixed_batch(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t *r
  * library's code holds until the process exits. The call allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine).
  * - Size limit: the call needs kda_chunk_prefill_workspace_bytes(...) bytes of scratch, one
- *   57,856-byte record per (chunk of 64 rows, head) with K and V in {64, 128} (e.g. 1,159 chunk-heads:
- *   36 chunks at H = 32). A larger request is rejected, before any CUDA call, with
+ *   57,856-byte record and one flag byte per (chunk of 64 rows, head) with K and V in
+ *   {64, 128} (at most 1,159 chunk-heads, e.g. 36 chunks at H = 32). A larger request is rejected, before any CUDA call, with
  *   KDA_ERR_WORKSPACE and a message naming both sizes; split it or use kda_chunk_prefill.
  *   Other head sizes need no scratch.
  * - Set-up: the first call on a device that needs scratch looks up the array's device

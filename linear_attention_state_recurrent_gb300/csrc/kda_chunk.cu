@@ -141,6 +141,9 @@ struct Args {
     int32_t num_seqs;
     int32_t pf_stride;         // prep: the unit whose inputs a CTA prefetches into L2 (bid + pf_stride)
     unsigned char *rec;        // records of this launch: (chunk, head) at (cb + j) * H + h
+    unsigned char *flags;      // unit flags of the call (16-byte aligned, after every record): 1 where
+                               // the unit needs the pairwise path; this launch's unit u at flag0 + u
+    int32_t flag0;
     int32_t cb[kMaxSeqs + 1];  // chunk prefix over the launch's sequences
     int32_t rs[kMaxSeqs + 1];  // row starts of the launch's sequences (the host copy of cu_seqlens)
     int32_t order[kMaxSeqs];   // chain order: longest sequence first
@@ -411,8 +414,15 @@ __device__ __forceinline__ float gate_log2(float x, float expA, float expA_l2e, 
 // split between the two threads of a row: the K thread takes the first 16 of the 32
 // channels, the Q thread the last 16. The gate pass uses channel c = tid & 63 of the
 // half and row block tid >> 6.
+//
+// Two instances per K. PW = false: one CTA per unit, without the pairwise path. A unit in
+// which some channel half needs that path is only marked in the unit flags, and its
+// [M1; M2] are not written. PW = true: the pass over the marked units, with the pairwise
+// path. A grid of a few CTAs per SM runs it; each CTA takes the marked units whose rank
+// among them is congruent to its index. Keeping the pairwise code out of the first
+// instance keeps that instance's code small and its registers for the common path.
 // ---------------------------------------------------------------------------
-template <int NH>   // channel halves that hold data: K = 64 NH
+template <int NH, bool PW>   // NH: channel halves that hold data (K = 64 NH)
 __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Args a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -460,20 +470,13 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         const int64_t rem = static_cast<int64_t>(a.rs[sq + 1]) - r0;
         nn = static_cast<int>(rem < C ? rem : C);
     };
-    const int bid = static_cast<int>(blockIdx.x);   // this CTA's unit; the unit pf_stride later starts on
-                                                     // a CTA slot about when this one ends
-    int h, n, sq = -1;
-    int64_t row0;
-    locate(bid, h, row0, n, sq);
-    // launched by launch_pdl: the barriers, the unit's location and the tensor-map
-    // prefetches above read kernel parameters only; every global read comes after this
-    pdl_wait_then_release();
-
     // ---- raw_g, then q and k (into the B-operand regions, free until operand generation)
     // by tensor copies from thread 0, issued before the tensor-memory allocation; thread 32
-    // prefetches a later unit's boxes into L2. The first gate pass runs while q and k are
-    // still in flight. Rows past the chunk hold the next sequence's rows (or zeros past the
-    // tensor) and are masked where read. ----
+    // prefetches a later unit's boxes into L2 (the unit pf_stride later starts on a CTA
+    // slot about when this one ends). The first gate pass runs while q and k are still in
+    // flight. Rows past the chunk hold the next sequence's rows (or zeros past the tensor)
+    // and are masked where read. ----
+    auto issue_loads = [&](const int bid, const int h, const int64_t row0, const int sq) {
     if (tid == 0) {
         const int y = static_cast<int>(row0), xg = h * kr;
         tc::mbar_expect_tx(lbar, 8192u * nhalf);
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             tc::tma_load_2d(sbase + SM_QSTG + 8192 * hf, &a.tm_qkv, xg + 64 * hf, y, lbar + 8);
             tc::tma_load_2d(sbase + SM_KSTG + 8192 * hf, &a.tm_qkv, static_cast<int>(HK) + xg + 64 * hf, y, lbar + 8);
         }
-    } else if (tid == 32 && bid + a.pf_stride < total) {
+    } else if (!PW && tid == 32 && bid + a.pf_stride < total) {
         int h2, n2, sq2 = sq;
         int64_t r2;
         locate(bid + a.pf_stride, h2, r2, n2, sq2);
@@ -494,15 +497,21 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             tc::tma_prefetch_2d(&a.tm_qkv, static_cast<int>(HK) + x2 + 64 * hf, y2);
         }
     }
-    if (warp == 0) tc::tmem_alloc<256>(sbase + SM_TMEMP);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEMP);
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    uint32_t phase = 0;
+    };
+    uint32_t tmem = 0, tlane = 0;
+    auto alloc_tmem = [&]() {
+        if (warp == 0) tc::tmem_alloc<256>(sbase + SM_TMEMP);
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEMP);
+        tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    };
+    uint32_t phase = 0;   // parity of the MMA barrier (kept across the units of a CTA)
     bool ok = true;
-    {
+    // ---- one unit, from its tensor copies (issued) to its record; lpar: the parity of the
+    // copies' barriers for this unit ----
+    auto compute = [&](const int bid, const int h, const int64_t row0, const int n, const uint32_t lpar) {
     // this unit's beta (consumed after the first gate pass, so its latency is hidden)
     const uint16_t braw = (tid < C && tid < n) ? p.rb[(row0 + tid) * p.ld_beta + h] : static_cast<uint16_t>(0);
     unsigned char *rec = a.rec + static_cast<size_t>(bid) * REC_BYTES;
@@ -511,7 +520,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     const float expA_l2e = expA * kLog2e, lb_l2e = p.lb * kLog2e;
     uint4 xr[2][4];   // own row of q or k: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31
     float rn = 0.f, rk = 0.f;   // norm factors of the own row and of the key row r
-    ok &= cta_wait(lbar, 0, smem + SM_WAITOK);   // raw_g has landed
+    ok &= cta_wait(lbar, lpar, smem + SM_WAITOK);   // raw_g has landed
 
     // ---- gate pass over one channel half: per (row, channel) e1 = e^{b - P_s} (the decay
     // since the block's reference) into SM_BH, or on the pairwise path the in-block log2
@@ -576,7 +585,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 const int rr = 8 * o8 + j;
-                const float2 val = flagged ? v[j] : make_float2(ex2(v[j].x), ex2(v[j].y));
+                const float2 val = (PW && flagged) ? v[j] : make_float2(ex2(v[j].x), ex2(v[j].y));
                 *reinterpret_cast<float2 *>(bh + (j * 256 + ((q4 ^ (rr & 7)) << 4)) / 4 + e4) = val;
             }
         }
@@ -601,9 +610,10 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         __syncthreads();
         return flagged;
     };
-    const bool pw0 = gate_half(0);
+    // fl: the half needs the pairwise path; pw: it takes it here
+    const bool fl0 = gate_half(0), pw0 = PW && fl0;
     if (tid < C) betas[tid] = tid < n ? sigmoid_f(bf16_to_f32(braw)) : 0.f;   // read in the assembly
-    ok &= cta_wait(lbar + 8, 0, smem + SM_WAITOK);   // q and k have landed
+    ok &= cta_wait(lbar + 8, lpar, smem + SM_WAITOK);   // q and k have landed
     {   // own row from the staged tile (zero past the chunk) and its half-row sums of squares
         const uint32_t stg = sbase + (kside ? SM_KSTG : SM_QSTG);
         float2 ss = make_float2(0.f, 0.f);
@@ -804,9 +814,10 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     issue_gram(pw0, false, false);
     if (pw0) pairwise_half();
     // ================= channel half 1 =================
-    bool pw1 = false;
+    bool fl1 = false, pw1 = false;
     if (nhalf == 2) {
-        pw1 = gate_half(1);
+        fl1 = gate_half(1);
+        pw1 = PW && fl1;
         // the half-0 products read the A operand and SM_BOFF / SM_BDIAG, which half 1 rewrites
         ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
         phase ^= 1;
@@ -1003,8 +1014,11 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         ok &= cta_wait(mbar, phase, smem + SM_WAITOK);
         phase ^= 1;
     }
-    // ================= [M1; M2] -> the record =================
-    if (ok) {
+    // ================= [M1; M2] -> the record (left to the pass over marked units if the
+    // pairwise path was needed and not taken) =================
+    const bool marked = !PW && (fl0 || fl1);
+    if (!PW && tid == 0) a.flags[a.flag0 + bid] = marked ? 1 : 0;
+    if (ok && !marked) {
         float v[2][16];
         tc::tmem_ld16(tlane + TM_W2 + 32 * sub, v[0]);
         tc::tmem_ld16(tlane + TM_W2 + 32 * sub + 16, v[1]);
@@ -1025,15 +1039,106 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             for (int q = 0; q < 4; q++)
                 *reinterpret_cast<uint4 *>(mm + tc::core_offset(l, 32 * sub + 8 * q, 64, 2)) = pack8_f16(&v[q >> 1][8 * (q & 1)]);
         }
-    } else if (tid == 0 && p.err) {
+    } else if (!ok && tid == 0 && p.err) {
         atomicOr(p.err, kErrTimeout);
     }
+    if (PW) tc::fence_proxy_async();   // the next unit's tensor copies overwrite these regions
     tc::fence_before_sync();
     __syncthreads();
+    };
+
+    // ---- (PW) the next marked unit at or after unit pos whose rank among the marked units
+    // (rk: the rank of the first marked unit at or after pos) is congruent to this CTA's
+    // index modulo the grid, or -1; pos and rk move past it. Every CTA counts ranks over
+    // the same flags, so each marked unit goes to exactly one CTA. A window is 16 flags
+    // (one 16-byte load) per thread. ----
+    auto next_marked = [&](int &pos, int &rk) -> int {
+        int *sc = reinterpret_cast<int *>(smem + SM_TOT);   // [8] per-warp counts, [8] the unit found
+        const int G = static_cast<int>(gridDim.x), me = static_cast<int>(blockIdx.x);
+        while (pos < total) {
+            const int g0 = (a.flag0 + pos) & ~15;    // flag index of the window's start
+            const int gi = g0 + 16 * tid;            // this thread's 16 flags
+            uint32_t bits = 0;                       // bit j: flag gi + j is set, within [pos, total)
+            if (gi - a.flag0 < total) {
+                const uint4 f = __ldcg(reinterpret_cast<const uint4 *>(a.flags + gi));   // from L2
+                const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int u = gi + j - a.flag0;
+                    if (((w4[j >> 2] >> (8 * (j & 3))) & 0xffu) != 0u && u >= pos && u < total) bits |= 1u << j;
+                }
+            }
+            const int cnt = __popc(bits);
+            int incl = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (lane == 31) sc[warp] = incl;
+            __syncthreads();
+            int before = 0, all = 0;
+#pragma unroll
+            for (int w = 0; w < PT / 32; w++) {
+                const int c = sc[w];
+                before += w < warp ? c : 0;
+                all += c;
+            }
+            const int want = rk + ((me - rk) % G + G) % G;   // the first rank >= rk that is this CTA's
+            const bool found = want < rk + all;
+            if (found) {
+                const int k = want - rk - (before + incl - cnt);   // among this thread's marked flags
+                if (k >= 0 && k < cnt) {
+                    uint32_t b = bits;
+                    for (int i = 0; i < k; i++) b &= b - 1u;
+                    sc[8] = gi + __ffs(static_cast<int>(b)) - 1 - a.flag0;
+                }
+            }
+            __syncthreads();
+            if (found) {
+                const int u = sc[8];
+                pos = u + 1;
+                rk = want + 1;
+                return u;
+            }
+            pos = g0 + 16 * PT - a.flag0;
+            rk += all;
+            __syncthreads();   // the counts are rewritten by the next window
+        }
+        return -1;
+    };
+
+    uint32_t lpar = 0;   // parity of the copy barriers for the current unit
+    if (!PW) {
+        const int bid = static_cast<int>(blockIdx.x);
+        int h, n, sq = -1;
+        int64_t row0;
+        locate(bid, h, row0, n, sq);
+        // launched by launch_pdl: the barriers, the unit's location and the tensor-map
+        // prefetches above read kernel parameters only; every global read comes after this
+        pdl_wait_then_release();
+        issue_loads(bid, h, row0, sq);
+        alloc_tmem();
+        compute(bid, h, row0, n, 0u);
+    } else {
+        pdl_wait_then_release();   // the first pass's flags are complete
+        alloc_tmem();
+        int pos = 0, rk = 0;
+        for (;;) {
+            const int u = next_marked(pos, rk);
+            if (u < 0) break;
+            int h, n, sq = -1;
+            int64_t row0;
+            locate(u, h, row0, n, sq);
+            issue_loads(u, h, row0, sq);
+            compute(u, h, row0, n, lpar);
+            if (!ok) break;
+            lpar ^= 1u;
+        }
     }
     if (!ok && tid == 0) {   // a wait gave up: give the copies and the product it waited for (bounded) time to end
-        (void)tc::mbar_wait(lbar, 0);
-        (void)tc::mbar_wait(lbar + 8, 0);
+        (void)tc::mbar_wait(lbar, lpar);
+        (void)tc::mbar_wait(lbar + 8, lpar);
         (void)tc::mbar_wait(mbar, phase ^ 1u);
     }
     tc::fence_before_sync();
@@ -1391,10 +1496,13 @@ static int64_t total_chunks(const int32_t *cu_host, int64_t num_seqs)
 // tiles; at 64 the channels or columns past the data are held at zero).
 static bool chunk_dims(int K, int V) { return (K == 64 || K == 128) && (V == 64 || V == 128); }
 
+// The records, then one flag byte per record (rounded up to 16 bytes).
 size_t chunk_workspace_bytes(const int32_t *cu_host, int64_t num_seqs, int H, int K, int V, int)
 {
     if (!chunk_dims(K, V) || num_seqs <= 0) return 0;
-    return static_cast<size_t>(total_chunks(cu_host, num_seqs)) * H * chunk::REC_BYTES;
+    const size_t units = static_cast<size_t>(total_chunks(cu_host, num_seqs)) * H;
+    if (units == 0) return 0;
+    return units * chunk::REC_BYTES + (units + 15) / 16 * 16;
 }
 
 // cuTensorMapEncodeTiled, fetched once through the runtime (no link against the driver library)
@@ -1441,10 +1549,13 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
     static_assert(sizeof(Args) < 32000, "kernel parameter space");
     cudaError_t err;
     // the instances for this K and V (64: one half of the 128-wide tile holds data, 128: two)
-    void (*prep)(Args) = K == 64 ? prep_kernel<1> : prep_kernel<2>;
+    void (*prep)(Args) = K == 64 ? prep_kernel<1, false> : prep_kernel<2, false>;
+    void (*prep_pw)(Args) = K == 64 ? prep_kernel<1, true> : prep_kernel<2, true>;
     void (*chain)(Args) = K == 64 ? (V == 64 ? chain_kernel<1, 1> : chain_kernel<1, 2>)
                                   : (V == 64 ? chain_kernel<2, 1> : chain_kernel<2, 2>);
     if ((err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(PREP_SMEM))) != cudaSuccess) return err;
+    if ((err = cudaFuncSetAttribute(prep_pw, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(PREP_SMEM))) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(CHAIN_SMEM))) != cudaSuccess) return err;
@@ -1452,6 +1563,8 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     unsigned char *recs = static_cast<unsigned char *>(workspace);
+    // the unit flags follow every record of the call
+    unsigned char *flags = recs + static_cast<size_t>(total_chunks(cu_host + entry_base, num_seqs)) * p.H * REC_BYTES;
     int64_t ch_done = 0;   // chunks (not chunk-heads) of the sequences already launched
     std::vector<int32_t> ord;
     // tensor maps over the rows of this call (every row any of its chunks reads lies below
@@ -1472,6 +1585,8 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
         a.num_seqs = static_cast<int32_t>(ns);
         a.pf_stride = 2 * sms;
         a.rec = recs + static_cast<size_t>(ch_done) * p.H * REC_BYTES;
+        a.flags = flags;
+        a.flag0 = static_cast<int32_t>(ch_done * p.H);
         const int32_t *cuh = cu_host + entry_base + s0;
         a.cb[0] = 0;
         for (int64_t i = 0; i < ns; i++)
@@ -1485,10 +1600,17 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
         for (int64_t i = 0; i < ns; i++) a.order[i] = ord[static_cast<size_t>(i)];
         const int64_t nch = a.cb[ns];
         if (nch > 0) {
-            if ((err = launch_pdl(prep, dim3(static_cast<unsigned>(nch * p.H)), dim3(PT), PREP_SMEM, stream, a)) !=
+            const int64_t units = nch * p.H;
+            if ((err = launch_pdl(prep, dim3(static_cast<unsigned>(units)), dim3(PT), PREP_SMEM, stream, a)) !=
                 cudaSuccess) return err;
+            if (after_prep && s0 == 0 && (err = cudaEventRecord(after_prep, stream)) != cudaSuccess) return err;
+            // the units marked by the first pass (none, usually: its CTAs find that and end)
+            const int64_t g = std::min<int64_t>(units, 2 * static_cast<int64_t>(sms));
+            if ((err = launch_pdl(prep_pw, dim3(static_cast<unsigned>(g)), dim3(PT), PREP_SMEM, stream, a)) !=
+                cudaSuccess) return err;
+        } else if (after_prep && s0 == 0 && (err = cudaEventRecord(after_prep, stream)) != cudaSuccess) {
+            return err;
         }
-        if (after_prep && s0 == 0 && (err = cudaEventRecord(after_prep, stream)) != cudaSuccess) return err;
         // every sequence gets a chain CTA: empty ones check their slot and return
         if ((err = launch_pdl(chain, dim3(static_cast<unsigned>(ns * p.H)), dim3(CT), CHAIN_SMEM, stream, a)) !=
             cudaSuccess) return err;

@@ -21,9 +21,9 @@
 
 static_assert(KDA_NO_ALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
 
-// The prefill's intra-chunk records (one per (chunk of 64 rows, head)). The first kernel
-// of a call writes every byte of each record the second kernel reads, so nothing in the
-// array has to start at zero, and what a previous call left there is never read.
+// The prefill's intra-chunk records (one per (chunk of 64 rows, head)) and their flags.
+// A call's kernels write every record byte and flag before they read it, so nothing in
+// the array has to start at zero, and what a previous call left there is never read.
 static __device__ __align__(256) unsigned char g_prefill_scratch[KDA_NO_ALLOC_SCRATCH_BYTES];
 
 namespace {

@@ -144,7 +144,8 @@ def test_workspace_query_is_host_only(kda):
     hd = _heads(kda)
     n = kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,
                                                   ctypes.byref(hd), 64)
-    assert n == (2 + 4 + 1) * 2 * 57856   # one record per (chunk of 64 rows, head)
+    # one record per (chunk of 64 rows, head), then one flag byte per record rounded up to 16
+    assert n == (2 + 4 + 1) * 2 * 57856 + 16
     for K, V in ((64, 64), (64, 128), (128, 64)):
         hk = _heads(kda, K=K, V=V)
         assert kda.lib.kda_chunk_prefill_workspace_bytes(cu.ctypes.data_as(ctypes.c_void_p), 3,

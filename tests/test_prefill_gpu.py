@@ -165,6 +165,27 @@ def test_prefill_strong_decay(kda, A_log):
     _run(kda, w, f"strong decay A_log={A_log}")
 
 
+def test_prefill_marked_units_over_the_grid(kda):
+    """Units whose channel halves need the pairwise path are marked by the first pass and
+    redone by a grid of a few CTAs per SM, each taking every G-th marked unit. Here 520
+    (chunk, head) units, 5 heads of 8 marked throughout: more marked units than that grid
+    has CTAs, so CTAs run several in turn, interleaved with unmarked units."""
+    w = wl.varlen_case([3000, 1100, 64, 1], 8, 128, 128, seed=78)
+    w.A_log = np.array([4.0, -1.0, 4.0, 0.5, 4.0, 4.0, -2.0, 3.0], dtype=np.float32)
+    _run(kda, w, "marked units over the grid")
+
+
+def test_prefill_more_than_1024_sequences(kda):
+    """More sequences than one launch takes (1024): the call splits into two launches
+    whose records and unit flags sit at their offsets in one workspace; one head is
+    marked everywhere, so both launches redo units."""
+    rng = np.random.default_rng(5)
+    lengths = [int(x) for x in rng.integers(0, 131, size=1100)]
+    w = wl.varlen_case(lengths, 2, 128, 128, seed=77)
+    w.A_log = np.array([4.0, -1.0], dtype=np.float32)
+    _run(kda, w, "1100 sequences")
+
+
 def test_prefill_weak_decay_long(kda):
     """Near-unit decay (A_log = -6) over 2000 rows: the state carries information across
     many chunks, so errors in the chain would accumulate."""

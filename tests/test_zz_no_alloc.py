@@ -31,6 +31,7 @@ def test_no_alloc_rejects_oversize_on_the_host(kda):
     fake = ctypes.c_void_p(1 << 20)
     H = 32
     chunks = kda.KDA_NO_ALLOC_SCRATCH_BYTES // (57856 * H) + 1   # one chunk too many at H = 32
+    need = chunks * H * 57856 + (chunks * H + 15) // 16 * 16    # records, then their flags
     cu = np.array([0, 64 * chunks], np.int32)
     hd = kda.KdaHeads(H=H, K=128, V=128, A_log=fake.value, dt_bias=None, has_lower_bound=0,
                       lower_bound=0.0, scale=0.1, l2_eps=1e-6)
@@ -43,7 +44,7 @@ def test_no_alloc_rejects_oversize_on_the_host(kda):
     assert s == kda.KDA_ERR_WORKSPACE
     msg = kda.last_error()
     assert "kda_chunk_prefill_no_alloc" in msg and str(kda.KDA_NO_ALLOC_SCRATCH_BYTES) in msg
-    assert str(chunks * H * 57856) in msg
+    assert str(need) in msg
 
 
 def _rel_l2(a, b):
