@@ -421,8 +421,10 @@ __device__ __forceinline__ float gate_log2(float x, float expA, float expA_l2e, 
 // path. A grid of a few CTAs per SM runs it; each CTA takes the marked units whose rank
 // among them is congruent to its index. Keeping the pairwise code out of the first
 // instance keeps that instance's code small and its registers for the common path.
+// LB: the gate form with a lower bound (the first pass only; the second reads it from the
+// parameters).
 // ---------------------------------------------------------------------------
-template <int NH, bool PW>   // NH: channel halves that hold data (K = 64 NH)
+template <int NH, bool PW, bool LB>   // NH: channel halves that hold data (K = 64 NH)
 __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Args a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             const uint32_t w = *reinterpret_cast<const uint32_t *>(gt + j * 128 + (((ch & 7) ^ j) << 4));
             v[j] = fadd2(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)), dtb);
         }
-        if (p.has_lb) {
+        if (PW ? p.has_lb != 0 : LB) {
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 const float2 t = fmul2(v[j], make_float2(-expA_l2e, -expA_l2e));
@@ -1549,8 +1551,9 @@ static cudaError_t launch_chunk_path(const Params &p, int K, int V, const int32_
     static_assert(sizeof(Args) < 32000, "kernel parameter space");
     cudaError_t err;
     // the instances for this K and V (64: one half of the 128-wide tile holds data, 128: two)
-    void (*prep)(Args) = K == 64 ? prep_kernel<1, false> : prep_kernel<2, false>;
-    void (*prep_pw)(Args) = K == 64 ? prep_kernel<1, true> : prep_kernel<2, true>;
+    void (*prep)(Args) = K == 64 ? (p.has_lb ? prep_kernel<1, false, true> : prep_kernel<1, false, false>)
+                                 : (p.has_lb ? prep_kernel<2, false, true> : prep_kernel<2, false, false>);
+    void (*prep_pw)(Args) = K == 64 ? prep_kernel<1, true, false> : prep_kernel<2, true, false>;
     void (*chain)(Args) = K == 64 ? (V == 64 ? chain_kernel<1, 1> : chain_kernel<1, 2>)
                                   : (V == 64 ? chain_kernel<2, 1> : chain_kernel<2, 2>);
     if ((err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
