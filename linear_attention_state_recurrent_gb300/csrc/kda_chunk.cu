@@ -36,7 +36,9 @@
 //   A_op = [K^e; Q^e],  K^e_r = k^_r e^{b_r - P_s(r)} (<= 1)      (tf32, in tensor memory)
 // Diagonal blocks:      X_diag = A_op (K^R)^T,  K^R_i = k^_i e^{P_s(i) - b_i}   (>= 1)
 // Off-diagonal blocks:  X_off  = A_op [B_1; B_2; B_3]^T,  B_R = rows i < 16R at
-//                       k^_i e^{P_R - b_i} (<= 1), for the rows of block R.
+//                       k^_i e^{P_R - b_i} (<= 1), for the rows of block R; both operands
+//                       in fp16 (every factor is at most 1 in magnitude: half the tf32
+//                       tensor time; parts below 2^-24 of the largest are lost).
 // K^R reaches e^{(decay over the block)}, which tf32 (fp32 range) holds while a block's
 // decay stays below 80 nats; a channel half in which some channel decays more within a
 // block computes its share of the diagonal blocks pairwise in fp32 instead.
@@ -90,7 +92,7 @@ constexpr uint32_t SBO_SB = SBO64_F16 + 16;
 // ---- prep shared memory (bytes) ----
 constexpr uint32_t SM_G = 0;            // bf16 [2][64][64] raw_g as two TMA boxes (128B swizzle, see tma_off)
 constexpr uint32_t SM_BH = 16384;       // fp32 [64][64]  b (log2 units) of the current channel half, swizzled
-constexpr uint32_t SM_BOFF = 32768;     // tf32 [96][64]  [B_1; B_2; B_3] of the current half (SBO 2048)
+constexpr uint32_t SM_BOFF = 32768;     // fp16 [96][64]  [B_1; B_2; B_3] of the current half (SBO 1024)
 constexpr uint32_t SM_BDIAG = 57344;    // tf32 [64][64]  K^R of the current half (SBO 2048); on the
                                         // pairwise path: fp16 [64][64] k^ then q^ (swizzled)
 constexpr uint32_t SM_SB = 73728;       // fp16 [192][64] Aqk rows 0..63, Kd^T rows 64..191 (SBO 1040)
@@ -122,6 +124,7 @@ static_assert(SM_XD + 8192 <= SM_SB, "solve scratch overlaps SB");
 constexpr uint32_t TM_XOFF = 0;     // X_off   96 columns
 constexpr uint32_t TM_XDIAG = 96;   // X_diag  64 columns
 constexpr uint32_t TM_A = 160;      // tf32 A operand [K^e; Q^e] of the current channel half (64 columns)
+constexpr uint32_t TM_A16 = 224;    // the same in fp16 pairs, the A operand of X_off (32 columns)
 constexpr uint32_t TM_W1 = 0;       // [Aqk; Kd^T rows 0..63] T diag(beta)   (after assembly)
 constexpr uint32_t TM_W2 = 64;      // Kd^T T diag(beta)
 constexpr uint32_t TM_L3X = 160;    // the solve's last level: X^T (32 columns)
@@ -693,6 +696,9 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
 #pragma unroll
                 for (int o = 0; o < 8; o++) d8[o] = tf32_rna(xe[o]);
                 tc::tmem_st8u(tlane + TM_A + cl, d8);
+                const uint4 h4 = pack8_f16(xe);
+                const uint32_t d4[4] = {h4.x, h4.y, h4.z, h4.w};
+                tc::tmem_st4u(tlane + TM_A16 + cl / 2, d4);
             }
             if (pw)      // the stash of the pairwise path: k^ / q^ in fp16
                 st_shared_u4(sbase + SM_BDIAG + side * 8192 + stash_off(r, cl), pack8_f16(x));
@@ -724,24 +730,16 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
                     for (int o = 0; o < 8; o++) kf[o] = kk[o] * ex2(t[o] - lp[o]);
                 }
                 // B_R rows (R = s + 1 .. 3): k e^{P_R - b} -> SM_BOFF row off_b_base(R) + r
-                if (s < 3) {
-                    const uint32_t a1 = boff + tc::core_offset(off_b_base(s + 1) + r, cl, 64, 4);
-                    st_shared_u4(a1, pack4_tf32(kf));
-                    st_shared_u4(a1 + 128, pack4_tf32(kf + 4));
-                }
+                if (s < 3) st_shared_u4(boff + tc::core_offset(off_b_base(s + 1) + r, cl, 64, 2), pack8_f16(kf));
                 if (s < 2) {
                     ld8(tbu + kD2 * 256, t);
                     mul8(v8, kf, t);
-                    const uint32_t a2 = boff + tc::core_offset(off_b_base(s + 2) + r, cl, 64, 4);
-                    st_shared_u4(a2, pack4_tf32(v8));
-                    st_shared_u4(a2 + 128, pack4_tf32(v8 + 4));
+                    st_shared_u4(boff + tc::core_offset(off_b_base(s + 2) + r, cl, 64, 2), pack8_f16(v8));
                 }
                 if (s < 1) {
                     ld8(tbu + kD3 * 256, t);
                     mul8(v8, kf, t);
-                    const uint32_t a3 = boff + tc::core_offset(48 + r, cl, 64, 4);
-                    st_shared_u4(a3, pack4_tf32(v8));
-                    st_shared_u4(a3 + 128, pack4_tf32(v8 + 4));
+                    st_shared_u4(boff + tc::core_offset(48 + r, cl, 64, 2), pack8_f16(v8));
                 }
                 // Kd^T = (k F e^{b_last - P_{s+1}})^T -> SB rows 64 + c
                 ld8(tbu + kD4 * 256, t);
@@ -800,7 +798,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         if (tid == 0 || tid == 32) {
             tc::fence_after_sync();
             if (tid == 0)
-                tc::gemm_ta_tf32<96, 64>(tmem + TM_XOFF, tmem + TM_A, sbase + SM_BOFF, SBO64_TF32, acc_off);
+                tc::gemm_ta<96, 64>(tmem + TM_XOFF, tmem + TM_A16, sbase + SM_BOFF, SBO64_F16, acc_off);
             else if (!pw)
                 tc::gemm_ta_tf32<64, 64>(tmem + TM_XDIAG, tmem + TM_A, sbase + SM_BDIAG, SBO64_TF32, acc_diag);
             tc::commit(mbar);
