@@ -71,6 +71,15 @@ def test_prefill_chunked_64_strong_decay(kda):
     _run(kda, w, "prefill K=V=64 strong decay")
 
 
+def test_mixed_batch_marked_units(kda):
+    """A mixed batch whose prefill heads need the pairwise diagonal path: the prep kernel's
+    pass over marked units runs while the decodes wait on the side stream."""
+    w = wl.varlen_case([1] * 5 + [300, 129, 64], 4, 128, 128, seed=97, index_stride=2,
+                       num_decodes=5, kind="mixed")
+    w.A_log = np.array([4.0, -1.0, 3.5, 0.0], dtype=np.float32)
+    _run(kda, w, "mixed marked units")
+
+
 def test_mixed_batch_64_wide(kda):
     w = wl.varlen_case([1] * 6 + [77, 200], 4, 64, 64, seed=95, lower_bound=-5.0, index_stride=2,
                        num_decodes=6, kind="mixed")

@@ -1,9 +1,10 @@
 """kda_chunk_prefill_no_alloc: the chunked prefill with its records in the library's fixed
 device scratch instead of a caller workspace, for callers that cannot allocate device
-memory. Checked through the C ABI against kda_chunk_prefill on two calls in a row (the
-second with other lengths and head counts, so that records the first call left in the
-shared array would show if they were read), and its size limit, which it enforces on the
-host before any CUDA call.
+memory. Checked through the C ABI against kda_chunk_prefill on calls in a row (the second
+with other lengths and head counts, so that records the first call left in the shared
+array would show if they were read; the third with heads whose units take the pairwise
+path, so that their flags sit in the array too), and its size limit, which it enforces on
+the host before any CUDA call.
 
 The file name makes pytest collect it last: its first GPU call does the per-device set-up
 of the scratch address, and it must pass both alone in a fresh process and after the
@@ -53,13 +54,15 @@ def _rel_l2(a, b):
 
 
 @pytest.mark.gpu
-def test_no_alloc_matches_chunk_prefill_on_two_calls(kda):
+def test_no_alloc_matches_chunk_prefill_on_calls_in_a_row(kda):
     from tests import kda_harness as hx
     dev = "cuda:0"
     cases = [
         wl.varlen_case([200, 1, 130, 0, 64, 300], 4, 128, 128, seed=71, lower_bound=-5.0),
         wl.varlen_case([129, 65, 7], 2, 128, 128, seed=72, lower_bound=None, index_stride=4),
+        wl.varlen_case([333, 64, 1], 2, 64, 64, seed=73, lower_bound=None),
     ]
+    cases[2].A_log = np.array([4.0, 0.5], dtype=np.float32)   # marked units: their flags live in the scratch too
     for i, w in enumerate(cases):
         assert 0 < kda.kda_chunk_prefill_workspace_bytes(torch.from_numpy(w.cu_seqlens), w.H, w.K, w.V) \
             <= kda.KDA_NO_ALLOC_SCRATCH_BYTES
