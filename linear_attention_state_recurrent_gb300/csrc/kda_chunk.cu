@@ -961,18 +961,15 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         phase ^= 1;
     }
     if (ok) {
-        if (warp == 0) {   // X^T (lanes 0..31) rounded to tf32 in place: the next product's A operand
-            float x0[16], x1[16];
-            tc::tmem_ld16(tlane + TM_L3X, x0);
-            tc::tmem_ld16(tlane + TM_L3X + 16, x1);
+        if ((warp & 3) == 0) {   // X^T (lanes 0..31) rounded to tf32 in place: the next product's A
+            // operand; warps 0 and 4 (both reach lanes 0..31) take 16 columns each
+            const uint32_t col = TM_L3X + 16 * (warp >> 2);
+            float x0[16];
+            tc::tmem_ld16(tlane + col, x0);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; u++) {
-                x0[u] = __uint_as_float(tf32_rna(x0[u]));
-                x1[u] = __uint_as_float(tf32_rna(x1[u]));
-            }
-            tc::tmem_st16(tlane + TM_L3X, x0);
-            tc::tmem_st16(tlane + TM_L3X + 16, x1);
+            for (int u = 0; u < 16; u++) x0[u] = __uint_as_float(tf32_rna(x0[u]));
+            tc::tmem_st16(tlane + col, x0);
             tc::tmem_st_wait();
         }
         tc::fence_before_sync();
@@ -986,19 +983,18 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         phase ^= 1;
     }
     if (ok) {
-        if (warp == 0) {   // T_ba = -(X^T T_b^T)^T -> rows j of the (T diag(beta))^T tile, K = 32..63
-            float y0[16], y1[16];
-            tc::tmem_ld16(tlane + TM_L3T, y0);
-            tc::tmem_ld16(tlane + TM_L3T + 16, y1);
+        if ((warp & 3) == 0) {   // T_ba = -(X^T T_b^T)^T -> rows j of the (T diag(beta))^T tile,
+            // K = 32..63; warps 0 and 4 take 16 columns each
+            const int hv = warp >> 2;
+            float y0[16];
+            tc::tmem_ld16(tlane + TM_L3T + 16 * hv, y0);
             tc::tmem_ld_wait();
             const float nb = -betas[lane];
 #pragma unroll
-            for (int u = 0; u < 16; u++) { y0[u] *= nb; y1[u] *= nb; }
+            for (int u = 0; u < 16; u++) y0[u] *= nb;
             const uint32_t tt = sbase + SM_TT;
-            st_shared_u4(tt + tc::core_offset(lane, 32, 64, 2), pack8_f16(y0));
-            st_shared_u4(tt + tc::core_offset(lane, 40, 64, 2), pack8_f16(y0 + 8));
-            st_shared_u4(tt + tc::core_offset(lane, 48, 64, 2), pack8_f16(y1));
-            st_shared_u4(tt + tc::core_offset(lane, 56, 64, 2), pack8_f16(y1 + 8));
+            st_shared_u4(tt + tc::core_offset(lane, 32 + 16 * hv, 64, 2), pack8_f16(y0));
+            st_shared_u4(tt + tc::core_offset(lane, 40 + 16 * hv, 64, 2), pack8_f16(y0 + 8));
         }
         tc::fence_proxy_async();   // the transpose is read by the products issued after the barrier
         tc::fence_before_sync();
@@ -1019,9 +1015,13 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     const bool marked = !PW && (fl0 || fl1);
     if (!PW && tid == 0) a.flags[a.flag0 + bid] = marked ? 1 : 0;
     if (ok && !marked) {
-        float v[2][16];
+        float v[2][16], w1[2][16];
         tc::tmem_ld16(tlane + TM_W2 + 32 * sub, v[0]);
         tc::tmem_ld16(tlane + TM_W2 + 32 * sub + 16, v[1]);
+        if (kside) {   // lanes 0..63 of the first product: M1 rows (loaded with the M2 rows)
+            tc::tmem_ld16(tlane + TM_W1 + 32 * sub, w1[0]);
+            tc::tmem_ld16(tlane + TM_W1 + 32 * sub + 16, w1[1]);
+        }
         tc::tmem_ld_wait();
         unsigned char *mm = rec + REC_MM;
         bool bad = false;   // [M1; M2] travel in fp16
@@ -1031,13 +1031,10 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
 #pragma unroll
         for (int q = 0; q < 4; q++)
             *reinterpret_cast<uint4 *>(mm + tc::core_offset(64 + l, 32 * sub + 8 * q, 64, 2)) = pack8_f16(&v[q >> 1][8 * (q & 1)]);
-        if (kside) {   // lanes 0..63 of the first product: M1 rows
-            tc::tmem_ld16(tlane + TM_W1 + 32 * sub, v[0]);
-            tc::tmem_ld16(tlane + TM_W1 + 32 * sub + 16, v[1]);
-            tc::tmem_ld_wait();
+        if (kside) {
 #pragma unroll
             for (int q = 0; q < 4; q++)
-                *reinterpret_cast<uint4 *>(mm + tc::core_offset(l, 32 * sub + 8 * q, 64, 2)) = pack8_f16(&v[q >> 1][8 * (q & 1)]);
+                *reinterpret_cast<uint4 *>(mm + tc::core_offset(l, 32 * sub + 8 * q, 64, 2)) = pack8_f16(&w1[q >> 1][8 * (q & 1)]);
         }
     } else if (!ok && tid == 0 && p.err) {
         atomicOr(p.err, kErrTimeout);
