@@ -636,6 +636,13 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             }
         nrm[sub * 128 + l] = ss.x + ss.y;
     }
+    // the Q thread's key share of channel half 0 (key row r, channels 32 sub + 16 .. + 31), from
+    // the staged k before operand generation overwrites it
+    uint4 kq0[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    if (!kside && r < n) {
+        kq0[0] = ld_shared_u4(sbase + SM_KSTG + tma_off(r, 4 * sub + 2));
+        kq0[1] = ld_shared_u4(sbase + SM_KSTG + tma_off(r, 4 * sub + 3));
+    }
     __syncthreads();   // the half-row norms; the staged q and k are consumed
     {   // rows past the chunk hold zeros; their norm factor is 0 so that eps = 0 gives no NaN
         auto norm_of = [&](int lane_idx, int row) -> float {
@@ -663,9 +670,10 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             dst[0] = lo4.x; dst[1] = lo4.y; dst[2] = lo4.z; dst[3] = lo4.w;
             dst[4] = hi4.x; dst[5] = hi4.y; dst[6] = hi4.z; dst[7] = hi4.w;
         };
-        // the Q thread's key share: key row r, channels 32 sub + 16 .. + 31 of the half
-        uint4 kq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-        if (!kside && r < n) {
+        // the Q thread's key share: key row r, channels 32 sub + 16 .. + 31 of the half (half 0
+        // from the staged tile, half 1 from L2)
+        uint4 kq[2] = {kq0[0], kq0[1]};
+        if (hf > 0 && !kside && r < n) {
             const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + HK + static_cast<int64_t>(h) * kr + 64 * hf + 32 * sub + 16;
             kq[0] = __ldg(reinterpret_cast<const uint4 *>(src));
             kq[1] = __ldg(reinterpret_cast<const uint4 *>(src + 8));
