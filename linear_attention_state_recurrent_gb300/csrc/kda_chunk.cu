@@ -1,4 +1,5 @@
-// Chunked varlen prefill on tcgen05 tensor cores (K = V = 128, chunk C = 64).
+// Chunked varlen prefill on tcgen05 tensor cores (K and V in {64, 128} on 128 x 128 tiles,
+// chunk C = 64).
 //
 // The chunked (WY) form of the gated delta rule (chunk_kda_with_fused_gate with its
 // recompute_w_u step, vLLM PR #50649, section Purpose). For one (sequence, head) and a
@@ -18,10 +19,12 @@
 // two kernels:
 //   prep_kernel   one CTA per (chunk, head), all of them in parallel (two CTAs per SM):
 //                 gate, norms, cumulative decay, the decay-weighted Gram matrices on the
-//                 tensor cores, the triangular solve and [Aqk; Kd^T] T diag(beta) on the
-//                 tensor cores. It writes one record per (chunk, head) to the workspace:
-//                 [K^G; Q^G] (fp16), gamma (fp32) and [M1; M2] (fp16), each already in the
-//                 shared-memory layout the chain's MMAs read.
+//                 tensor cores, the triangular solve (its last level on the tensor cores)
+//                 and [Aqk; Kd^T] T diag(beta) on the tensor cores. It writes one record
+//                 per (chunk, head) to the workspace: [K^G; Q^G] (fp16), gamma (fp32) and
+//                 [M1; M2] (fp16), each already in the shared-memory layout the chain's
+//                 MMAs read, and a flag per unit; a second launch redoes the flagged units
+//                 (a channel half decaying too fast within a block) with the pairwise path.
 //   chain_kernel  one CTA per (sequence, head) chain (one per SM): the state stays in
 //                 tensor memory, transposed (lane = value column j, column = key channel);
 //                 per chunk two products
