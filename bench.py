@@ -410,31 +410,36 @@ def main():
             stream.synchronize()
 
         # Pipelined steps, as a serving loop with asynchronous scheduling runs them: step i's
-        # input copy (on a copy stream, into one of two device buffers) overlaps step i-1's
-        # call; each step's output is copied to the host after its call on the compute stream,
-        # and the host waits for step i-1's output right after issuing step i. Every step's
-        # copies are inside the timed region.
+        # input copy (a copy stream, into one of two device buffers) overlaps step i-1's call;
+        # its output is copied to the host on a third stream once its call is done (so the
+        # next call follows this one directly), and the host waits for step i-1's output
+        # right after issuing step i. Every step's copies are inside the timed region.
         d_in = [d_all, torch.empty(tot, dtype=torch.uint8, device=dev)]
         d_views = [[seg(d, k) for k in range(4)] for d in d_in]
         d_out = [out, torch.empty_like(out)]
         h_outs = [h_out, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
-        copy_stream = torch.cuda.Stream()
+        in_stream, out_stream = torch.cuda.Stream(), torch.cuda.Stream()
         ev_in = [torch.cuda.Event() for _ in range(2)]     # step's input copy done
-        ev_done = [torch.cuda.Event() for _ in range(2)]   # step's call and output copy done
+        ev_call = [torch.cuda.Event() for _ in range(2)]   # step's call done
+        ev_done = [torch.cuda.Event() for _ in range(2)]   # step's output copy done (buffers b free)
 
         def e2e_pipelined_step(i):
             b = i & 1
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(ev_done[b])   # step i-2 has finished with buffer b
+            with torch.cuda.stream(in_stream):
+                in_stream.wait_event(ev_done[b])   # step i-2 has finished with buffers b
                 d_in[b].copy_(h_all[i & 3], non_blocking=True)
-                ev_in[b].record(copy_stream)
+                ev_in[b].record(in_stream)
             stream.wait_event(ev_in[b])
+            stream.wait_event(ev_done[b])
             vq, vg, vb, vi = d_views[b]
             o, _ = kda.kda_packed_decode(vq, vg, vb, dw.A_log, dw.dt_bias, w.lower_bound,
                                          dw.pool_view(), vi, scale=w.scale, l2_eps=w.eps,
                                          out=d_out[b])
-            h_outs[b].copy_(o, non_blocking=True)
-            ev_done[b].record(stream)
+            ev_call[b].record(stream)
+            with torch.cuda.stream(out_stream):
+                out_stream.wait_event(ev_call[b])
+                h_outs[b].copy_(o, non_blocking=True)
+                ev_done[b].record(out_stream)
             if i > 0:
                 ev_done[b ^ 1].synchronize()   # the host takes step i-1's result
 
@@ -455,8 +460,8 @@ def main():
                "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
                "api": "kda.kda_packed_decode, pipelined: step i's pinned host -> device input copy "
                       "(copy stream, two device buffers) overlaps step i-1's call; each step's output "
-                      "is copied device -> host after its call and the host waits for step i-1's "
-                      "output after issuing step i",
+                      "is copied device -> host on a third stream after its call, and the host waits "
+                      "for step i-1's output after issuing step i",
                "one_step_at_a_time": {"value": total_bytes * e2e_steps / dt_sync / 1e9, "unit": "GB/s",
                                       "ms_per_step": dt_sync / e2e_steps * 1e3,
                                       "api": "copy in, call, copy out, stream sync, each step"}}
