@@ -111,7 +111,8 @@ constexpr uint32_t SM_MBAR = SM_BETA + 256;        // mbarrier of the MMAs (two 
 constexpr uint32_t SM_LBAR = SM_MBAR + 8;          // mbarriers of the tensor copies: raw_g, then q and k
 constexpr uint32_t SM_TMEMP = SM_LBAR + 16;
 constexpr uint32_t SM_WAITOK = SM_TMEMP + 4;
-constexpr uint32_t PREP_SMEM = SM_WAITOK + 4;
+constexpr uint32_t SM_GFLAG = SM_WAITOK + 4;       // int: some channel of the gate pass's half decays too fast
+constexpr uint32_t PREP_SMEM = SM_GFLAG + 4;
 static_assert(SM_MBAR % 8 == 0, "mbarrier alignment");
 static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two prep CTAs per SM");
 // solve-phase aliases over SM_G .. SM_BDIAG (dead once the Gram products are done)
@@ -571,6 +572,8 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
 #pragma unroll
         for (int j = 1; j < 8; j++) v[j] = fadd2(v[j], v[j - 1]);
         *reinterpret_cast<float2 *>(tot + o8 * 64 + 2 * cp) = v[7];
+        if (!PW && tid == 0) *reinterpret_cast<int *>(smem + SM_GFLAG) = 0;   // read only after the pass's
+                                                                             // last barrier, set after its first
         // the second octet of a block starts from the first octet's sum; the block sum
         // decides the path (a block decaying beyond kBlockSpan2 nats)
         __syncthreads();
@@ -581,7 +584,11 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         const float2 blk2 = fadd2(oct[4], oct[5]), blk3 = fadd2(oct[6], oct[7]);
         const float2 acc = sg == 0 ? blk0 : (sg == 1 ? blk1 : (sg == 2 ? blk2 : blk3));
         const int fl = (-acc.x > kBlockSpan2 || -acc.y > kBlockSpan2) ? 1 : 0;
-        const bool flagged = __syncthreads_or(fl) != 0;
+        // with the pairwise path compiled in, the values stored below depend on the decision;
+        // otherwise it is only reported, read after the pass's last barrier
+        bool flagged = false;
+        if (PW) flagged = __syncthreads_or(fl) != 0;
+        else if (fl) atomicOr(reinterpret_cast<int *>(smem + SM_GFLAG), 1);
         if (o8 & 1) {
             const float2 first = sg == 0 ? oct[0] : (sg == 1 ? oct[2] : (sg == 2 ? oct[4] : oct[6]));
 #pragma unroll
@@ -616,6 +623,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             if (sg == 3) *reinterpret_cast<float2 *>(rec + REC_GAM + 4 * cg) = make_float2(ex2(P4.x), ex2(P4.y));
         }
         __syncthreads();
+        if (!PW) flagged = *reinterpret_cast<volatile int *>(smem + SM_GFLAG) != 0;
         return flagged;
     };
     // fl: the half needs the pairwise path; pw: it takes it here
@@ -646,6 +654,12 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
         kq0[0] = ld_shared_u4(sbase + SM_KSTG + tma_off(r, 4 * sub + 2));
         kq0[1] = ld_shared_u4(sbase + SM_KSTG + tma_off(r, 4 * sub + 3));
     }
+    // ... and of half 1: the key thread of row r leaves those channels of its own row in SB's
+    // Aqk rows (free until the row assembly) for the query thread
+    if (nhalf == 2 && kside) {
+        st_shared_u4(sbase + SM_SB + (r * 2 + sub) * 32, xr[1][2]);
+        st_shared_u4(sbase + SM_SB + (r * 2 + sub) * 32 + 16, xr[1][3]);
+    }
     __syncthreads();   // the half-row norms; the staged q and k are consumed
     {   // rows past the chunk hold zeros; their norm factor is 0 so that eps = 0 gives no NaN
         auto norm_of = [&](int lane_idx, int row) -> float {
@@ -674,12 +688,11 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
             dst[4] = hi4.x; dst[5] = hi4.y; dst[6] = hi4.z; dst[7] = hi4.w;
         };
         // the Q thread's key share: key row r, channels 32 sub + 16 .. + 31 of the half (half 0
-        // from the staged tile, half 1 from L2)
+        // from the staged tile, half 1 as the key thread left it)
         uint4 kq[2] = {kq0[0], kq0[1]};
-        if (hf > 0 && !kside && r < n) {
-            const uint16_t *src = p.qkv + (row0 + r) * p.ld_qkv + HK + static_cast<int64_t>(h) * kr + 64 * hf + 32 * sub + 16;
-            kq[0] = __ldg(reinterpret_cast<const uint4 *>(src));
-            kq[1] = __ldg(reinterpret_cast<const uint4 *>(src + 8));
+        if (hf > 0 && !kside) {
+            kq[0] = ld_shared_u4(sbase + SM_SB + (r * 2 + sub) * 32);
+            kq[1] = ld_shared_u4(sbase + SM_SB + (r * 2 + sub) * 32 + 16);
         }
 #pragma unroll
         for (int u = 0; u < 4; u++) {
