@@ -527,6 +527,17 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
 
     const float expA = __expf(__ldg(p.A_log + h));
     const float expA_l2e = expA * kLog2e, lb_l2e = p.lb * kLog2e;
+    // dt_bias of this thread's channel pair in the gate passes (channels 64 hf + 2 (tid & 31) ..),
+    // loaded before the passes so that its latency is hidden
+    float2 dtb_h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    if (p.dt_bias) {
+#pragma unroll
+        for (int hf = 0; hf < nhalf; hf++)
+        {   // two scalar loads: dt_bias is only 4-byte aligned
+            const float *d = p.dt_bias + h * kr + 64 * hf + 2 * (tid & 31);
+            dtb_h[hf] = make_float2(__ldg(d), __ldg(d + 1));
+        }
+    }
     uint4 xr[2][4];   // own row of q or k: [half][4 x 8 bf16] = channels 64 hf + 32 sub .. + 31
     float rn = 0.f, rk = 0.f;   // norm factors of the own row and of the key row r
     ok &= cta_wait(lbar, lpar, smem + SM_WAITOK);   // raw_g has landed
@@ -540,8 +551,7 @@ __global__ void __launch_bounds__(PT, 2) prep_kernel(const __grid_constant__ Arg
     auto gate_half = [&](int hf) -> bool {
         const int cp = tid & 31, o8 = tid >> 5, sg = o8 >> 1;
         const int cg = 64 * hf + 2 * cp;                 // first channel of the pair (in the head)
-        const float2 dtb = p.dt_bias ? make_float2(__ldg(p.dt_bias + h * kr + cg), __ldg(p.dt_bias + h * kr + cg + 1))
-                                     : make_float2(0.f, 0.f);
+        const float2 dtb = hf ? dtb_h[1] : dtb_h[0];
         const int ch = cg >> 3;
         const unsigned char *gt = smem + SM_G + (ch >> 3) * 8192 + 8 * o8 * 128 + (cg & 7) * 2;
         const int nv = n - 8 * o8;               // rows of this octet inside the chunk
