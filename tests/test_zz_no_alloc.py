@@ -87,3 +87,29 @@ def test_no_alloc_matches_chunk_prefill_on_calls_in_a_row(kda):
         assert np.all(np.isfinite(pa)), label
         assert _rel_l2(pa, pb) <= hx.REL_L2, label
         assert int(got.err.item()) == int(ref.err.item()) == 0, label
+
+
+@pytest.mark.gpu
+def test_no_alloc_at_its_largest_size_equals_the_workspace_call(kda):
+    """The largest call the scratch holds at H = 32 (36 chunks x 32 heads = 1,152 of its
+    1,159 chunk-heads; the last sequences ragged): the same kernels as kda_chunk_prefill
+    with a caller workspace, so outputs, states and error word are bit-identical."""
+    from tests import kda_harness as hx
+    dev = "cuda:0"
+    w = wl.varlen_case([1000, 1024, 130, 5], 32, 128, 128, seed=74, lower_bound=-5.0)
+    assert wl.num_chunks([1000, 1024, 130, 5]) == 36
+    nb = kda.kda_chunk_prefill_workspace_bytes(torch.from_numpy(w.cu_seqlens), w.H, w.K, w.V)
+    assert nb <= kda.KDA_NO_ALLOC_SCRATCH_BYTES < nb + 57856 * w.H   # one more chunk would not fit
+    ref = hx.DeviceWorkload(w, dev)
+    got = hx.DeviceWorkload(w, dev)
+    out_ref = hx.run_gpu(ref, kda)
+    out = torch.empty(w.N, w.H * w.V, dtype=torch.bfloat16, device=dev)
+    kda.kda_chunk_prefill_no_alloc(got.mixed_qkv, got.raw_g, got.raw_beta, got.A_log,
+                                   got.dt_bias, w.lower_bound, got.pool_view(),
+                                   got.indices_view(), got.cu, torch.from_numpy(w.cu_seqlens),
+                                   out, scale=w.scale, l2_eps=w.eps, null_slot=w.null_slot,
+                                   err_flags=got.err)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_ref.view(torch.int16))
+    assert torch.equal(got.pool_flat, ref.pool_flat)
+    assert int(got.err.item()) == int(ref.err.item()) == 0
