@@ -203,6 +203,15 @@ def test_prefill_weak_decay_long(kda):
     _run(kda, w, "weak decay long")
 
 
+def test_prefill_one_long_sequence(kda):
+    """One sequence of 65,573 rows (1,025 chunks, the last of 37 rows): a chain sixteen
+    times longer than the bench's longest. Head 0 decays weakly (A_log = -6), so the state
+    carries every chunk's contribution to the end; head 1 decays at the workloads' rates."""
+    w = wl.varlen_case([65573], 2, 128, 128, seed=78)
+    w.A_log = np.array([-6.0, 0.3], dtype=np.float32)
+    _run(kda, w, "one long sequence")
+
+
 def test_prefill_repeat_bit_identical(kda):
     w = wl.varlen_case([300, 129, 64], 4, 128, 128, seed=23)
     dw = hx.DeviceWorkload(w)
