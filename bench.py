@@ -363,13 +363,13 @@ def main():
     value = total_bytes * args.steps / (ms_total * 1e-3) / 1e9
     achieved = state_bytes / (ms_step * 1e-3) / 1e9
     sha = source_sha("kda_recurrent.cu", "kda_common.cuh", "kda_pdl.cuh")
-    traffic = ncu_traffic("recurrent_kernel<128,128> serving_decode", sha)
+    traffic = ncu_traffic("decode_kernel<128,128> serving_decode", sha)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{pk['source']} HBM copy bandwidth (of {pk['source']})",
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
                 "algorithmic_bytes_per_launch": state_bytes,
-                "kernel": "kda::recurrent_kernel<128,128>"}
+                "kernel": "kda::decode_kernel<128,128>"}
 
     # ---- end to end through the public binding with host buffers ----
     e2e = None

@@ -298,8 +298,8 @@ int kda_chunk_prefill(const uint16_t *mixed_qkv, int64_t ld_qkv, const uint16_t 
  * length-1 sequences). Sequences 0..num_decodes-1 must have length 1 and take the
  * recurrent decode path; sequences num_decodes..num_decodes+num_prefills-1 take
  * the chunked prefill path. One cu_seqlens (device + host copies) and one strided
- * index view cover all of them, decodes first. The decodes run the packed-decode kernel
- * (recurrent_kernel, rows located through cu_seqlens); the prefills run kda_chunk_prefill's
+ * index view cover all of them, decodes first. The decodes run kda_packed_decode's kernel
+ * (decode d on row cu_seqlens_host[0] + d, every decode being one row); the prefills run kda_chunk_prefill's
  * kernels on `stream`. When both are present and K, V are in {64, 128}, the decodes run on
  * a low-priority stream of the library that starts once the prefill's first kernel is done
  * (so that they take the SMs the prefill chains leave free) and is joined back into

@@ -1708,12 +1708,12 @@ cudaError_t launch_mixed(const Params &p, int K, int V, const int32_t *cu, const
         if ((e = launch_chunk_path(p, K, V, cu, cu_host, num_decodes, num_prefills, workspace, stream,
                                    ss->after_prep)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->s, ss->after_prep, 0)) != cudaSuccess) return e;
-        if ((e = launch_recurrent(p, K, V, 2, 1, cu, 0, num_decodes, ss->s)) != cudaSuccess) return e;
+        if ((e = launch_decode(p, K, V, cu_host[0], num_decodes, ss->s)) != cudaSuccess) return e;
         if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
         return cudaStreamWaitEvent(stream, ss->join, 0);
     }
     if (num_decodes > 0) {
-        cudaError_t e = launch_recurrent(p, K, V, 2, 1, cu, 0, num_decodes, stream);
+        cudaError_t e = launch_decode(p, K, V, cu_host[0], num_decodes, stream);
         if (e != cudaSuccess) return e;
     }
     return launch_chunk_prefill(p, K, V, cu, cu_host, num_decodes, num_prefills, 64, workspace, 0, stream);

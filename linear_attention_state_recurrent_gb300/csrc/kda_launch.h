@@ -17,6 +17,11 @@ cudaError_t launch_gate(const Params &p, int K, int64_t N, float *g_out, float *
 cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
                              int64_t entry_base, int64_t num_entries, cudaStream_t stream);
 
+// Single-token decode: entries 0 .. num_entries - 1 (their slots), entry e at row
+// row_base + e.
+cudaError_t launch_decode(const Params &p, int K, int V, int64_t row_base, int64_t num_entries,
+                          cudaStream_t stream);
+
 // Spec-verify: T consecutive rows per request.
 cudaError_t launch_spec(const Params &p, int K, int V, int T, int64_t num_reqs, cudaStream_t stream);
 constexpr int kSpecCkptMaxT = 16;   // longest request the checkpointing verify kernel takes

@@ -58,11 +58,10 @@ __global__ void __launch_bounds__(256) gate_kernel(Params p, int K, int64_t N, f
 // ---------------------------------------------------------------------------
 enum RowMode { kRowsDecode = 0, kRowsSpec = 1, kRowsVarlen = 2 };
 
-// 8 CTAs per SM (64 registers per thread): the decode is bound by how many state bytes
-// are in flight, and at 8 resident CTAs each SM keeps 128 KiB of loads outstanding.
-// ONE: every entry is a single token (decode mode), so nothing is reused across tokens
-// and s_k needs no second buffer.
-template <int K, int V, bool ONE>
+// 8 CTAs per SM (64 registers per thread): the multi-token modes are bound by how many
+// state bytes are in flight, and at 8 resident CTAs each SM keeps 128 KiB of loads
+// outstanding. (The single-token decode runs decode_kernel below.)
+template <int K, int V>
 __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, int T,
                                                         const int32_t *cu, int64_t entry_base)
 {
@@ -74,7 +73,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     // s_k is read again in [C], after the second barrier, so it alternates between two
     // buffers by token parity: token t+1's [A] may run while slower warps are still in
     // token t's [C]. The other arrays are last read before the second barrier.
-    __shared__ float s_a[K], s_k[ONE ? 1 : 2][K], s_q[K];
+    __shared__ float s_a[K], s_k[2][K], s_q[K];
     __shared__ float s_part[KW][3];
     __shared__ float s_red[4][2][VT];
 
@@ -145,7 +144,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
     if (row0 < row1) fetch(row0);
 
     for (int64_t t = row0; t < row1; t++) {
-        const int kb = ONE ? 0 : static_cast<int>((t - row0) & 1);
+        const int kb = static_cast<int>((t - row0) & 1);
         // ---- [A] gate + stash ----
         const float4 v = nv;
         const float beta = sigmoid_f(nb);
@@ -220,6 +219,152 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 #pragma unroll
         for (int i = 0; i < RPT; i++)
             *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V + j0) = S[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Packed decode: one token per entry, the state slice in shared memory.
+//
+// recurrent_kernel's thread layout and phases for one token, with the slice (K rows x 32
+// columns, 16 KiB at K = 128) copied by cp.async into shared memory and kept there: each
+// thread copies, decays (writing back), reads again and stores the same RPT float4, so the
+// slice needs no barrier of its own. No register holds the tile (40 registers a thread),
+// and shared memory sets how many CTAs an SM keeps: 11 at K = 128 (176 KiB of state loads
+// in flight), where the register-resident tile allowed 8 (128 KiB).
+// ---------------------------------------------------------------------------
+template <int K, int V>
+__global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_base, int64_t row_base)
+{
+    constexpr int VT = 32;              // value columns per CTA
+    constexpr int VS = V / VT;          // V slices per (entry, head)
+    constexpr int RPT = K / 16;         // rows per thread
+    constexpr int KW = K / 32;          // warps that own channels in [A]
+
+    __shared__ __align__(16) float4 s_tile[RPT][128];   // [row step][thread]
+    __shared__ float s_a[K], s_k[K], s_q[K];
+    __shared__ float s_part[KW][3];
+    __shared__ float s_red[4][2][VT];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int cg = tid & 7;
+    const int rg = tid >> 3;
+
+    pdl_wait_then_release();   // launched by launch_pdl: no global read before this
+
+    const int64_t b = blockIdx.x;
+    const int vs = static_cast<int>(b % VS);
+    const int h = static_cast<int>((b / VS) % p.H);
+    const int64_t ei = b / (static_cast<int64_t>(VS) * p.H);
+    const int64_t e = ei + entry_base, t = ei + row_base;   // entry (its slot) and row
+    const int j0 = vs * VT + cg * 4;                    // first of this thread's 4 columns
+    const int64_t slot = load_slot(p, e);
+    uint16_t *orow = p.out + t * p.ld_out + static_cast<int64_t>(h) * V + j0;
+
+    if (slot >= p.num_slots) {                          // out of range: flag, zero outputs
+        if (tid == 0 && p.err) atomicOr(p.err, kErrSlotRange);
+        if (rg == 0) *reinterpret_cast<uint2 *>(orow) = make_uint2(0u, 0u);
+        return;
+    }
+    const bool has_state = slot >= 0;
+    const bool writable = has_state && slot != p.null_slot;
+    float *tile = has_state ? p.pool + slot * p.slot_stride + static_cast<int64_t>(h) * K * V + j0 : nullptr;
+
+    // the state copies first, so they are in flight during the gate math
+    if (has_state) {
+#pragma unroll
+        for (int i = 0; i < RPT; i++)
+            cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&s_tile[i][tid])),
+                       tile + static_cast<int64_t>(rg + 16 * i) * V, true);
+    }
+    cp_async_commit();
+
+    const bool chan = tid < K;
+    const int64_t HK = static_cast<int64_t>(p.H) * K;
+    const uint16_t *row = p.qkv + t * p.ld_qkv;
+    float q = 0.f, k = 0.f, gr = 0.f, dtb = 0.f;
+    if (chan) {
+        q = bf16_to_f32(row[h * K + tid]);
+        k = bf16_to_f32(row[HK + h * K + tid]);
+        gr = bf16_to_f32(p.rg[t * p.ld_g + h * K + tid]);
+        if (p.dt_bias) dtb = __ldg(p.dt_bias + h * K + tid);
+    }
+    const uint16_t *vp = row + 2 * HK + static_cast<int64_t>(h) * V + j0;
+    const float vv[4] = {bf16_to_f32(vp[0]), bf16_to_f32(vp[1]), bf16_to_f32(vp[2]), bf16_to_f32(vp[3])};
+    const float beta = sigmoid_f(bf16_to_f32(p.rb[t * p.ld_beta + h]));
+    const float expA = expf(__ldg(p.A_log + h));
+
+    // ---- [A] gate + stash ----
+    if (chan) {
+        const float g = gate_log_decay(gr + dtb, expA, p.has_lb, p.lb);
+        s_a[tid] = expf(g);
+        s_k[tid] = k;
+        s_q[tid] = q;
+        const float qq = warp_sum(q * q), kk = warp_sum(k * k), qk = warp_sum(q * k);
+        if (lane == 0) { s_part[warp][0] = qq; s_part[warp][1] = kk; s_part[warp][2] = qk; }
+    }
+    cp_async_wait_all();   // this thread's own copies
+    __syncthreads();
+
+    // ---- [B] decay (written back) + partial reductions ----
+    float qq = 0.f, kk = 0.f, qk = 0.f;
+#pragma unroll
+    for (int w = 0; w < KW; w++) { qq += s_part[w][0]; kk += s_part[w][1]; qk += s_part[w][2]; }
+    const float rq = p.scale * rsqrtf(qq + p.eps);
+    const float rk = rsqrtf(kk + p.eps);
+    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < RPT; i++) {
+        const int r = rg + 16 * i;
+        const float a = s_a[r], kr = s_k[r], qr = s_q[r];
+        float4 S = has_state ? s_tile[i][tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+        S.x *= a; S.y *= a; S.z *= a; S.w *= a;
+        s_tile[i][tid] = S;
+        pk[0] += kr * S.x; pk[1] += kr * S.y; pk[2] += kr * S.z; pk[3] += kr * S.w;
+        pq[0] += qr * S.x; pq[1] += qr * S.y; pq[2] += qr * S.z; pq[3] += qr * S.w;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++) {
+        pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 8);
+        pk[jj] += __shfl_xor_sync(0xffffffffu, pk[jj], 16);
+        pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 8);
+        pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 16);
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            s_red[warp][0][cg * 4 + jj] = pk[jj];
+            s_red[warp][1][cg * 4 + jj] = pq[jj];
+        }
+    }
+    __syncthreads();
+
+    // ---- [C] u, o, rank-1 update, stores ----
+    float u[4], o[4];
+    const float qkh = qk * rq * rk;
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++) {
+        const int c = cg * 4 + jj;
+        const float ks = (s_red[0][0][c] + s_red[1][0][c] + s_red[2][0][c] + s_red[3][0][c]) * rk;
+        const float qs = (s_red[0][1][c] + s_red[1][1][c] + s_red[2][1][c] + s_red[3][1][c]) * rq;
+        u[jj] = beta * (vv[jj] - ks);
+        o[jj] = qs + qkh * u[jj];
+    }
+    if (rg == 0) {
+        uint2 packed;
+        packed.x = static_cast<uint32_t>(f32_to_bf16(o[0])) | (static_cast<uint32_t>(f32_to_bf16(o[1])) << 16);
+        packed.y = static_cast<uint32_t>(f32_to_bf16(o[2])) | (static_cast<uint32_t>(f32_to_bf16(o[3])) << 16);
+        *reinterpret_cast<uint2 *>(orow) = packed;
+    }
+    if (writable) {
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const float kh = s_k[rg + 16 * i] * rk;
+            float4 S = s_tile[i][tid];
+            S.x += kh * u[0]; S.y += kh * u[1]; S.z += kh * u[2]; S.w += kh * u[3];
+            *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V) = S;
+        }
     }
 }
 
@@ -478,9 +623,29 @@ static cudaError_t launch_rec_kv(const Params &p, int mode, int T, const int32_t
 {
     const int64_t grid = num_entries * p.H * (V / 32);
     const dim3 g(static_cast<unsigned>(grid)), blk(128);
-    if (mode == kRowsDecode)
-        return launch_pdl(recurrent_kernel<K, V, true>, g, blk, 0, stream, p, mode, T, cu, entry_base);
-    return launch_pdl(recurrent_kernel<K, V, false>, g, blk, 0, stream, p, mode, T, cu, entry_base);
+    if (mode == kRowsDecode)   // row e for entry e
+        return launch_pdl(decode_kernel<K, V>, g, blk, 0, stream, p, entry_base, entry_base);
+    return launch_pdl(recurrent_kernel<K, V>, g, blk, 0, stream, p, mode, T, cu, entry_base);
+}
+
+template <int K, int V>
+static cudaError_t launch_dec_kv(const Params &p, int64_t row_base, int64_t num_entries, cudaStream_t stream)
+{
+    const dim3 g(static_cast<unsigned>(num_entries * p.H * (V / 32))), blk(128);
+    return launch_pdl(decode_kernel<K, V>, g, blk, 0, stream, p, static_cast<int64_t>(0), row_base);
+}
+
+cudaError_t launch_decode(const Params &p, int K, int V, int64_t row_base, int64_t num_entries,
+                          cudaStream_t stream)
+{
+    if (num_entries <= 0) return cudaSuccess;
+#define KDA_DEC_CASE(KK, VV) \
+    if (K == KK && V == VV) return launch_dec_kv<KK, VV>(p, row_base, num_entries, stream);
+    KDA_DEC_CASE(32, 32) KDA_DEC_CASE(32, 64) KDA_DEC_CASE(32, 128)
+    KDA_DEC_CASE(64, 32) KDA_DEC_CASE(64, 64) KDA_DEC_CASE(64, 128)
+    KDA_DEC_CASE(128, 32) KDA_DEC_CASE(128, 64) KDA_DEC_CASE(128, 128)
+#undef KDA_DEC_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_recurrent(const Params &p, int K, int V, int mode, int T, const int32_t *cu,
