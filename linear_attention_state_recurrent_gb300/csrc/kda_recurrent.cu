@@ -227,8 +227,9 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 //
 // recurrent_kernel's thread layout and phases for one token, with the slice (K rows x 32
 // columns, 16 KiB at K = 128) copied by cp.async into shared memory and kept there: each
-// thread copies, decays (writing back), reads again and stores the same RPT float4, so the
-// slice needs no barrier of its own. No register holds the tile (40 registers a thread),
+// thread copies, reads twice (the reductions, with the decay folded into k and q, then the
+// update) and stores the same RPT float4, so the slice needs no barrier of its own and is
+// never written back. No register holds the tile (40 registers a thread),
 // and shared memory sets how many CTAs an SM keeps: 11 at K = 128 (176 KiB of state loads
 // in flight), where the register-resident tile allowed 8 (128 KiB).
 // ---------------------------------------------------------------------------
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
     cp_async_wait_all();   // this thread's own copies
     __syncthreads();
 
-    // ---- [B] decay (written back) + partial reductions ----
+    // ---- [B] partial reductions over the decayed state (k alpha)^T S, (q alpha)^T S ----
     float qq = 0.f, kk = 0.f, qk = 0.f;
 #pragma unroll
     for (int w = 0; w < KW; w++) { qq += s_part[w][0]; kk += s_part[w][1]; qk += s_part[w][2]; }
@@ -317,10 +318,8 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
 #pragma unroll
     for (int i = 0; i < RPT; i++) {
         const int r = rg + 16 * i;
-        const float a = s_a[r], kr = s_k[r], qr = s_q[r];
-        float4 S = has_state ? s_tile[i][tid] : make_float4(0.f, 0.f, 0.f, 0.f);
-        S.x *= a; S.y *= a; S.z *= a; S.w *= a;
-        s_tile[i][tid] = S;
+        const float a = s_a[r], kr = s_k[r] * a, qr = s_q[r] * a;
+        const float4 S = has_state ? s_tile[i][tid] : make_float4(0.f, 0.f, 0.f, 0.f);
         pk[0] += kr * S.x; pk[1] += kr * S.y; pk[2] += kr * S.z; pk[3] += kr * S.w;
         pq[0] += qr * S.x; pq[1] += qr * S.y; pq[2] += qr * S.z; pq[3] += qr * S.w;
     }
@@ -340,7 +339,7 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
     }
     __syncthreads();
 
-    // ---- [C] u, o, rank-1 update, stores ----
+    // ---- [C] u, o, S <- Diag(alpha) S + k^ u^T, stores ----
     float u[4], o[4];
     const float qkh = qk * rq * rk;
 #pragma unroll
@@ -360,10 +359,12 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
     if (writable) {
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
-            const float kh = s_k[rg + 16 * i] * rk;
+            const int r = rg + 16 * i;
+            const float a = s_a[r], kh = s_k[r] * rk;
             float4 S = s_tile[i][tid];
-            S.x += kh * u[0]; S.y += kh * u[1]; S.z += kh * u[2]; S.w += kh * u[3];
-            *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(rg + 16 * i) * V) = S;
+            S.x = fmaf(S.x, a, kh * u[0]); S.y = fmaf(S.y, a, kh * u[1]);
+            S.z = fmaf(S.z, a, kh * u[2]); S.w = fmaf(S.w, a, kh * u[3]);
+            *reinterpret_cast<float4 *>(tile + static_cast<int64_t>(r) * V) = S;
         }
     }
 }
