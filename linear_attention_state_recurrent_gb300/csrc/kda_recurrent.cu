@@ -234,16 +234,19 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 // in flight), where the register-resident tile allowed 8 (128 KiB).
 // ---------------------------------------------------------------------------
 template <int K, int V>
-__global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_base, int64_t row_base)
+__global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p, int64_t entry_base, int64_t row_base)
 {
     constexpr int VT = 32;              // value columns per CTA
     constexpr int VS = V / VT;          // V slices per (entry, head)
     constexpr int RPT = K / 16;         // rows per thread
-    constexpr int KW = K / 32;          // warps that own channels in [A]
+    constexpr int CPL = K / 32;         // channels per lane in the norms
 
+    // 18,432 bytes at K = 128: twelve CTAs fill an SM's 228 KiB (with the 1 KiB each
+    // reserves). q and k stay in bf16 (their input type: exact); every warp forms the norms
+    // itself, so no exchange array is needed for them.
     __shared__ __align__(16) float4 s_tile[RPT][128];   // [row step][thread]
-    __shared__ float s_a[K], s_k[K], s_q[K];
-    __shared__ float s_part[KW][3];
+    __shared__ float s_a[K];
+    __shared__ uint16_t s_k[K], s_q[K];
     __shared__ float s_red[4][2][VT];
 
     const int tid = threadIdx.x;
@@ -284,10 +287,16 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
     const bool chan = tid < K;
     const int64_t HK = static_cast<int64_t>(p.H) * K;
     const uint16_t *row = p.qkv + t * p.ld_qkv;
-    float q = 0.f, k = 0.f, gr = 0.f, dtb = 0.f;
+    // channels lane + 32 c of q and k (every warp: the norms); this thread's own channel is
+    // the one with c == warp
+    uint16_t qb[CPL], kb[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; c++) {
+        qb[c] = row[h * K + lane + 32 * c];
+        kb[c] = row[HK + h * K + lane + 32 * c];
+    }
+    float gr = 0.f, dtb = 0.f;
     if (chan) {
-        q = bf16_to_f32(row[h * K + tid]);
-        k = bf16_to_f32(row[HK + h * K + tid]);
         gr = bf16_to_f32(p.rg[t * p.ld_g + h * K + tid]);
         if (p.dt_bias) dtb = __ldg(p.dt_bias + h * K + tid);
     }
@@ -300,25 +309,30 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
     if (chan) {
         const float g = gate_log_decay(gr + dtb, expA, p.has_lb, p.lb);
         s_a[tid] = expf(g);
-        s_k[tid] = k;
-        s_q[tid] = q;
-        const float qq = warp_sum(q * q), kk = warp_sum(k * k), qk = warp_sum(q * k);
-        if (lane == 0) { s_part[warp][0] = qq; s_part[warp][1] = kk; s_part[warp][2] = qk; }
+#pragma unroll
+        for (int c = 0; c < CPL; c++)
+            if (c == warp) { s_k[tid] = kb[c]; s_q[tid] = qb[c]; }
     }
+    float qq = 0.f, kk = 0.f, qk = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; c++) {
+        const float qf = bf16_to_f32(qb[c]), kf = bf16_to_f32(kb[c]);
+        qq += qf * qf; kk += kf * kf; qk += qf * kf;
+    }
+    qq = warp_sum(qq);
+    kk = warp_sum(kk);
+    qk = warp_sum(qk);
     cp_async_wait_all();   // this thread's own copies
     __syncthreads();
 
     // ---- [B] partial reductions over the decayed state (k alpha)^T S, (q alpha)^T S ----
-    float qq = 0.f, kk = 0.f, qk = 0.f;
-#pragma unroll
-    for (int w = 0; w < KW; w++) { qq += s_part[w][0]; kk += s_part[w][1]; qk += s_part[w][2]; }
     const float rq = p.scale * rsqrtf(qq + p.eps);
     const float rk = rsqrtf(kk + p.eps);
     float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < RPT; i++) {
         const int r = rg + 16 * i;
-        const float a = s_a[r], kr = s_k[r] * a, qr = s_q[r] * a;
+        const float a = s_a[r], kr = bf16_to_f32(s_k[r]) * a, qr = bf16_to_f32(s_q[r]) * a;
         const float4 S = has_state ? s_tile[i][tid] : make_float4(0.f, 0.f, 0.f, 0.f);
         pk[0] += kr * S.x; pk[1] += kr * S.y; pk[2] += kr * S.z; pk[3] += kr * S.w;
         pq[0] += qr * S.x; pq[1] += qr * S.y; pq[2] += qr * S.z; pq[3] += qr * S.w;
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(128) decode_kernel(Params p, int64_t entry_bas
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + 16 * i;
-            const float a = s_a[r], kh = s_k[r] * rk;
+            const float a = s_a[r], kh = bf16_to_f32(s_k[r]) * rk;
             float4 S = s_tile[i][tid];
             S.x = fmaf(S.x, a, kh * u[0]); S.y = fmaf(S.y, a, kh * u[1]);
             S.z = fmaf(S.z, a, kh * u[2]); S.w = fmaf(S.w, a, kh * u[3]);
