@@ -242,11 +242,11 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
     constexpr int CPL = K / 32;         // channels per lane in the norms
 
     // 18,432 bytes at K = 128: twelve CTAs fill an SM's 228 KiB (with the 1 KiB each
-    // reserves). q and k stay in bf16 (their input type: exact); every warp forms the norms
-    // itself, so no exchange array is needed for them.
+    // reserves). k and q stay in bf16 (their input type: exact), one word per channel; every
+    // warp forms the norms itself, so no exchange array is needed for them.
     __shared__ __align__(16) float4 s_tile[RPT][128];   // [row step][thread]
     __shared__ float s_a[K];
-    __shared__ uint16_t s_k[K], s_q[K];
+    __shared__ uint32_t s_kq[K];   // bf16 k (low half) and q (high half) of each channel
     __shared__ float s_red[4][2][VT];
 
     const int tid = threadIdx.x;
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
         s_a[tid] = expf(g);
 #pragma unroll
         for (int c = 0; c < CPL; c++)
-            if (c == warp) { s_k[tid] = kb[c]; s_q[tid] = qb[c]; }
+            if (c == warp) s_kq[tid] = static_cast<uint32_t>(kb[c]) | (static_cast<uint32_t>(qb[c]) << 16);
     }
     float qq = 0.f, kk = 0.f, qk = 0.f;
 #pragma unroll
@@ -332,7 +332,8 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
 #pragma unroll
     for (int i = 0; i < RPT; i++) {
         const int r = rg + 16 * i;
-        const float a = s_a[r], kr = bf16_to_f32(s_k[r]) * a, qr = bf16_to_f32(s_q[r]) * a;
+        const uint32_t kq = s_kq[r];
+        const float a = s_a[r], kr = __uint_as_float(kq << 16) * a, qr = __uint_as_float(kq & 0xffff0000u) * a;
         const float4 S = has_state ? s_tile[i][tid] : make_float4(0.f, 0.f, 0.f, 0.f);
         pk[0] += kr * S.x; pk[1] += kr * S.y; pk[2] += kr * S.z; pk[3] += kr * S.w;
         pq[0] += qr * S.x; pq[1] += qr * S.y; pq[2] += qr * S.z; pq[3] += qr * S.w;
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + 16 * i;
-            const float a = s_a[r], kh = bf16_to_f32(s_k[r]) * rk;
+            const float a = s_a[r], kh = __uint_as_float(s_kq[r] << 16) * rk;
             float4 S = s_tile[i][tid];
             S.x = fmaf(S.x, a, kh * u[0]); S.y = fmaf(S.y, a, kh * u[1]);
             S.z = fmaf(S.z, a, kh * u[2]); S.w = fmaf(S.w, a, kh * u[3]);
