@@ -4,9 +4,11 @@
 // One CTA owns one (entry, head, 32-wide V slice) state tile. The value columns
 // of S are independent in the update (column j of S_t depends only on column j
 // of S_{t-1}; the coupling is only through the K-reductions k^T S and q^T S), so
-// a K x V tile splits along V with no communication. The tile lives in registers
-// for the whole call: loaded once with 128-bit coalesced loads, advanced over the
-// entry's tokens, stored once. Gate, beta and the q/k L2 norms are fused in.
+// a K x V tile splits along V with no communication. The tile is loaded once with
+// 128-bit coalesced accesses, advanced over the entry's tokens and stored once: in
+// registers for the multi-token modes (recurrent_kernel), in shared memory for the
+// single-token decode (decode_kernel), where no register then holds it and more CTAs fit
+// on an SM. Gate, beta and the q/k L2 norms are fused in.
 #include "kda_common.cuh"
 #include "kda_launch.h"
 #include "kda_pdl.cuh"
