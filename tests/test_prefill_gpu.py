@@ -149,6 +149,31 @@ def test_mixed_batch_config(kda):
     _run(kda, w, "mixed batch", heads=(0, 32))
 
 
+def test_mixed_batch_rows_after_an_offset(kda):
+    """cu_seqlens starting at row 3: three leading rows that no sequence covers (filled with
+    other values). The decodes read rows cu_seqlens[0] + d and the prefills their own rows;
+    results equal the oracle's on the unshifted batch, and the leading output rows keep
+    what they held."""
+    off = 3
+    lengths = [1] * 5 + [130, 64, 1, 70]
+    w = wl.varlen_case(lengths, 2, 128, 128, seed=79, index_stride=2, num_decodes=5, kind="mixed")
+    dw = hx.DeviceWorkload(w)
+    ref = ko.run(w)
+
+    def shifted(t):   # off rows of other values (the batch's last rows, reversed) in front
+        return torch.cat([t[-off:].flip(0), t]).contiguous()
+    mq, rg, rb = shifted(dw.mixed_qkv), shifted(dw.raw_g), shifted(dw.raw_beta)
+    cu_h = torch.from_numpy(w.cu_seqlens + off)
+    out = torch.full((w.N + off, w.H * w.V), 1.0, dtype=torch.bfloat16, device=dw.device)
+    kda.kda_mixed_batch(mq, rg, rb, dw.A_log, dw.dt_bias, w.lower_bound, dw.pool_view(),
+                        dw.indices_view(), cu_h.to(dw.device), w.num_decodes, cu_seqlens_host=cu_h,
+                        scale=w.scale, l2_eps=w.eps, null_slot=w.null_slot, out=out,
+                        err_flags=dw.err)
+    torch.cuda.synchronize()
+    assert torch.equal(out[:off], torch.full_like(out[:off], 1.0))
+    hx.check(dw, out[off:], ref, fp32_path=False, label="mixed batch after an offset")
+
+
 @pytest.mark.parametrize("lower_bound", [-5.0, None])
 @pytest.mark.parametrize("stride", [1, 8])
 def test_mixed_batch_matrix(kda, lower_bound, stride):
