@@ -244,12 +244,12 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
     constexpr int CPL = K / 32;         // channels per lane in the norms
 
     // 18,432 bytes at K = 128: twelve CTAs fill an SM's 228 KiB (with the 1 KiB each
-    // reserves). k and q stay in bf16 (their input type: exact), one word per channel; every
-    // warp forms the norms itself, so no exchange array is needed for them.
+    // reserves). k and q stay in bf16 (their input type: exact); every warp forms the norms
+    // itself, so no exchange array is needed for them. A row's alpha, k and q are one 8-byte
+    // read, a warp's four partial sums of a phase one 16-byte read.
     __shared__ __align__(16) float4 s_tile[RPT][128];   // [row step][thread]
-    __shared__ float s_a[K];
-    __shared__ uint32_t s_kq[K];   // bf16 k (low half) and q (high half) of each channel
-    __shared__ float s_red[4][2][VT];
+    __shared__ __align__(8) uint2 s_akq[K];   // per channel: alpha (fp32 bits), bf16 k | q << 16
+    __shared__ __align__(16) float4 s_red[4][2][VT / 4];   // [warp][k^T S, q^T S][column group]
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -310,10 +310,11 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
     // ---- [A] gate + stash ----
     if (chan) {
         const float g = gate_log_decay(gr + dtb, expA, p.has_lb, p.lb);
-        s_a[tid] = expf(g);
+        uint32_t kq = 0;
 #pragma unroll
         for (int c = 0; c < CPL; c++)
-            if (c == warp) s_kq[tid] = static_cast<uint32_t>(kb[c]) | (static_cast<uint32_t>(qb[c]) << 16);
+            if (c == warp) kq = static_cast<uint32_t>(kb[c]) | (static_cast<uint32_t>(qb[c]) << 16);
+        s_akq[tid] = make_uint2(__float_as_uint(expf(g)), kq);
     }
     float qq = 0.f, kk = 0.f, qk = 0.f;
 #pragma unroll
@@ -334,8 +335,9 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
 #pragma unroll
     for (int i = 0; i < RPT; i++) {
         const int r = rg + 16 * i;
-        const uint32_t kq = s_kq[r];
-        const float a = s_a[r], kr = __uint_as_float(kq << 16) * a, qr = __uint_as_float(kq & 0xffff0000u) * a;
+        const uint2 akq = s_akq[r];
+        const float a = __uint_as_float(akq.x);
+        const float kr = __uint_as_float(akq.y << 16) * a, qr = __uint_as_float(akq.y & 0xffff0000u) * a;
         const float4 S = has_state ? s_tile[i][tid] : make_float4(0.f, 0.f, 0.f, 0.f);
         pk[0] += kr * S.x; pk[1] += kr * S.y; pk[2] += kr * S.z; pk[3] += kr * S.w;
         pq[0] += qr * S.x; pq[1] += qr * S.y; pq[2] += qr * S.z; pq[3] += qr * S.w;
@@ -348,24 +350,27 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
         pq[jj] += __shfl_xor_sync(0xffffffffu, pq[jj], 16);
     }
     if (lane < 8) {
-#pragma unroll
-        for (int jj = 0; jj < 4; jj++) {
-            s_red[warp][0][cg * 4 + jj] = pk[jj];
-            s_red[warp][1][cg * 4 + jj] = pq[jj];
-        }
+        s_red[warp][0][cg] = make_float4(pk[0], pk[1], pk[2], pk[3]);
+        s_red[warp][1][cg] = make_float4(pq[0], pq[1], pq[2], pq[3]);
     }
     __syncthreads();
 
     // ---- [C] u, o, S <- Diag(alpha) S + k^ u^T, stores ----
     float u[4], o[4];
     const float qkh = qk * rq * rk;
+    {
+        float4 kw[4], qw[4];
 #pragma unroll
-    for (int jj = 0; jj < 4; jj++) {
-        const int c = cg * 4 + jj;
-        const float ks = (s_red[0][0][c] + s_red[1][0][c] + s_red[2][0][c] + s_red[3][0][c]) * rk;
-        const float qs = (s_red[0][1][c] + s_red[1][1][c] + s_red[2][1][c] + s_red[3][1][c]) * rq;
-        u[jj] = beta * (vv[jj] - ks);
-        o[jj] = qs + qkh * u[jj];
+        for (int w = 0; w < 4; w++) { kw[w] = s_red[w][0][cg]; qw[w] = s_red[w][1][cg]; }
+        const float ks[4] = {(kw[0].x + kw[1].x + kw[2].x + kw[3].x) * rk, (kw[0].y + kw[1].y + kw[2].y + kw[3].y) * rk,
+                             (kw[0].z + kw[1].z + kw[2].z + kw[3].z) * rk, (kw[0].w + kw[1].w + kw[2].w + kw[3].w) * rk};
+        const float qs[4] = {(qw[0].x + qw[1].x + qw[2].x + qw[3].x) * rq, (qw[0].y + qw[1].y + qw[2].y + qw[3].y) * rq,
+                             (qw[0].z + qw[1].z + qw[2].z + qw[3].z) * rq, (qw[0].w + qw[1].w + qw[2].w + qw[3].w) * rq};
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            u[jj] = beta * (vv[jj] - ks[jj]);
+            o[jj] = qs[jj] + qkh * u[jj];
+        }
     }
     if (rg == 0) {
         uint2 packed;
@@ -377,7 +382,8 @@ __global__ void __launch_bounds__(128, K == 128 ? 12 : 8) decode_kernel(Params p
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + 16 * i;
-            const float a = s_a[r], kh = __uint_as_float(s_kq[r] << 16) * rk;
+            const uint2 akq = s_akq[r];
+            const float a = __uint_as_float(akq.x), kh = __uint_as_float(akq.y << 16) * rk;
             float4 S = s_tile[i][tid];
             S.x = fmaf(S.x, a, kh * u[0]); S.y = fmaf(S.y, a, kh * u[1]);
             S.z = fmaf(S.z, a, kh * u[2]); S.w = fmaf(S.w, a, kh * u[3]);
