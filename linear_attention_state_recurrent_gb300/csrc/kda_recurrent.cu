@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(128, 8) recurrent_kernel(Params p, int mode, i
 // thread copies, reads twice (the reductions, with the decay folded into k and q, then the
 // update) and stores the same RPT float4, so the slice needs no barrier of its own and is
 // never written back. No register holds the tile (40 registers a thread),
-// and shared memory sets how many CTAs an SM keeps: 11 at K = 128 (176 KiB of state loads
+// and shared memory sets how many CTAs an SM keeps: 12 at K = 128 (192 KiB of state loads
 // in flight), where the register-resident tile allowed 8 (128 KiB).
 // ---------------------------------------------------------------------------
 template <int K, int V>
